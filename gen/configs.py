@@ -1,0 +1,58 @@
+"""The five synthetic workloads (shapes, value distributions, routing recipe).
+
+All weights are float32 ~N(0, 1/sqrt(fan_in)) quantised to FP8 E4M3 with
+128x128 power-of-two block scales; x is bf16 ~N(0, 1); seed 0.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+from . import routes
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    H: int
+    I: int
+    E: int
+    K: int
+    routing: str          # softmax_normal | softmax_uniform | block_perm | zipf
+    seed: int = 0
+
+    def with_tokens(self, T: int) -> "Workload":
+        return Workload(self.name, T, self.H, self.I, self.E, self.K, self.routing, self.seed)
+
+    @property
+    def routed_flops(self) -> int:
+        """6*T*K*H*I: FC1 (2*R*H*2I) + FC2 (2*R*I*H) with R = T*K routes."""
+        return 6 * self.T * self.K * self.H * self.I
+
+    def make_routes(self):
+        T, E, K, s = self.T, self.E, self.K, self.seed
+        if self.routing == "softmax_normal":
+            return routes.softmax_topk(T, E, K, s, "normal")
+        if self.routing == "softmax_uniform":
+            return routes.softmax_topk(T, E, K, s, "uniform")
+        if self.routing == "block_perm":
+            return routes.block_permutation(T, E, K, s)
+        if self.routing == "zipf":
+            return routes.zipf_skew(T, E, K, s)
+        raise ValueError(self.routing)
+
+
+TINY = Workload("tiny_T128_H512_I256_E8_K2", 128, 512, 256, 8, 2, "softmax_normal")
+V2LITE = Workload("dsv2lite_T4096_H2048_I1408_E64_K6", 4096, 2048, 1408, 64, 6, "softmax_uniform")
+V3_PREFILL = Workload("dsv3_prefill_T8192_H7168_I2048_E256_K8", 8192, 7168, 2048, 256, 8, "block_perm")
+V3_DECODE = Workload("dsv3_decode_H7168_I2048_E256_K8", 8, 7168, 2048, 256, 8, "softmax_normal")
+DECODE_TOKENS = (8, 64, 256, 1024)
+SKEW = Workload("skew_T16384_H4096_I1536_E128_K8", 16384, 4096, 1536, 128, 8, "zipf")
+
+WORKLOADS = {
+    "tiny": TINY,
+    "v2lite": V2LITE,
+    "v3prefill": V3_PREFILL,
+    **{f"v3decode{t}": V3_DECODE.with_tokens(t) for t in DECODE_TOKENS},
+    "skew": SKEW,
+}

@@ -1,0 +1,371 @@
+/*
+ * oracle.c -- plain CPU oracle of the single-GPU MoE layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py may load this file's library.
+ * It shares no code with the GPU path (no header, table or helper in common).
+ *
+ * What it computes (flashinfer PR #4069 "SM90 push FP8 mega-MoE backend",
+ * Description, the forward diagram: compact -> FC1 with SwiGLU + 1x128
+ * quantization -> FC2 -> combine with FP32 route reduction), restricted to one
+ * GPU, where dispatch is a local stable permute and combine a local reduce:
+ *
+ *   1. route    validate (expert id in [0,E) or -1, no duplicate active id
+ *               per token, finite weight on active routes); counts[E];
+ *               exclusive scan offsets[E+1]; stable counting sort of the
+ *               active routes by expert keyed by flat route id r = t*K + k
+ *               giving perm[pos] = r and inv[r] = pos (or -1 when masked).
+ *   2. quant    1x128 activation quantisation: per row and 128-column block,
+ *               s = the smallest power of two with amax <= 448*s (s = 1 when
+ *               amax = 0; the exponent is kept in [-127, 127], the range of
+ *               an E8M0 scale), q = E4M3FN round-to-nearest-even of v/s.
+ *   3. gather   A[pos] = xq[perm[pos] / K], As[pos] = xs[perm[pos] / K].
+ *   4. FC1      gu[pos, n] = BF16( sum_kb ( sum_{j in kb} dec(A)*dec(W1[e,n,j]) )
+ *                                          * As[pos,kb] * W1s[e, n/128, kb] ),
+ *               W1 rows [0, I) are the gate, [I, 2I) the up projection.
+ *   5. SwiGLU   h = float( g / (1 + exp(-g)) * u ), g, u the bf16 gu values.
+ *   6. requant  hq, hs = quant1x128(h) along I.
+ *   7. FC2      y[pos, c] = BF16( sum_kb (sum_j dec(hq)*dec(W2[e,c,j])) * hs * W2s ).
+ *   8. combine  out[t, c] = BF16( sum over active k, ascending, of
+ *                                 w[t,k] * y[inv[t*K+k], c] ); no route -> +0.
+ *
+ * Exactness: every E4M3 value is a multiple of 2^-9 with magnitude <= 448, so
+ * each product is a multiple of 2^-18 below 2^18 and every 128-term block sum
+ * is a multiple of 2^-18 below 2^25: at most 43 significant bits, exact in
+ * double in any order.  Scaling by powers of two is exact.  Only the final sum
+ * over the H/128 (or I/128) block terms rounds, at 2^-53 relative, before the
+ * one BF16 rounding.  Because block sums are exact, the compiler may evaluate
+ * them in any order (the simd pragma); no result changes.
+ *
+ * Readings where the pages are silent (listed with their reasons in the
+ * design notes): E4M3 is the OCP E4M3FN variant (max 448, NaN 0x7F/0xFF, no
+ * infinity); scales are powers of two; gate/up are rounded to BF16 before
+ * SwiGLU and h stays float into the re-quantisation; y is BF16; the sort is
+ * stable in flat route id; offsets are unpadded.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_ERR_ROUTE_RANGE 0x1u
+#define OR_ERR_ROUTE_DUP 0x2u
+#define OR_ERR_ROUTE_NONFINITE 0x4u
+
+/* ---------------------------------------------------------------------------
+ * Number formats, from their definitions.
+ * ------------------------------------------------------------------------- */
+
+/* OCP FP8 E4M3FN: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits.
+ * Exponent field 0 encodes subnormals m/8 * 2^-6; S.1111.111 is NaN; there is
+ * no infinity, so the largest finite value is 1.75 * 2^8 = 448. */
+double or_e4m3_decode(uint8_t code) {
+  int sign = code >> 7;
+  int ef = (code >> 3) & 0xF;
+  int m = code & 7;
+  double v;
+  if (ef == 15 && m == 7) return NAN;
+  if (ef == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, ef - 7);
+  return sign ? -v : v;
+}
+
+/* round a non-negative double to an integer, ties to even */
+static double round_half_even(double q) {
+  double f = floor(q);
+  double d = q - f;
+  if (d > 0.5) return f + 1.0;
+  if (d < 0.5) return f;
+  return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+}
+
+/* nearest E4M3FN code to v (ties to even mantissa), saturating to +-448.
+ * The sign is kept, so values that round to zero from below give 0x80. */
+uint8_t or_e4m3_encode(double v) {
+  uint8_t sign = (signbit(v) != 0) ? 0x80 : 0x00;
+  double a = fabs(v);
+  if (isnan(v)) return 0x7F;
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: multiples of 2^-9 */
+    double m = round_half_even(ldexp(a, 9)); /* 0..8; 8 is the smallest normal */
+    return sign | (uint8_t)m;
+  }
+  int ex;
+  frexp(a, &ex); /* a = f * 2^ex, f in [0.5, 1) */
+  int e = ex - 1; /* a in [2^e, 2^(e+1)) */
+  double m = round_half_even((ldexp(a, -e) - 1.0) * 8.0); /* 0..8 */
+  if (m == 8.0) {
+    m = 0.0;
+    e += 1;
+  }
+  int ef = e + 7;
+  if (ef > 15 || (ef == 15 && m == 7.0)) return sign | 0x7E;
+  return sign | (uint8_t)((ef << 3) | (int)m);
+}
+
+/* BF16: 1 sign, 8 exponent bits (bias 127), 7 mantissa bits; subnormals are
+ * multiples of 2^-133.  Round a double once, to nearest, ties to even. */
+uint16_t or_bf16_round(double v) {
+  uint16_t sign = (signbit(v) != 0) ? 0x8000 : 0x0000;
+  double a = fabs(v);
+  if (isnan(v)) return 0x7FC0;
+  if (isinf(v)) return sign | 0x7F80;
+  if (a == 0.0) return sign;
+  int ex;
+  frexp(a, &ex);
+  int e = ex - 1;              /* a in [2^e, 2^(e+1)) */
+  if (e < -126) e = -126;      /* subnormal: fixed quantum 2^-133 */
+  double m = round_half_even(ldexp(a, 7 - e)); /* significand in units of 2^(e-7) */
+  if (m >= 256.0) {
+    m = 128.0;
+    e += 1;
+  }
+  if (e > 127) return sign | 0x7F80; /* overflow to infinity */
+  if (m < 128.0) return sign | (uint16_t)m; /* subnormal (e == -126) */
+  return sign | (uint16_t)(((e + 127) << 7) | ((int)m - 128));
+}
+
+double or_bf16_decode(uint16_t b) {
+  union { uint32_t u; float f; } c;
+  c.u = (uint32_t)b << 16;
+  return (double)c.f;
+}
+
+/* smallest e with amax <= 448 * 2^e, kept in [-127, 127]; amax = 0 gives 0 */
+int or_pow2_scale_exp(double amax) {
+  if (!(amax > 0.0)) return 0;
+  int ex;
+  frexp(amax / 448.0, &ex); /* first guess, corrected by exact comparisons */
+  int e = ex;
+  while (448.0 * ldexp(1.0, e) < amax) e++;
+  while (e > -200 && 448.0 * ldexp(1.0, e - 1) >= amax) e--;
+  if (e < -127) e = -127;
+  if (e > 127) e = 127;
+  return e;
+}
+
+/* ---------------------------------------------------------------------------
+ * 1x128 quantisation of rows, and 128x128 quantisation of weight matrices.
+ * ------------------------------------------------------------------------- */
+
+/* v [rows, cols] (cols % 128 == 0) -> q [rows, cols], s [rows, cols/128] */
+void or_quant_rows(const double* v, int64_t rows, int64_t cols, uint8_t* q, float* s) {
+  int64_t nb = cols / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const double* src = v + r * cols + b * 128;
+      double amax = 0.0;
+      for (int j = 0; j < 128; ++j) amax = fmax(amax, fabs(src[j]));
+      int e = or_pow2_scale_exp(amax);
+      for (int j = 0; j < 128; ++j) q[r * cols + b * 128 + j] = or_e4m3_encode(ldexp(src[j], -e));
+      s[r * nb + b] = (float)ldexp(1.0, e);
+    }
+  }
+}
+
+/* bf16 rows -> 1x128 quantisation */
+void or_quant_rows_bf16(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* q, float* s) {
+  double* v = (double*)malloc(sizeof(double) * (size_t)(rows * cols));
+  for (int64_t i = 0; i < rows * cols; ++i) v[i] = or_bf16_decode(x[i]);
+  or_quant_rows(v, rows, cols, q, s);
+  free(v);
+}
+
+/* w [nmat, rows, cols] float -> q (same shape), s [nmat, rows/128, cols/128] */
+void or_quant_weights(const float* w, int64_t nmat, int64_t rows, int64_t cols, uint8_t* q,
+                      float* s) {
+  int64_t rb = rows / 128, cb = cols / 128;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t m = 0; m < nmat; ++m) {
+    for (int64_t bi = 0; bi < rb; ++bi) {
+      for (int64_t bj = 0; bj < cb; ++bj) {
+        double amax = 0.0;
+        for (int64_t i = 0; i < 128; ++i)
+          for (int64_t j = 0; j < 128; ++j)
+            amax = fmax(amax, fabs((double)w[(m * rows + bi * 128 + i) * cols + bj * 128 + j]));
+        int e = or_pow2_scale_exp(amax);
+        for (int64_t i = 0; i < 128; ++i)
+          for (int64_t j = 0; j < 128; ++j) {
+            int64_t o = (m * rows + bi * 128 + i) * cols + bj * 128 + j;
+            q[o] = or_e4m3_encode(ldexp((double)w[o], -e));
+          }
+        s[(m * rb + bi) * cb + bj] = (float)ldexp(1.0, e);
+      }
+    }
+  }
+}
+
+/* ---------------------------------------------------------------------------
+ * Routing: validation, histogram, exclusive scan, stable scatter.
+ * ------------------------------------------------------------------------- */
+
+/* Returns the error bits.  Routes whose id is out of range are flagged and
+ * then treated as masked; duplicates are flagged and kept. */
+uint32_t or_route(int64_t T, int K, int E, const int32_t* idx, const float* w, int check,
+                  int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv) {
+  uint32_t err = 0;
+  for (int64_t t = 0; t < T; ++t) {
+    for (int k = 0; k < K; ++k) {
+      int32_t id = idx[t * K + k];
+      if (id == -1) continue;
+      if (id < 0 || id >= E) {
+        err |= OR_ERR_ROUTE_RANGE;
+        continue;
+      }
+      if (check) {
+        for (int k2 = 0; k2 < k; ++k2)
+          if (idx[t * K + k2] == id) err |= OR_ERR_ROUTE_DUP;
+        if (!isfinite(w[t * K + k])) err |= OR_ERR_ROUTE_NONFINITE;
+      }
+    }
+  }
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (int64_t r = 0; r < T * K; ++r)
+    if (idx[r] >= 0 && idx[r] < E) counts[idx[r]]++;
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  int32_t* cursor = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+  for (int64_t r = 0; r < T * K; ++r) {
+    int32_t id = idx[r];
+    if (id >= 0 && id < E) {
+      int32_t pos = offsets[id] + cursor[id]++;
+      perm[pos] = (int32_t)r;
+      inv[r] = pos;
+    } else {
+      inv[r] = -1;
+    }
+  }
+  free(cursor);
+  return err;
+}
+
+/* ---------------------------------------------------------------------------
+ * One FP8 block-scaled row-times-matrix product: for row a (len K, scales
+ * as[K/128]) and matrix W [N, K] with block scales ws [N/128, K/128],
+ * out[n] = BF16( sum_kb blocksum(kb) * as[kb] * ws[n/128, kb] ).
+ * ------------------------------------------------------------------------- */
+static void fp8_row_matmul(const double* a, const float* as, const double* Wd, const float* ws,
+                           int64_t N, int64_t Kd, uint16_t* out) {
+  int64_t kbn = Kd / 128;
+  for (int64_t n = 0; n < N; ++n) {
+    double acc = 0.0;
+    for (int64_t kb = 0; kb < kbn; ++kb) {
+      const double* ar = a + kb * 128;
+      const double* wr = Wd + n * Kd + kb * 128;
+      double bs = 0.0;
+#pragma omp simd reduction(+ : bs)
+      for (int j = 0; j < 128; ++j) bs += ar[j] * wr[j];
+      acc += bs * (double)as[kb] * (double)ws[(n / 128) * kbn + kb];
+    }
+    out[n] = or_bf16_round(acc);
+  }
+}
+
+static void decode_e4m3_array(const uint8_t* q, int64_t n, double* out) {
+  double table[256];
+  for (int c = 0; c < 256; ++c) table[c] = or_e4m3_decode((uint8_t)c);
+  for (int64_t i = 0; i < n; ++i) out[i] = table[q[i]];
+}
+
+/* SwiGLU of one bf16 gate/up pair, rounded once to float */
+float or_swiglu(uint16_t g_bits, uint16_t u_bits) {
+  double g = or_bf16_decode(g_bits), u = or_bf16_decode(u_bits);
+  return (float)(g / (1.0 + exp(-g)) * u);
+}
+
+/* ---------------------------------------------------------------------------
+ * The expert FFN of one sorted position: A row -> gu -> h -> hq/hs -> y.
+ * Positions are processed expert by expert so each expert's weights are
+ * decoded once.  `sel` (nullable) marks which positions to compute.
+ * ------------------------------------------------------------------------- */
+void or_expert_ffn(int H, int I, int E, const int32_t* offsets, const uint8_t* A, const float* As,
+                   const uint8_t* W1, const float* W1s, const uint8_t* W2, const float* W2s,
+                   const uint8_t* sel, uint16_t* gu, uint8_t* hq, float* hs, uint16_t* y) {
+  const int64_t HB = H / 128, IB = I / 128;
+  double* w1d = (double*)malloc(sizeof(double) * (size_t)(2 * I) * (size_t)H);
+  double* w2d = (double*)malloc(sizeof(double) * (size_t)H * (size_t)I);
+  for (int e = 0; e < E; ++e) {
+    int64_t p0 = offsets[e], p1 = offsets[e + 1];
+    int any = 0;
+    for (int64_t p = p0; p < p1; ++p)
+      if (!sel || sel[p]) any = 1;
+    if (!any) continue;
+    decode_e4m3_array(W1 + (int64_t)e * 2 * I * H, (int64_t)2 * I * H, w1d);
+    decode_e4m3_array(W2 + (int64_t)e * H * I, (int64_t)H * I, w2d);
+    const float* w1s = W1s + (int64_t)e * (2 * I / 128) * HB;
+    const float* w2s = W2s + (int64_t)e * (H / 128) * IB;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t p = p0; p < p1; ++p) {
+      if (sel && !sel[p]) continue;
+      double* a = (double*)malloc(sizeof(double) * (size_t)H);
+      double* h = (double*)malloc(sizeof(double) * (size_t)I);
+      double* hd = (double*)malloc(sizeof(double) * (size_t)I);
+      uint16_t* gup = gu + p * 2 * I;
+      decode_e4m3_array(A + p * H, H, a);
+      fp8_row_matmul(a, As + p * HB, w1d, w1s, 2 * I, H, gup);
+      for (int n = 0; n < I; ++n) h[n] = (double)or_swiglu(gup[n], gup[I + n]);
+      or_quant_rows(h, 1, I, hq + p * I, hs + p * IB);
+      decode_e4m3_array(hq + p * I, I, hd);
+      fp8_row_matmul(hd, hs + p * IB, w2d, w2s, H, I, y + p * H);
+      free(a);
+      free(h);
+      free(hd);
+    }
+  }
+  free(w1d);
+  free(w2d);
+}
+
+/* combine: out[t, c] = BF16( sum_k active  w[t,k] * y[inv[t*K+k], c] ) */
+void or_combine(int64_t T, int K, int H, const int32_t* inv, const float* w, const uint16_t* y,
+                const uint8_t* tok_sel, uint16_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    if (tok_sel && !tok_sel[t]) continue;
+    for (int c = 0; c < H; ++c) {
+      double acc = 0.0;
+      for (int k = 0; k < K; ++k) {
+        int32_t p = inv[t * K + k];
+        if (p < 0) continue;
+        acc += (double)w[t * K + k] * or_bf16_decode(y[(int64_t)p * H + c]);
+      }
+      out[t * H + c] = or_bf16_round(acc);
+    }
+  }
+}
+
+/* ---------------------------------------------------------------------------
+ * The whole forward.  Intermediate outputs are optional (nullable) except the
+ * ones the caller needs; `tok_sel` (nullable) restricts the expert FFN and the
+ * combine to the selected tokens (routing always covers every token).
+ * Returns the route error bits; on error nothing past routing is computed.
+ * ------------------------------------------------------------------------- */
+uint32_t or_forward(int64_t T, int H, int I, int E, int K, int check, const uint16_t* x,
+                    const int32_t* idx, const float* w, const uint8_t* W1, const float* W1s,
+                    const uint8_t* W2, const float* W2s, const uint8_t* tok_sel,
+                    int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                    uint8_t* xq, float* xs, uint8_t* A, float* As, uint16_t* gu, uint8_t* hq,
+                    float* hs, uint16_t* y, uint16_t* out) {
+  uint32_t err = or_route(T, K, E, idx, w, check, counts, offsets, perm, inv);
+  if (err) return err;
+  const int64_t R = offsets[E], HB = H / 128;
+  or_quant_rows_bf16(x, T, H, xq, xs);
+  uint8_t* sel = NULL;
+  if (tok_sel) {
+    sel = (uint8_t*)calloc((size_t)(R > 0 ? R : 1), 1);
+    for (int64_t p = 0; p < R; ++p) sel[p] = tok_sel[perm[p] / K];
+  }
+  for (int64_t p = 0; p < R; ++p) {
+    int64_t t = perm[p] / K;
+    memcpy(A + p * H, xq + t * H, (size_t)H);
+    memcpy(As + p * HB, xs + t * HB, sizeof(float) * (size_t)HB);
+  }
+  or_expert_ffn(H, I, E, offsets, A, As, W1, W1s, W2, W2s, sel, gu, hq, hs, y);
+  or_combine(T, K, H, inv, w, y, tok_sel, out);
+  free(sel);
+  return 0;
+}
