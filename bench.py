@@ -1,0 +1,417 @@
+"""Benchmark of the single-GPU MoE layer forward (one JSON line on rank 0).
+
+A step is one whole forward -- routing, 1x128 FP8 quantisation + dispatch,
+FC1 with the fused SwiGLU/re-quantisation epilogue, FC2, combine -- over one
+batch of the workload, replayed from a CUDA graph.  L2 is flushed (a 256 MiB
+write, outside the timed span) before every timed step; each step is timed
+with CUDA events on the launching stream and the K step times are summed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain C, float64) as it stands on the
+host cores, on a bounded token sample of the same workload per step.
+Under torchrun (N > 1) every rank runs its own replica of the workload (no
+data-path collective: the layer does not shard on one-GPU machines); the time is
+the max over ranks and the value counts the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer routed TFLOPS & tokens/s on 1 GB300; % of FP8-peak/HBM roofline"
+KERNELS = ["status_reset", "route_count", "route_scan", "route_scatter", "quant_dispatch", "fc1",
+           "swiglu_quant", "fc2", "combine"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--config", default="v2lite")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--unfused", action="store_true", help="time the unfused reference path")
+    p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-tokens", type=int, default=0)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def algorithmic_bytes(wl, counts):
+    """compulsory HBM bytes of the layer: FP8 weights + scales of every expert
+    with at least one route, x read (bf16), out write (bf16), routes."""
+    touched = int((counts > 0).sum())
+    w = touched * (2 * wl.I * wl.H + wl.H * wl.I + (2 * wl.I // 128) * (wl.H // 128) * 4
+                   + (wl.H // 128) * (wl.I // 128) * 4)
+    io = wl.T * wl.H * 2 * 2 + wl.T * wl.K * 8
+    return w + io, touched
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    def __init__(self, index: int):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(wl, x_bits, idx, w, tokens):
+    """Times the oracle on the listed tokens (a mini-problem of those tokens and
+    the experts they route to); returns (seconds, routed FLOPs of the sample)."""
+    import oracle
+    from gen import problem
+    sub = idx[tokens]
+    experts = sorted(set(int(e) for e in sub.ravel() if e >= 0))
+    remap = {e: i for i, e in enumerate(experts)}
+    mini = np.vectorize(lambda e: remap.get(int(e), -1))(sub).astype(np.int32)
+    w1q, w1s = oracle.quant_weights(problem.w1_f32(wl, experts))
+    w2q, w2s = oracle.quant_weights(problem.w2_f32(wl, experts))
+    t0 = time.perf_counter()
+    r = oracle.forward(x_bits[tokens], mini, w[tokens], w1q, w1s, w2q, w2s)
+    dt = time.perf_counter() - t0
+    assert r["err"] == 0
+    routes = int((sub >= 0).sum())
+    return dt, 6 * routes * wl.H * wl.I
+
+
+def cpu_sample_tokens(wl, requested):
+    if requested:
+        return requested
+    # about 10-30 s of oracle work on a 16-core host
+    per_route = 6 * wl.H * wl.I
+    return max(8, min(wl.T, int(2.0e11 / (per_route * wl.K))))
+
+
+def run_reference(args):
+    from gen import configs, problem
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = configs.WORKLOADS[args.config]
+    x = problem.x_bits(wl)
+    idx, w = wl.make_routes()
+    n_tok = max(1, cpu_sample_tokens(wl, args.cpu_sample_tokens) // max(1, args.steps // 4))
+    rng = np.random.default_rng(0)
+    times, flops = [], []
+    for s in range(args.warmup + args.steps):
+        toks = np.sort(rng.choice(wl.T, size=min(n_tok, wl.T), replace=False))
+        dt, fl = oracle_sample(wl, x, idx, w, toks)
+        if s >= args.warmup:
+            times.append(dt)
+            flops.append(fl)
+    total = sum(times)
+    value = sum(flops) / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "sample_tokens_per_step": int(n_tok)},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"{n_tok} random tokens of {wl.name} per step (their experts' "
+                                   "FFN + combine; routing of the whole batch)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+
+    import __graft_entry__ as ge
+    ge.build()
+    import serving_route_gb300 as S
+    from gen import configs, problem
+    from gen import inputs as g
+
+    wl = configs.WORKLOADS[args.config]
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+    fused = not args.unfused
+
+    layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, expected_m=wl.T,
+                           fuse_fc1=fused, check_routes=True)
+    # weights: generated and quantised on the GPU, bound once
+    w1q = torch.empty((wl.E, 2 * wl.I, wl.H), dtype=torch.uint8, device=dev)
+    w1s = torch.empty((wl.E, 2 * wl.I // 128, wl.H // 128), dtype=torch.float32, device=dev)
+    w2q = torch.empty((wl.E, wl.H, wl.I), dtype=torch.uint8, device=dev)
+    w2s = torch.empty((wl.E, wl.H // 128, wl.I // 128), dtype=torch.float32, device=dev)
+    chunk = 16
+    with torch.cuda.stream(stream):
+        for e0 in range(0, wl.E, chunk):
+            ne = min(chunk, wl.E - e0)
+            f = torch.empty((ne, 2 * wl.I, wl.H), dtype=torch.float32, device=dev)
+            g.dev_normal_f32(wl.seed, g.STREAM_W1, e0 * 2 * wl.I * wl.H, f.numel(),
+                             g.weight_sigma(wl.H), f.data_ptr(), sp)
+            q, s = layer.quantize_weights(f, stream)
+            w1q[e0:e0 + ne].copy_(q)
+            w1s[e0:e0 + ne].copy_(s)
+            f = torch.empty((ne, wl.H, wl.I), dtype=torch.float32, device=dev)
+            g.dev_normal_f32(wl.seed, g.STREAM_W2, e0 * wl.H * wl.I, f.numel(),
+                             g.weight_sigma(wl.I), f.data_ptr(), sp)
+            q, s = layer.quantize_weights(f, stream)
+            w2q[e0:e0 + ne].copy_(q)
+            w2s[e0:e0 + ne].copy_(s)
+            del f, q, s
+        layer.bind_weights(w1q, w1s, w2q, w2s, stream)
+    del w1q, w1s, w2q, w2s
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    # inputs: x on the GPU from the device generator; routes from the host recipe
+    x = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
+    g.dev_normal_bf16(wl.seed, g.STREAM_X, 0, wl.T * wl.H, x.data_ptr(), sp)
+    idx_np, w_np = wl.make_routes()
+    idx = torch.from_numpy(idx_np).to(dev)
+    wts = torch.from_numpy(w_np).to(dev)
+    counts = np.bincount(idx_np.ravel()[idx_np.ravel() >= 0], minlength=wl.E)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+    layer.set_profile_events(ev)
+
+    def fwd():
+        layer.forward(x, idx, wts, stream=stream)
+
+    use_graph = not args.no_graph
+    graph = None
+    with torch.cuda.stream(stream):
+        fwd()
+    stream.synchronize()
+    st, bits = layer.read_status(stream)
+    if st != 0:
+        raise RuntimeError(f"forward reported device status {bits:#x}")
+    if use_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                fwd()
+            stream.synchronize()
+        except Exception as e:  # fall back to direct launches
+            print(f"# graph capture failed ({e}); timing direct launches", file=sys.stderr)
+            graph = None
+
+    def step():
+        if graph is not None:
+            with torch.cuda.stream(stream):
+                graph.replay()
+        else:
+            with torch.cuda.stream(stream):
+                fwd()
+
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+
+    def timed_steps(n, record):
+        tot = 0.0
+        per_kernel = {k: 0.0 for k in KERNELS}
+        for _ in range(n):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                t_start.record(stream)
+            step()
+            with torch.cuda.stream(stream):
+                t_end.record(stream)
+            stream.synchronize()
+            tot += t_start.elapsed_time(t_end)
+            if record:
+                for i, k in enumerate(KERNELS):
+                    per_kernel[k] += ev[i].elapsed_time(ev[i + 1])
+        return tot, per_kernel
+
+    timed_steps(args.warmup, False)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    total_ms, per_kernel = timed_steps(args.steps, True)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st, bits = layer.read_status(stream)
+    if st != 0:
+        raise RuntimeError(f"timed forwards reported device status {bits:#x}")
+
+    # ---------------------------------------------------------------- e2e
+    # the public call a user makes with host buffers: pinned H2D of x and the
+    # routes, the forward, D2H of the output; all inside the timed span
+    x_host = torch.from_numpy(problem.x_bits(wl).view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    idx_host = torch.from_numpy(idx_np).pin_memory()
+    w_host = torch.from_numpy(w_np).pin_memory()
+    out_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    idx_d = torch.empty_like(idx)
+    w_d = torch.empty_like(wts)
+    h2d = x_host.numel() * 2 + idx_host.numel() * 4 + w_host.numel() * 4
+    d2h = out_host.numel() * 2
+    layer.set_profile_events([])
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            x_d.copy_(x_host, non_blocking=True)
+            idx_d.copy_(idx_host, non_blocking=True)
+            w_d.copy_(w_host, non_blocking=True)
+            out = layer.forward(x_d, idx_d, w_d, stream=stream)
+            out_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    stream.synchronize()
+    e2e_ms = 0.0
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            t_start.record(stream)
+        e2e_step()
+        with torch.cuda.stream(stream):
+            t_end.record(stream)
+        stream.synchronize()
+        e2e_ms += t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    st, bits = layer.read_status(stream)
+    if st != 0:
+        raise RuntimeError(f"e2e forwards reported device status {bits:#x}")
+
+    # ---------------------------------------------------------------- report
+    K = args.steps
+    flops = wl.routed_flops
+    ms_step = total_ms / K
+    value = world * flops * K / (total_ms * 1e-3) / 1e12
+    e2e_value = world * flops * K / (e2e_ms * 1e-3) / 1e12
+    hbm, bf16, bf16_sus, src = peaks()
+    fp8_peak = 2.0 * bf16  # FP8 dense = 2x BF16 dense (nominal 4.5 vs 2.25 PFLOP/s)
+    b_alg, touched = algorithmic_bytes(wl, counts)
+    t_roof = max(flops / (fp8_peak * 1e12), b_alg / (hbm * 1e9))
+    kern_ms = {k: v / K for k, v in per_kernel.items()}
+    # dominant kernel: FC1 (fused epilogue), a dense FP8 contraction
+    R = int(counts.sum())
+    fc1_flops = 2 * R * wl.H * 2 * wl.I
+    fc1_ms = kern_ms["fc1"]
+    fc1_bytes = touched * (2 * wl.I * wl.H) + R * wl.H
+    fc1_ai = fc1_flops / fc1_bytes
+    ridge = fp8_peak * 1e12 / (hbm * 1e9)
+    if fc1_ai >= ridge:
+        roof = {"bound": "tensor", "achieved": fc1_flops / (fc1_ms * 1e-3) / 1e12, "peak": fp8_peak,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": fc1_bytes / (fc1_ms * 1e-3) / 1e9, "peak": hbm,
+                "unit": "GB/s"}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "kernel": "fc1",
+                 "peak_source": f"{src}: FP8 = 2 x bf16 burst" if roof["bound"] == "tensor"
+                 else f"{src}: hbm copy"})
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "K": wl.K,
+                   "fc1_epilogue": "fused" if fused else "unfused",
+                   "l2": "flushed before every step (256 MiB write, untimed)",
+                   "launch": "cuda graph replay" if graph is not None else "direct launches",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": world * wl.T * K / (total_ms * 1e-3),
+        "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
+                           "b_alg_bytes": b_alg, "experts_touched": touched,
+                           "fp8_peak_tflops": fp8_peak, "hbm_gbs": hbm, "source": src},
+        "roofline": roof,
+        "kernel_ms": kern_ms,
+        "gpu_launches": K * (7 if fused else 8),
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / K},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x_bits = x_host.view(torch.int16).numpy().view(np.uint16)
+        n = cpu_sample_tokens(wl, args.cpu_sample_tokens)
+        toks = np.sort(np.random.default_rng(0).choice(wl.T, size=n, replace=False))
+        dt, fl = oracle_sample(wl, x_bits, idx_np, w_np, toks)
+        line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+                                "kind": "oracle", "seconds": dt,
+                                "sample": f"{n} random tokens of {wl.name} (their experts' FFN + "
+                                          "combine; routing of the whole batch)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

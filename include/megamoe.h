@@ -1,0 +1,208 @@
+/*
+ * megamoe.h -- C ABI of the single-GPU MoE layer forward for GB300 (sm_103a).
+ *
+ * The layer (flashinfer PR #4069 "SM90 push FP8 mega-MoE backend",
+ * Description, the forward diagram) on one GPU, where dispatch and combine
+ * become a local permute and a local reduce:
+ *   route + dispatch -> 1x128 FP8 E4M3 activation quantisation ->
+ *   FC1 grouped GEMM (+ SwiGLU + 1x128 re-quantisation) -> FC2 grouped GEMM ->
+ *   combine (top-k weighted FP32 reduction, written as BF16).
+ *
+ * Conventions for every call:
+ *   - "d_" pointers are device pointers, "h_" pointers host pointers.  The
+ *     caller allocates and owns all device memory (workspace, weight store,
+ *     inputs, output); the library keeps pointers only.  The handle itself is
+ *     host memory owned by the library (moe_create / moe_destroy).
+ *   - BF16 tensors are passed as uint16_t bit patterns; FP8 E4M3 (OCP E4M3FN)
+ *     tensors as uint8_t codes.  All arrays are dense row-major.
+ *   - Streams are CUDA runtime streams (struct CUstream_st* is cudaStream_t);
+ *     NULL is the legacy default stream.
+ *   - Host-side argument errors return a status before anything is enqueued.
+ *     Errors found on the device (bad routes, capacity, watchdog) are written
+ *     to a device status word that moe_read_status returns.
+ *   - No call is thread-safe on the same handle.
+ */
+#ifndef MEGAMOE_H
+#define MEGAMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* null pointer, negative size, misaligned buffer */
+  MOE_ERR_UNSUPPORTED = 2,    /* dims outside the supported set (explicit, no fallback) */
+  MOE_ERR_CAPACITY = 3,       /* num_tokens > max_rows, or routed rows beyond capacity */
+  MOE_ERR_NOT_BOUND = 4,      /* forward before moe_bind_weights / moe_stage_inputs */
+  MOE_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed */
+  MOE_ERR_BAD_ROUTE = 6,      /* device: expert id out of range, duplicate, non-finite weight */
+  MOE_ERR_DEVICE_TIMEOUT = 7, /* device: a bounded wait inside a kernel expired */
+  MOE_ERR_BAD_SCALE = 8,      /* bind: a block scale is not a power of two in [2^-127, 2^127] */
+  MOE_ERR_WORKSPACE = 9       /* workspace or weight store smaller than the query said */
+} moe_status;
+
+/* Bits of the device status word (moe_read_status). */
+#define MOE_DEV_ROUTE_RANGE 0x01u     /* an expert id outside [-1, E) */
+#define MOE_DEV_ROUTE_DUP 0x02u       /* the same active expert twice in one token */
+#define MOE_DEV_ROUTE_NONFINITE 0x04u /* NaN/inf weight on an active route */
+#define MOE_DEV_CAPACITY 0x08u        /* padded routed rows exceed the workspace capacity */
+#define MOE_DEV_TIMEOUT 0x10u         /* a kernel's bounded wait expired; output undefined */
+#define MOE_DEV_BAD_SCALE 0x20u       /* bind: a weight scale is not a power of two */
+
+/* moe_dims.flags */
+#define MOE_FLAG_FUSE_FC1_EPILOGUE 0x1u /* SwiGLU + 1x128 quant inside the FC1 epilogue (opt-in) */
+#define MOE_FLAG_CHECK_ROUTES 0x2u      /* duplicate / finite-weight checks (range check always on) */
+#define MOE_FLAG_EMIT_FC1 0x4u          /* also keep the BF16 gate||up FC1 output (debug) */
+
+typedef struct moe_dims {
+  int32_t hidden;      /* H: multiple of 128, 128..16384 */
+  int32_t inter;       /* I: expert intermediate size, multiple of 128, 128..16384 */
+  int32_t num_experts; /* E: 1..1024 */
+  int32_t top_k;       /* K: one of 1, 2, 4, 6, 8 */
+  uint32_t flags;      /* MOE_FLAG_* */
+} moe_dims;
+
+typedef struct moe_handle moe_handle;
+
+/*
+ * moe_workspace_query -- pure host arithmetic, no CUDA call.
+ * Capacity contract (flashinfer PR #4069, "Contracts introduced by this PR":
+ * capacity_factor bounds the GEMM, TMA and scale buffers; the query takes
+ * explicit expected_m and max_rows so the tactic stays independent of the
+ * memory bound).
+ *   expected_m      typical tokens per forward; picks the GEMM tactic only,
+ *                   never a buffer size.  >= 1.
+ *   max_rows        the largest num_tokens any forward will pass.  >= 1.
+ *   capacity_factor routed rows are bounded by ceil(capacity_factor *
+ *                   max_rows * top_k) (plus per-expert tile padding); any
+ *                   value >= 1 can never overflow.  In (0, 64].
+ * Outputs (bytes): *workspace_bytes for the per-forward workspace and
+ * *weight_bytes for the transformed weight store.  Any 16-byte aligned base
+ * works: both sizes include slack for the library's internal 1024-byte
+ * alignment of its sub-buffers.
+ */
+MOE_API moe_status moe_workspace_query(const moe_dims* dims, int64_t expected_m, int64_t max_rows,
+                               float capacity_factor, size_t* workspace_bytes,
+                               size_t* weight_bytes);
+
+/*
+ * moe_create -- binds dims and caller-owned device regions; creates no CUDA
+ * stream and allocates no device memory.  Sets kernel attributes, so call it
+ * before any stream capture.  *out receives a host handle.
+ */
+MOE_API moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows,
+                      float capacity_factor, void* d_workspace, size_t workspace_bytes,
+                      void* d_weight_store, size_t weight_bytes, moe_handle** out);
+
+/*
+ * moe_quantize_weights -- FP32 expert weights to the format moe_bind_weights
+ * takes: 128x128 blocks, scale = the smallest power of two >= amax/448 (1 for
+ * an all-zero block), codes = E4M3 round-to-nearest-even of w/scale.
+ *   d_w     float [num_mats, rows, cols]; rows and cols multiples of 128.
+ *   d_q     uint8 [num_mats, rows, cols] (output).
+ *   d_scale float [num_mats, rows/128, cols/128] (output).
+ * Asynchronous on `stream`.
+ */
+MOE_API moe_status moe_quantize_weights(const float* d_w, int64_t num_mats, int32_t rows, int32_t cols,
+                                uint8_t* d_q, float* d_scale, struct CUstream_st* stream);
+
+/*
+ * moe_bind_weights -- the layer holds its static weights in a transformed,
+ * kernel-ready form that is built once, at set-up (flashinfer PR #4069,
+ * "Contracts introduced by this PR": the stateful backend contract).  Copies
+ * and transforms into the weight store:
+ *   d_w1        E4M3 [E, 2I, H]: rows [0, I) gate, rows [I, 2I) up.
+ *   d_w1_scale  float [E, 2I/128, H/128], powers of two.
+ *   d_w2        E4M3 [E, H, I].
+ *   d_w2_scale  float [E, H/128, I/128], powers of two.
+ * Enqueued on `stream`, then waits for that stream: the caller may free the
+ * inputs when this returns.  Returns MOE_ERR_BAD_SCALE if any scale is not a
+ * power of two within the E8M0 range.
+ */
+MOE_API moe_status moe_bind_weights(moe_handle* h, const uint8_t* d_w1, const float* d_w1_scale,
+                            const uint8_t* d_w2, const float* d_w2_scale,
+                            struct CUstream_st* stream);
+
+/*
+ * moe_stage_inputs -- binds the caller's BF16 output tensor d_out [max_rows, H]
+ * ahead of the forwards that write it (flashinfer PR #4069, "Contracts
+ * introduced by this PR": output binding at staging time).  May be called
+ * again to rebind.
+ */
+MOE_API moe_status moe_stage_inputs(moe_handle* h, uint16_t* d_out);
+
+/*
+ * moe_forward -- one layer forward, asynchronous on `stream`, with no host
+ * synchronisation (expert offsets stay on the device), capturable in a CUDA
+ * graph.
+ *   d_x         BF16 [num_tokens, H]
+ *   d_topk_idx  int32 [num_tokens, K]; -1 marks a masked slot.  For graph
+ *               replay with fewer live tokens, fill the tail rows with -1
+ *               (flashinfer PR #6398, tail masking).
+ *   d_topk_w    float [num_tokens, K]; ignored (may be NaN) on masked slots.
+ *   num_tokens  0..max_rows.  0 returns MOE_OK and writes nothing.
+ * Writes d_out[0:num_tokens, :] of the staged output.  Route errors set the
+ * device status word; the output is then undefined.
+ */
+MOE_API moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk_idx,
+                       const float* d_topk_w, int64_t num_tokens, struct CUstream_st* stream);
+
+/*
+ * moe_read_status -- copies the device status word of the latest forward on
+ * `stream` to *h_status (MOE_DEV_* bits) and synchronises that stream: the
+ * caller chooses this sync point.  Returns MOE_OK when the word is 0, else
+ * the matching error (route, capacity, timeout).
+ */
+MOE_API moe_status moe_read_status(moe_handle* h, uint32_t* h_status, struct CUstream_st* stream);
+
+/* Device pointers to internal buffers and their layouts, for tests and tools. */
+typedef struct moe_debug_view {
+  uint32_t* status;        /* device status word */
+  int32_t* counts;         /* [E] rows per expert */
+  int32_t* offsets;        /* [E+1] exclusive scan of counts (unpadded positions) */
+  int32_t* pad_offsets;    /* [E+1] scan of counts rounded up to 128 (GEMM rows) */
+  int32_t* perm;           /* [R] route id r = t*K + k at unpadded position pos */
+  int32_t* inv;            /* [T*K] unpadded position of route r, or -1 */
+  int32_t* inv_pad;        /* [T*K] padded GEMM row of route r, or -1 */
+  uint8_t* a;              /* [rows_alloc, H] E4M3 gathered activations (padded rows) */
+  uint8_t* a_sf;           /* E8M0 scale atoms of a: [rows_alloc/128][H/128][512] */
+  uint16_t* gu;            /* [rows_alloc, 2I] BF16 gate||up (unfused or EMIT_FC1), else NULL */
+  uint8_t* hq;             /* [rows_alloc, I] E4M3 re-quantised SwiGLU output */
+  uint8_t* h_sf;           /* E8M0 scale atoms of hq: [rows_alloc/128][I/128][512] */
+  uint16_t* y;             /* [rows_alloc, H] BF16 FC2 output per padded row */
+  int64_t rows_alloc;      /* padded-row capacity (multiple of 128) */
+  int32_t sf_atom_bytes;   /* 512: 128 rows x 4 bytes, byte (r%32)*16 + (r/32)*4 + j */
+} moe_debug_view;
+
+MOE_API moe_status moe_debug_views(moe_handle* h, moe_debug_view* out);
+
+/*
+ * moe_set_profile_events -- optional per-kernel timing: when n > 0, every
+ * following moe_forward records events[i] (cudaEvent_t, created by the
+ * caller) before its i-th kernel and events[n-1] after the last one, on the
+ * forward's stream.  Kernel order: 0 status reset, 1 route_count,
+ * 2 route_scan, 3 route_scatter, 4 quant_dispatch, 5 fc1, 6 swiglu_quant
+ * (skipped when fused), 7 fc2, 8 combine, 9 end.  n must be 0 or 10.
+ */
+MOE_API moe_status moe_set_profile_events(moe_handle* h, void* const* events, int32_t n);
+
+MOE_API void moe_destroy(moe_handle* h);
+MOE_API const char* moe_status_str(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEGAMOE_H */

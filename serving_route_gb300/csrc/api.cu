@@ -1,0 +1,392 @@
+// api.cu -- the C ABI (include/megamoe.h): argument checks, workspace and
+// weight-store layout, TMA tensor-map encoding, and the stream-ordered launch
+// sequence of one forward.  The calls follow the problem statement of
+// flashinfer PR #4069 ("Contracts introduced by this PR": capacity-bounded
+// workspace query with expected_m / max_rows, construction binding
+// transformed static weights, stage_inputs pre-binding the output) and the
+// tail-masking convention of flashinfer PR #6398.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace mm;
+
+struct moe_handle {
+  moe_dims dims;
+  Layout L;
+  int64_t expected_m;
+  Workspace ws;
+  WeightStore wst;
+  CUtensorMap tm_a, tm_hq, tm_w1, tm_w2;
+  bool bound;
+  uint16_t* out;
+  int num_sms;
+  int device;
+  cudaEvent_t ev[10];
+  int n_ev;
+};
+
+namespace {
+
+constexpr size_t kAlign = 1024;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool valid_dims(const moe_dims* d) {
+  if (!d) return false;
+  const bool hk = d->hidden >= 128 && d->hidden <= 16384 && d->hidden % 128 == 0;
+  const bool ik = d->inter >= 128 && d->inter <= 16384 && d->inter % 128 == 0;
+  const bool ek = d->num_experts >= 1 && d->num_experts <= 1024;
+  const bool kk = d->top_k == 1 || d->top_k == 2 || d->top_k == 4 || d->top_k == 6 || d->top_k == 8;
+  return hk && ik && ek && kk;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [outer, inner], tile box [box_outer, 128], 128-byte swizzle.
+bool encode_u8_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                   uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {128, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+namespace mm {
+
+moe_status compute_layout(const moe_dims* d, int64_t max_rows, float cf, Layout* L) {
+  if (!valid_dims(d)) return MOE_ERR_UNSUPPORTED;
+  if (max_rows < 1 || max_rows > (int64_t)1 << 24) return MOE_ERR_INVALID_ARG;
+  if (!(cf > 0.f) || !(cf <= 64.f)) return MOE_ERR_INVALID_ARG;
+  memset(L, 0, sizeof(*L));
+  L->H = d->hidden;
+  L->I = d->inter;
+  L->E = d->num_experts;
+  L->K = d->top_k;
+  L->max_rows = max_rows;
+  const int64_t rk = max_rows * L->K;
+  int64_t cap = (int64_t)std::ceil((double)cf * (double)rk);
+  if (cap > rk) cap = rk;
+  if (cap < 1) cap = 1;
+  L->cap_rows = cap;
+  const int64_t pad = cap + 127 * (cap < L->E ? cap : (int64_t)L->E);
+  L->rows_alloc = (int64_t)align_up((size_t)(pad < 128 ? 128 : pad), 128);
+  if (L->rows_alloc > ((int64_t)1 << 31) - 256) return MOE_ERR_INVALID_ARG;
+  L->nb_max = (max_rows + 127) / 128;
+  L->keep_gu = !(d->flags & MOE_FLAG_FUSE_FC1_EPILOGUE) || (d->flags & MOE_FLAG_EMIT_FC1);
+  const size_t H = L->H, I = L->I, E = L->E, R = L->rows_alloc, MB = R / 128;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, kAlign);
+    return at;
+  };
+  L->o_status = take(1024);  // status word at +0, total_mtiles at +4
+  L->o_counts = take(4 * E);
+  L->o_offsets = take(4 * (E + 1));
+  L->o_pad_offsets = take(4 * (E + 1));
+  L->o_mtile_expert = take(4 * MB);
+  L->o_block_counts = take(4 * (size_t)L->nb_max * E);
+  L->o_base_u = take(4 * (size_t)L->nb_max * E);
+  L->o_base_p = take(4 * (size_t)L->nb_max * E);
+  L->o_perm = take(4 * (size_t)rk);
+  L->o_inv = take(4 * (size_t)rk);
+  L->o_inv_pad = take(4 * (size_t)rk);
+  L->o_a = take(R * H);
+  L->o_a_sf = take(MB * (H / 128) * kSfAtomBytes);
+  L->o_gu = L->keep_gu ? take(R * 2 * I * 2) : 0;
+  L->o_hq = take(R * I);
+  L->o_h_sf = take(MB * (I / 128) * kSfAtomBytes);
+  L->o_y = take(R * H * 2);
+  L->ws_bytes = o + kAlign;  // slack to align the caller's base
+  o = 0;
+  L->o_w1 = take(E * 2 * I * H);
+  L->o_w2 = take(E * H * I);
+  L->o_w1_sf = take(E * (2 * I / 128) * (H / 128));
+  L->o_w2_sf = take(E * (H / 128) * (I / 128));
+  L->w_bytes = o + kAlign;
+  return MOE_OK;
+}
+
+}  // namespace mm
+
+extern "C" {
+
+moe_status moe_workspace_query(const moe_dims* dims, int64_t expected_m, int64_t max_rows,
+                               float capacity_factor, size_t* workspace_bytes,
+                               size_t* weight_bytes) {
+  if (!dims || !workspace_bytes || !weight_bytes) return MOE_ERR_INVALID_ARG;
+  if (expected_m < 1) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  const moe_status st = compute_layout(dims, max_rows, capacity_factor, &L);
+  if (st != MOE_OK) return st;
+  *workspace_bytes = L.ws_bytes;
+  *weight_bytes = L.w_bytes;
+  return MOE_OK;
+}
+
+moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows,
+                      float capacity_factor, void* d_workspace, size_t workspace_bytes,
+                      void* d_weight_store, size_t weight_bytes, moe_handle** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!dims || !d_workspace || !d_weight_store || expected_m < 1) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  moe_status st = compute_layout(dims, max_rows, capacity_factor, &L);
+  if (st != MOE_OK) return st;
+  if (workspace_bytes < L.ws_bytes || weight_bytes < L.w_bytes) return MOE_ERR_WORKSPACE;
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
+  if (gemm_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
+  moe_handle* h = new (std::nothrow) moe_handle;
+  if (!h) return MOE_ERR_INVALID_ARG;
+  memset(h, 0, sizeof(*h));
+  h->dims = *dims;
+  h->L = L;
+  h->expected_m = expected_m;
+  h->num_sms = sms;
+  h->device = dev;
+  uint8_t* b = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(d_workspace), kAlign));
+  Workspace& w = h->ws;
+  w.status = reinterpret_cast<uint32_t*>(b + L.o_status);
+  w.total_mtiles = reinterpret_cast<int32_t*>(b + L.o_status + 4);
+  w.counts = reinterpret_cast<int32_t*>(b + L.o_counts);
+  w.offsets = reinterpret_cast<int32_t*>(b + L.o_offsets);
+  w.pad_offsets = reinterpret_cast<int32_t*>(b + L.o_pad_offsets);
+  w.mtile_expert = reinterpret_cast<int32_t*>(b + L.o_mtile_expert);
+  w.block_counts = reinterpret_cast<int32_t*>(b + L.o_block_counts);
+  w.base_u = reinterpret_cast<int32_t*>(b + L.o_base_u);
+  w.base_p = reinterpret_cast<int32_t*>(b + L.o_base_p);
+  w.perm = reinterpret_cast<int32_t*>(b + L.o_perm);
+  w.inv = reinterpret_cast<int32_t*>(b + L.o_inv);
+  w.inv_pad = reinterpret_cast<int32_t*>(b + L.o_inv_pad);
+  w.a = b + L.o_a;
+  w.a_sf = b + L.o_a_sf;
+  w.gu = L.keep_gu ? reinterpret_cast<uint16_t*>(b + L.o_gu) : nullptr;
+  w.hq = b + L.o_hq;
+  w.h_sf = b + L.o_h_sf;
+  w.y = reinterpret_cast<uint16_t*>(b + L.o_y);
+  uint8_t* wb =
+      reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(d_weight_store), kAlign));
+  h->wst.w1 = wb + L.o_w1;
+  h->wst.w2 = wb + L.o_w2;
+  h->wst.w1_sf = wb + L.o_w1_sf;
+  h->wst.w2_sf = wb + L.o_w2_sf;
+  if (!encode_u8_map(&h->tm_a, w.a, L.H, L.rows_alloc, 128) ||
+      !encode_u8_map(&h->tm_hq, w.hq, L.I, L.rows_alloc, 128)) {
+    delete h;
+    return MOE_ERR_CUDA;
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+moe_status moe_quantize_weights(const float* d_w, int64_t num_mats, int32_t rows, int32_t cols,
+                                uint8_t* d_q, float* d_scale, struct CUstream_st* stream) {
+  if (!d_w || !d_q || !d_scale || num_mats < 0 || rows <= 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+  if (rows % 128 || cols % 128) return MOE_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(d_w) % 16 || reinterpret_cast<uintptr_t>(d_q) % 16)
+    return MOE_ERR_INVALID_ARG;
+  if (launch_quantize_weights(d_w, num_mats, rows, cols, d_q, d_scale, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_bind_weights(moe_handle* h, const uint8_t* d_w1, const float* d_w1_scale,
+                            const uint8_t* d_w2, const float* d_w2_scale,
+                            struct CUstream_st* stream) {
+  if (!h || !d_w1 || !d_w1_scale || !d_w2 || !d_w2_scale) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(d_w1) % 16) return MOE_ERR_INVALID_ARG;
+  h->bound = false;
+  const Layout& L = h->L;
+  if (cudaMemsetAsync(h->ws.status, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_bind_transform(h->wst, L, d_w1, d_w1_scale, d_w2, d_w2_scale, h->ws.status, stream) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  uint32_t st = 0;
+  if (cudaMemcpyAsync(&st, h->ws.status, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (st & MOE_DEV_BAD_SCALE) return MOE_ERR_BAD_SCALE;
+  if (!encode_u8_map(&h->tm_w1, h->wst.w1, L.H, (uint64_t)L.E * 2 * L.I, 256) ||
+      !encode_u8_map(&h->tm_w2, h->wst.w2, L.I, (uint64_t)L.E * L.H, 256))
+    return MOE_ERR_CUDA;
+  h->bound = true;
+  return MOE_OK;
+}
+
+moe_status moe_stage_inputs(moe_handle* h, uint16_t* d_out) {
+  if (!h || !d_out) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(d_out) % 16) return MOE_ERR_INVALID_ARG;
+  h->out = d_out;
+  return MOE_OK;
+}
+
+moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk_idx,
+                       const float* d_topk_w, int64_t num_tokens, struct CUstream_st* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (!h->bound || !h->out) return MOE_ERR_NOT_BOUND;
+  if (num_tokens < 0) return MOE_ERR_INVALID_ARG;
+  if (num_tokens > h->L.max_rows) return MOE_ERR_CAPACITY;
+  if (num_tokens == 0) return MOE_OK;
+  if (!d_x || !d_topk_idx || !d_topk_w) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(d_x) % 16) return MOE_ERR_INVALID_ARG;
+  const Layout& L = h->L;
+  const Workspace& ws = h->ws;
+  cudaStream_t s = stream;
+  const cudaEvent_t* ev = h->n_ev ? h->ev : nullptr;
+  const bool fused = (h->dims.flags & MOE_FLAG_FUSE_FC1_EPILOGUE) != 0;
+  const bool emit = (h->dims.flags & MOE_FLAG_EMIT_FC1) != 0;
+  const bool check = (h->dims.flags & MOE_FLAG_CHECK_ROUTES) != 0;
+
+  if (ev) record_event(ev[0], s);
+  cudaMemsetAsync(ws.status, 0, 4, s);
+  if (launch_route(ws, L, d_topk_idx, d_topk_w, num_tokens, check, s, ev ? ev + 1 : nullptr) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (ev) record_event(ev[4], s);
+  if (launch_quant_dispatch(ws, L, d_x, num_tokens, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  GemmArgs g1;
+  memset(&g1, 0, sizeof(g1));
+  g1.sfa = ws.a_sf;
+  g1.sfb = h->wst.w1_sf;
+  g1.mtile_expert = ws.mtile_expert;
+  g1.total_mtiles = ws.total_mtiles;
+  g1.KB = L.H / 128;
+  g1.NT = L.I / 128;  // 256-wide tiles over 2I
+  g1.N = 2 * L.I;
+  g1.NB = 2 * L.I / 128;
+  g1.max_mtiles = (int)(L.rows_alloc / 128);
+  g1.out = ws.gu;
+  g1.ld_out = 2 * (int64_t)L.I;
+  g1.inter = L.I;
+  g1.hq = ws.hq;
+  g1.h_sf = ws.h_sf;
+  g1.IB = L.I / 128;
+  g1.status = ws.status;
+  const GemmMode m1 = fused ? (emit ? kModeFusedGU : kModeFused) : kModeGU;
+  if (ev) record_event(ev[5], s);
+  if (launch_gemm(m1, &h->tm_a, &h->tm_w1, g1, h->num_sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ev) record_event(ev[6], s);
+  if (!fused && launch_swiglu_quant(ws, L, h->num_sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  GemmArgs g2;
+  memset(&g2, 0, sizeof(g2));
+  g2.sfa = ws.h_sf;
+  g2.sfb = h->wst.w2_sf;
+  g2.mtile_expert = ws.mtile_expert;
+  g2.total_mtiles = ws.total_mtiles;
+  g2.KB = L.I / 128;
+  g2.NT = (L.H + 255) / 256;
+  g2.N = L.H;
+  g2.NB = L.H / 128;
+  g2.max_mtiles = (int)(L.rows_alloc / 128);
+  g2.out = ws.y;
+  g2.ld_out = L.H;
+  g2.status = ws.status;
+  if (ev) record_event(ev[7], s);
+  if (launch_gemm(kModeY, &h->tm_hq, &h->tm_w2, g2, h->num_sms, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (ev) record_event(ev[8], s);
+  if (launch_combine(ws, L, d_topk_w, h->out, num_tokens, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ev) record_event(ev[9], s);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_read_status(moe_handle* h, uint32_t* h_status, struct CUstream_st* stream) {
+  if (!h || !h_status) return MOE_ERR_INVALID_ARG;
+  uint32_t st = 0;
+  if (cudaMemcpyAsync(&st, h->ws.status, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *h_status = st;
+  if (st & MOE_DEV_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
+  if (st & (MOE_DEV_ROUTE_RANGE | MOE_DEV_ROUTE_DUP | MOE_DEV_ROUTE_NONFINITE))
+    return MOE_ERR_BAD_ROUTE;
+  if (st & MOE_DEV_CAPACITY) return MOE_ERR_CAPACITY;
+  if (st & MOE_DEV_BAD_SCALE) return MOE_ERR_BAD_SCALE;
+  return MOE_OK;
+}
+
+moe_status moe_debug_views(moe_handle* h, moe_debug_view* v) {
+  if (!h || !v) return MOE_ERR_INVALID_ARG;
+  const Workspace& w = h->ws;
+  v->status = w.status;
+  v->counts = w.counts;
+  v->offsets = w.offsets;
+  v->pad_offsets = w.pad_offsets;
+  v->perm = w.perm;
+  v->inv = w.inv;
+  v->inv_pad = w.inv_pad;
+  v->a = w.a;
+  v->a_sf = w.a_sf;
+  v->gu = w.gu;
+  v->hq = w.hq;
+  v->h_sf = w.h_sf;
+  v->y = w.y;
+  v->rows_alloc = h->L.rows_alloc;
+  v->sf_atom_bytes = kSfAtomBytes;
+  return MOE_OK;
+}
+
+moe_status moe_set_profile_events(moe_handle* h, void* const* events, int32_t n) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (n == 0) {
+    h->n_ev = 0;
+    return MOE_OK;
+  }
+  if (n != 10 || !events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 10; ++i) h->ev[i] = reinterpret_cast<cudaEvent_t>(events[i]);
+  h->n_ev = 10;
+  return MOE_OK;
+}
+
+void moe_destroy(moe_handle* h) { delete h; }
+
+const char* moe_status_str(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_CAPACITY: return "capacity exceeded";
+    case MOE_ERR_NOT_BOUND: return "weights or output not bound";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_BAD_ROUTE: return "invalid routes";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_BAD_SCALE: return "weight scale is not a power of two";
+    case MOE_ERR_WORKSPACE: return "workspace or weight store too small";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

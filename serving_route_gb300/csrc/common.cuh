@@ -1,0 +1,295 @@
+// common.cuh -- device helpers of the MoE layer kernels (sm_103a only).
+//
+// Inline PTX wrappers for mbarriers, TMA, and the 5th-generation tensor core
+// (tcgen05: TMEM allocation, block-scaled MMA, shared->TMEM copies, TMEM
+// loads), plus the number-format helpers every kernel shares: the power-of-two
+// 1x128 scale rule, E4M3 packing through the hardware convert, the E8M0 scale
+// atom layout, and SwiGLU.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/megamoe.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ != 1030)
+#error "this library is written for sm_103a only"
+#endif
+
+namespace mm {
+
+// ----------------------------------------------------------------------------
+// Scale atoms: E8M0 scale bytes of 128 rows x 4 consecutive 32-wide K chunks
+// (one 128-wide K block), 512 bytes, in the order the block-scaled MMA reads
+// them from TMEM after a 32x128b.warpx4 copy: row r of the 128-row tile sits
+// at byte (r % 32) * 16 + (r / 32) * 4 + j, j = K chunk.  A 1x128 scale is the
+// same for the 4 chunks, so each row stores its byte four times.
+// ----------------------------------------------------------------------------
+constexpr int kSfAtomBytes = 512;
+
+__host__ __device__ __forceinline__ int64_t sf_atom_offset(int64_t row, int64_t kblock,
+                                                          int64_t kblocks) {
+  return ((row >> 7) * kblocks + kblock) * kSfAtomBytes + (row & 31) * 16 + ((row & 127) >> 5) * 4;
+}
+
+// Smallest e with amax <= 448 * 2^e, kept in [-127, 127]; amax == 0 gives 0.
+// amax = m * 2^E, m in [1, 2): e = E - 8 when m <= 1.75, else E - 7
+// (448 = 1.75 * 2^8).  Subnormal amax lies below every kept scale.
+__device__ __forceinline__ int pow2_scale_exp(float amax) {
+  uint32_t b = __float_as_uint(amax);
+  if (b == 0u) return 0;
+  uint32_t ef = b >> 23;
+  if (ef == 0u) return -127;
+  int e = (int)ef - 127 - 8 + (((b & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^-e as a float, exact for e in [-127, 127] (2^-127 is subnormal).
+__device__ __forceinline__ float pow2_neg(int e) {
+  int k = -e;
+  return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Two floats to two E4M3 codes (round to nearest even, saturating), low byte = a.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  __nv_fp8x2_storage_t v = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  return (uint32_t)v;
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+__device__ __forceinline__ float bf16_round(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// SwiGLU of one gate/up pair: silu(g) * u = g / (1 + exp(-g)) * u, in float,
+// each operation rounded to nearest.  The fused FC1 epilogue and the unfused
+// kernel both call this one function, so they agree bit for bit.
+__device__ __forceinline__ float swiglu(float g, float u) {
+  float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+  return __fmul_rn(s, u);
+}
+
+// Profiling events are recorded as external event nodes when the stream is
+// being captured, so per-kernel timing also works inside CUDA graphs.
+static inline void record_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+}
+
+__device__ __forceinline__ void record_status(uint32_t* status, uint32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// ----------------------------------------------------------------------------
+// Shared memory, mbarriers, TMA.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Every wait in these kernels is bounded: after `limit_ns` (or once another
+// role of the CTA has given up, *abort != 0) it records MOE_DEV_TIMEOUT and
+// returns false so the kernel can wind down instead of hanging the GPU.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      record_status(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const void* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+
+// 2-D tiled TMA load (box given by the tensor map) into shared memory,
+// completing `bytes` of transaction on the mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint32_t bar, int x,
+                                            int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Untiled bulk copy global -> shared (16-byte aligned, size multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"((uint64_t)src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ----------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor core, accumulators in tensor memory).
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation issued so far by this
+// thread has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// Shared-memory matrix descriptor, K-major operand staged by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+// Fields: start address >> 4 (bits 0-13), leading byte offset >> 4 (16-29,
+// unused for swizzled K-major), stride byte offset >> 4 (32-45), descriptor
+// version 1 (bit 46), swizzle mode 2 = 128B (bits 61-63).
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(16u >> 4) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Descriptor of a 512-byte scale atom (32 rows x 16 bytes, no swizzle, 8-row
+// core matrices 128 bytes apart) for the 32x128b shared->TMEM copy.
+__device__ __forceinline__ uint64_t sdesc_sf_atom(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128u >> 4) << 16;
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4 with block scales:
+// A and B E4M3 (format 0, bits 7-9 / 10-12), both K-major (bits 15, 16 = 0),
+// N >> 3 (bits 17-22), scale type E8M0 (bit 23), M >> 7 (bits 27-28), scale
+// factor byte selectors 0 (bits 4-5 for B, 29-30 for A).
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N) {
+  return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 7) << 27);
+}
+
+// D[tmem] (+)= (A * 2^sfa) x (B * 2^sfb)^T, FP32 accumulation, K = 32.
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared -> TMEM copy of one scale atom: 32 lanes x 128 bits, replicated to
+// the four 32-lane quadrants.
+__device__ __forceinline__ void tc_cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Each thread of the warp reads 32 consecutive 32-bit columns of its TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+}  // namespace mm

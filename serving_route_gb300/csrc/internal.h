@@ -1,0 +1,102 @@
+// internal.h -- host-side layout of the workspace / weight store and the
+// launchers each kernel file exports to the C-ABI layer (api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/megamoe.h"
+
+namespace mm {
+
+// Device buffers carved out of the caller's workspace (all 1024-byte aligned).
+struct Workspace {
+  uint32_t* status;        // device status word (MOE_DEV_* bits)
+  int32_t* total_mtiles;   // number of 128-row GEMM tiles of this forward
+  int32_t* counts;         // [E]
+  int32_t* offsets;        // [E+1]
+  int32_t* pad_offsets;    // [E+1]
+  int32_t* mtile_expert;   // [max_mtiles]
+  int32_t* block_counts;   // [nb_max][E] routes per (128-token block, expert)
+  int32_t* base_u;         // [nb_max][E] unpadded start of a block's expert run
+  int32_t* base_p;         // [nb_max][E] padded start of a block's expert run
+  int32_t* perm;           // [max_rows*K]
+  int32_t* inv;            // [max_rows*K]
+  int32_t* inv_pad;        // [max_rows*K]
+  uint8_t* a;              // [rows_alloc, H]
+  uint8_t* a_sf;           // atoms [rows_alloc/128][H/128][512]
+  uint16_t* gu;            // [rows_alloc, 2I] or nullptr
+  uint8_t* hq;             // [rows_alloc, I]
+  uint8_t* h_sf;           // atoms [rows_alloc/128][I/128][512]
+  uint16_t* y;             // [rows_alloc, H]
+};
+
+struct WeightStore {
+  uint8_t* w1;     // [E, 2I, H]: per 256-row tile j, gate rows 128j.. then up rows 128j..
+  uint8_t* w2;     // [E, H, I]
+  uint8_t* w1_sf;  // [E, 2I/128, H/128] E8M0, in the interleaved row-block order of w1
+  uint8_t* w2_sf;  // [E, H/128, I/128] E8M0
+};
+
+struct Layout {
+  int H, I, E, K;
+  int64_t max_rows;
+  int64_t cap_rows;    // routed-row capacity before padding
+  int64_t rows_alloc;  // padded GEMM rows (multiple of 128)
+  int64_t nb_max;      // 128-token blocks of max_rows
+  bool keep_gu;
+  size_t ws_bytes, w_bytes;
+  // byte offsets inside the workspace / weight store
+  size_t o_status, o_counts, o_offsets, o_pad_offsets, o_mtile_expert, o_block_counts, o_base_u,
+      o_base_p, o_perm, o_inv, o_inv_pad, o_a, o_a_sf, o_gu, o_hq, o_h_sf, o_y;
+  size_t o_w1, o_w2, o_w1_sf, o_w2_sf;
+};
+
+// layout.cpp-style pure host arithmetic (api.cu)
+moe_status compute_layout(const moe_dims* d, int64_t max_rows, float capacity_factor, Layout* L);
+
+// route.cu
+cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* topk_idx,
+                         const float* topk_w, int64_t T, bool check, cudaStream_t s,
+                         cudaEvent_t const* ev);
+
+// quant.cu
+cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
+                                  int64_t T, cudaStream_t s);
+cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int num_sms, cudaStream_t s);
+cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
+                                    float* scale, cudaStream_t s);
+cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const uint8_t* w1,
+                                  const float* w1s, const uint8_t* w2, const float* w2s,
+                                  uint32_t* status, cudaStream_t s);
+
+// gemm.cu
+enum GemmMode { kModeY = 0, kModeGU = 1, kModeFused = 2, kModeFusedGU = 3 };
+struct GemmArgs {
+  const uint8_t* sfa;          // scale atoms of A: [mblocks][KB][512]
+  const uint8_t* sfb;          // E8M0 bytes of B: [E][NB][KB]
+  const int32_t* mtile_expert;
+  const int32_t* total_mtiles;
+  int KB;                      // K / 128
+  int NT;                      // 256-wide N tiles per expert
+  int N;                       // B rows per expert
+  int NB;                      // N / 128
+  int max_mtiles;
+  uint16_t* out;               // kModeY: y; kModeGU/kModeFusedGU: gu
+  int64_t ld_out;              // elements per output row
+  int inter;                   // I: column offset of the up half in gu
+  uint8_t* hq;                 // fused: [rows, I]
+  uint8_t* h_sf;               // fused: scale atoms [mblocks][I/128][512]
+  int IB;                      // I / 128
+  uint32_t* status;
+};
+cudaError_t gemm_set_attributes();
+cudaError_t launch_gemm(GemmMode mode, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                        const GemmArgs& g, int num_sms, cudaStream_t s);
+
+// combine.cu
+cudaError_t launch_combine(const Workspace& ws, const Layout& L, const float* topk_w,
+                           uint16_t* out, int64_t T, cudaStream_t s);
+
+}  // namespace mm

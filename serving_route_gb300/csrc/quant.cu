@@ -1,0 +1,265 @@
+// quant.cu -- the element-wise kernels of the layer:
+//   quant_dispatch  step 2 + 3: 1x128 FP8 E4M3 quantisation of x with a
+//                   power-of-two scale per 128-column block ("DeepSeek-style
+//                   FP8 block scaling", flashinfer PR #4069, Limitations),
+//                   written straight into the padded, expert-sorted GEMM rows
+//                   of every active route of the token (the dispatch gather
+//                   fused into the quantiser: x is read once).
+//   swiglu_quant    the unfused reference path after FC1: SwiGLU of the BF16
+//                   gate||up rows and 1x128 re-quantisation (flashinfer PR
+//                   #4069, Description: the unfused path is the maintained
+//                   reference, the fused epilogue must match it bit for bit).
+//   quantize_weights / bind_transform: setup-time weight preparation.
+// All of them are HBM-bound streaming kernels: 16-byte loads, one 128-column
+// block per half-warp, amax by shuffles, grids sized to the SM count.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mm {
+
+__device__ __forceinline__ float half_warp_max(float v) {
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// 8 floats -> 8 E4M3 codes with scale 2^e (v * 2^-e is exact).
+__device__ __forceinline__ uint2 quant8(const float (&v)[8], int e) {
+  const float inv = pow2_neg(e);
+  uint2 q;
+  q.x = e4m3x4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+  q.y = e4m3x4(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
+  return q;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 p, float (&v)[8]) {
+  const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
+    v[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+  }
+}
+
+// One warp handles two 128-column blocks of one token per iteration (one per
+// half-warp); each lane owns 8 consecutive columns.
+__global__ void __launch_bounds__(256) quant_dispatch_kernel(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pad, int64_t T, int H, int K,
+    uint8_t* __restrict__ a, uint8_t* __restrict__ a_sf) {
+  const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
+  const int KB = H >> 7;
+  const int units = (KB + 1) >> 1;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < T * units;
+       u += nwarps) {
+    const int64_t t = u / units;
+    const int b = (int)(u - t * units) * 2 + half;
+    const bool valid = b < KB;
+    const int p_lane = (lane < K) ? inv_pad[t * K + lane] : -1;
+    float v[8];
+    if (valid) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(x + t * H + b * 128 + l16 * 8);
+      unpack_bf16x8(raw, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = half_warp_max(amax);
+    const int e = pow2_scale_exp(amax);
+    const uint2 q = quant8(v, e);
+    const uint32_t sf4 = (uint32_t)(e + 127) * 0x01010101u;
+    for (int k = 0; k < K; ++k) {
+      const int p = __shfl_sync(0xFFFFFFFFu, p_lane, k);
+      if (p >= 0 && valid) {
+        *reinterpret_cast<uint2*>(a + (int64_t)p * H + b * 128 + l16 * 8) = q;
+        if (l16 == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_atom_offset(p, b, KB)) = sf4;
+      }
+    }
+  }
+}
+
+// Unfused SwiGLU + re-quantisation over the padded GEMM rows of this forward.
+__global__ void __launch_bounds__(256) swiglu_quant_kernel(
+    const uint16_t* __restrict__ gu, const int32_t* __restrict__ total_mtiles, int I,
+    uint8_t* __restrict__ hq, uint8_t* __restrict__ h_sf) {
+  const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
+  const int IB = I >> 7;
+  const int units = (IB + 1) >> 1;
+  const int64_t rows = (int64_t)(*total_mtiles) * 128;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < rows * units;
+       u += nwarps) {
+    const int64_t row = u / units;
+    const int b = (int)(u - row * units) * 2 + half;
+    const bool valid = b < IB;
+    float g[8], up[8], h[8];
+    if (valid) {
+      const uint16_t* src = gu + row * 2 * I + b * 128 + l16 * 8;
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(src), g);
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(src + I), up);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = up[i] = 0.f;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      h[i] = swiglu(g[i], up[i]);
+      amax = fmaxf(amax, fabsf(h[i]));
+    }
+    amax = half_warp_max(amax);
+    const int e = pow2_scale_exp(amax);
+    if (valid) {
+      *reinterpret_cast<uint2*>(hq + row * I + b * 128 + l16 * 8) = quant8(h, e);
+      if (l16 == 0)
+        *reinterpret_cast<uint32_t*>(h_sf + sf_atom_offset(row, b, IB)) =
+            (uint32_t)(e + 127) * 0x01010101u;
+    }
+  }
+}
+
+// 128x128 block quantisation of float weights: one CTA per block, each thread
+// owns half a row (64 floats in registers).
+__global__ void __launch_bounds__(256) quantize_weights_kernel(const float* __restrict__ w,
+                                                               int rows, int cols,
+                                                               uint8_t* __restrict__ q,
+                                                               float* __restrict__ scale) {
+  __shared__ float red[8];
+  const int rb = rows >> 7, cb = cols >> 7;
+  const int64_t blk = blockIdx.x;
+  const int64_t m = blk / ((int64_t)rb * cb);
+  const int bi = (int)((blk / cb) % rb), bj = (int)(blk % cb);
+  const int r = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 64;
+  const int64_t base = (m * rows + (int64_t)bi * 128 + r) * cols + (int64_t)bj * 128 + c0;
+  float v[64];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float4 f = *reinterpret_cast<const float4*>(w + base + 4 * i);
+    v[4 * i] = f.x;
+    v[4 * i + 1] = f.y;
+    v[4 * i + 2] = f.z;
+    v[4 * i + 3] = f.w;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  const int e = pow2_scale_exp(amax);
+  const float inv = pow2_neg(e);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 o;
+    o.x = e4m3x4(v[16 * i + 0] * inv, v[16 * i + 1] * inv, v[16 * i + 2] * inv, v[16 * i + 3] * inv);
+    o.y = e4m3x4(v[16 * i + 4] * inv, v[16 * i + 5] * inv, v[16 * i + 6] * inv, v[16 * i + 7] * inv);
+    o.z = e4m3x4(v[16 * i + 8] * inv, v[16 * i + 9] * inv, v[16 * i + 10] * inv, v[16 * i + 11] * inv);
+    o.w = e4m3x4(v[16 * i + 12] * inv, v[16 * i + 13] * inv, v[16 * i + 14] * inv, v[16 * i + 15] * inv);
+    *reinterpret_cast<uint4*>(q + base + 16 * i) = o;
+  }
+  if (threadIdx.x == 0) scale[(m * rb + bi) * cb + bj] = pow2_neg(-e);
+}
+
+// float power-of-two scale -> E8M0 byte; anything else flags MOE_DEV_BAD_SCALE.
+__device__ __forceinline__ uint8_t scale_to_e8m0(float s, uint32_t* status) {
+  const uint32_t b = __float_as_uint(s);
+  const uint32_t ef = (b >> 23) & 0xFFu, m = b & 0x7FFFFFu;
+  if ((b >> 31) == 0u && m == 0u && ef >= 1u && ef <= 254u) return (uint8_t)ef;
+  if (b == 0x00400000u) return 0;  // 2^-127
+  record_status(status, MOE_DEV_BAD_SCALE);
+  return 127;
+}
+
+// W1 rows reordered so that 256-row tile j holds gate rows [128j, 128j+128)
+// followed by up rows [128j, 128j+128): one FC1 tile then owns all 128 SwiGLU
+// columns of one 1x128 re-quantisation block.
+__global__ void bind_w1_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                               int E, int I, int H) {
+  const int64_t chunks_per_row = H / 16;
+  const int64_t total = (int64_t)E * 2 * I * chunks_per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / chunks_per_row, ch = i % chunks_per_row;
+    const int64_t e = row / (2 * I), n = row % (2 * I);
+    const int64_t j = n >> 8, within = n & 255;
+    const int64_t src_n = (within < 128) ? (j * 128 + within) : (I + j * 128 + within - 128);
+    reinterpret_cast<uint4*>(dst)[i] =
+        reinterpret_cast<const uint4*>(src + (e * 2 * I + src_n) * H)[ch];
+  }
+}
+
+__global__ void bind_w1_scale_kernel(const float* __restrict__ s, uint8_t* __restrict__ d, int E,
+                                     int IB, int HB, uint32_t* status) {
+  const int64_t total = (int64_t)E * 2 * IB * HB;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = i / (2 * IB * HB), rem = i % (2 * IB * HB);
+    const int64_t nb = rem / HB, kb = rem % HB;
+    const int64_t src_nb = (nb & 1) ? (IB + (nb >> 1)) : (nb >> 1);
+    d[i] = scale_to_e8m0(s[(e * 2 * IB + src_nb) * HB + kb], status);
+  }
+}
+
+__global__ void scale_convert_kernel(const float* __restrict__ s, uint8_t* __restrict__ d,
+                                     int64_t n, uint32_t* status) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    d[i] = scale_to_e8m0(s[i], status);
+}
+
+static int stream_grid(int64_t work, int per_block) {
+  int64_t b = (work + per_block - 1) / per_block;
+  const int64_t cap = 152 * 16;
+  return (int)(b < 1 ? 1 : (b > cap ? cap : b));
+}
+
+cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
+                                  int64_t T, cudaStream_t s) {
+  const int64_t warps = T * ((L.H / 128 + 1) / 2);
+  quant_dispatch_kernel<<<stream_grid(warps, 8), 256, 0, s>>>(x, ws.inv_pad, T, L.H, L.K, ws.a,
+                                                              ws.a_sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int num_sms,
+                                cudaStream_t s) {
+  (void)num_sms;
+  const int64_t warps = (L.rows_alloc) * ((L.I / 128 + 1) / 2);
+  swiglu_quant_kernel<<<stream_grid(warps, 8), 256, 0, s>>>(ws.gu, ws.total_mtiles, L.I, ws.hq,
+                                                            ws.h_sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
+                                    float* scale, cudaStream_t s) {
+  const int64_t blocks = nmat * (rows / 128) * (cols / 128);
+  if (blocks == 0) return cudaSuccess;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  quantize_weights_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, rows, cols, q, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const uint8_t* w1,
+                                  const float* w1s, const uint8_t* w2, const float* w2s,
+                                  uint32_t* status, cudaStream_t s) {
+  const int E = L.E, I = L.I, H = L.H;
+  const int64_t w1_chunks = (int64_t)E * 2 * I * (H / 16);
+  bind_w1_kernel<<<stream_grid(w1_chunks, 256), 256, 0, s>>>(w1, wst.w1, E, I, H);
+  cudaError_t err = cudaMemcpyAsync(wst.w2, w2, (size_t)E * H * I, cudaMemcpyDeviceToDevice, s);
+  if (err != cudaSuccess) return err;
+  const int64_t n1 = (int64_t)E * 2 * (I / 128) * (H / 128);
+  bind_w1_scale_kernel<<<stream_grid(n1, 256), 256, 0, s>>>(w1s, wst.w1_sf, E, I / 128, H / 128,
+                                                            status);
+  const int64_t n2 = (int64_t)E * (H / 128) * (I / 128);
+  scale_convert_kernel<<<stream_grid(n2, 256), 256, 0, s>>>(w2s, wst.w2_sf, n2, status);
+  return cudaGetLastError();
+}
+
+}  // namespace mm

@@ -1,0 +1,121 @@
+"""MegaMoELayer: owns the torch allocations of one layer instance and calls the
+C ABI (binding.py).  PyTorch provides device memory and streams only."""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class MegaMoELayer:
+    def __init__(self, hidden: int, inter: int, num_experts: int, top_k: int, *, max_rows: int,
+                 expected_m: int | None = None, capacity_factor: float = 1.0,
+                 fuse_fc1: bool = False, check_routes: bool = True, emit_fc1: bool = False,
+                 device="cuda"):
+        self.H, self.I, self.E, self.K = hidden, inter, num_experts, top_k
+        self.max_rows = max_rows
+        self.flags = ((B.MOE_FLAG_FUSE_FC1_EPILOGUE if fuse_fc1 else 0)
+                      | (B.MOE_FLAG_CHECK_ROUTES if check_routes else 0)
+                      | (B.MOE_FLAG_EMIT_FC1 if emit_fc1 else 0))
+        em = expected_m if expected_m is not None else max_rows
+        ws, wb = B.moe_workspace_query(hidden, inter, num_experts, top_k, self.flags, em, max_rows,
+                                       capacity_factor)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.weight_store = torch.empty(wb, dtype=torch.uint8, device=device)
+        self.handle = B.moe_create(hidden, inter, num_experts, top_k, self.flags, em, max_rows,
+                                   capacity_factor, self.workspace.data_ptr(), ws,
+                                   self.weight_store.data_ptr(), wb)
+        self.out = torch.empty(max_rows, hidden, dtype=torch.bfloat16, device=device)
+        B.moe_stage_inputs(self.handle, self.out.data_ptr())
+
+    # -- weights ----------------------------------------------------------------
+    @staticmethod
+    def quantize_weights(w: torch.Tensor, stream=None):
+        """float32 [n, rows, cols] on the GPU -> (E4M3 uint8, float scales [n, rows/128, cols/128])."""
+        assert w.dtype == torch.float32 and w.is_cuda and w.is_contiguous() and w.dim() == 3
+        n, r, c = w.shape
+        q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+        s = torch.empty((n, r // 128, c // 128), dtype=torch.float32, device=w.device)
+        B.moe_quantize_weights(w.data_ptr(), n, r, c, q.data_ptr(), s.data_ptr(), _stream_ptr(stream))
+        return q, s
+
+    def bind_weights(self, w1_q, w1_s, w2_q, w2_s, stream=None) -> None:
+        for t in (w1_q, w1_s, w2_q, w2_s):
+            assert t.is_cuda and t.is_contiguous()
+        assert tuple(w1_q.shape) == (self.E, 2 * self.I, self.H) and w1_q.dtype == torch.uint8
+        assert tuple(w2_q.shape) == (self.E, self.H, self.I) and w2_q.dtype == torch.uint8
+        B.moe_bind_weights(self.handle, w1_q.data_ptr(), w1_s.data_ptr(), w2_q.data_ptr(),
+                           w2_s.data_ptr(), _stream_ptr(stream))
+
+    # -- forward ------------------------------------------------------------------
+    def forward(self, x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                num_tokens: int | None = None, stream=None) -> torch.Tensor:
+        T = x.shape[0] if num_tokens is None else num_tokens
+        assert x.dtype == torch.bfloat16 and topk_idx.dtype == torch.int32
+        assert topk_w.dtype == torch.float32
+        B.moe_forward(self.handle, x.data_ptr(), topk_idx.data_ptr(), topk_w.data_ptr(), T,
+                      _stream_ptr(stream))
+        return self.out[:T]
+
+    def read_status(self, stream=None):
+        return B.moe_read_status(self.handle, _stream_ptr(stream))
+
+    def set_profile_events(self, events) -> None:
+        B.moe_set_profile_events(self.handle, [e.cuda_event for e in events] if events else [])
+
+    # -- introspection -------------------------------------------------------------
+    def debug(self) -> dict:
+        """torch views of the internal buffers (slices of the workspace)."""
+        v = B.moe_debug_views(self.handle)
+        base = self.workspace.data_ptr()
+        R = v.rows_alloc
+        H, I, E, K = self.H, self.I, self.E, self.K
+
+        def view(ptr, nbytes, dtype, shape):
+            off = ptr - base
+            t = self.workspace[off:off + nbytes]
+            return t.view(dtype).view(shape)
+
+        d = dict(
+            status=view(v.status, 4, torch.int32, (1,)),
+            counts=view(v.counts, 4 * E, torch.int32, (E,)),
+            offsets=view(v.offsets, 4 * (E + 1), torch.int32, (E + 1,)),
+            pad_offsets=view(v.pad_offsets, 4 * (E + 1), torch.int32, (E + 1,)),
+            perm=view(v.perm, 4 * self.max_rows * K, torch.int32, (self.max_rows * K,)),
+            inv=view(v.inv, 4 * self.max_rows * K, torch.int32, (self.max_rows * K,)),
+            inv_pad=view(v.inv_pad, 4 * self.max_rows * K, torch.int32, (self.max_rows * K,)),
+            a=view(v.a, R * H, torch.uint8, (R, H)),
+            a_sf=view(v.a_sf, (R // 128) * (H // 128) * 512, torch.uint8, (R // 128, H // 128, 512)),
+            hq=view(v.hq, R * I, torch.uint8, (R, I)),
+            h_sf=view(v.h_sf, (R // 128) * (I // 128) * 512, torch.uint8, (R // 128, I // 128, 512)),
+            y=view(v.y, R * H * 2, torch.bfloat16, (R, H)),
+            rows_alloc=R,
+        )
+        if v.gu:
+            d["gu"] = view(v.gu, R * 2 * I * 2, torch.bfloat16, (R, 2 * I))
+        return d
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            B.moe_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def sf_atom_rows(atoms: torch.Tensor, rows: int) -> torch.Tensor:
+    """Decode scale atoms [mblocks, kblocks, 512] into E8M0 bytes [rows, kblocks]
+    (row r of an m-block at byte (r%32)*16 + (r//32)*4; the 4 copies are equal)."""
+    mb, kbn, _ = atoms.shape
+    a = atoms.view(mb, kbn, 32, 4, 4)            # [mb, kb, r%32, r//32, copy]
+    a = a[..., 0].permute(0, 3, 2, 1)            # [mb, r//32, r%32, kb]
+    return a.reshape(mb * 128, kbn)[:rows]

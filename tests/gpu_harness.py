@@ -1,0 +1,94 @@
+"""Shared set-up of the GPU parity tests.
+
+Each side prepares its own inputs from the shared seeded generator:
+  * oracle: host generator (C) -> float32 weights -> the oracle's quantiser;
+  * GPU:    device generator (CUDA) -> float32 weights in HBM -> the library's
+            quantiser (moe_quantize_weights) -> moe_bind_weights.
+Routes and x come from the host generator and are copied to the device (they
+are inputs, identical on both sides).  No oracle input or expected value is
+ever taken from the GPU path.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from gen import inputs as g
+from gen import problem
+from gen.configs import Workload
+
+
+def rel_l2(a: np.ndarray, b: np.ndarray) -> float:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    den = np.sqrt(np.sum(b * b))
+    return float(np.sqrt(np.sum((a - b) ** 2)) / (den if den > 0 else 1.0))
+
+
+def bf16_np(t: torch.Tensor) -> np.ndarray:
+    """bf16 torch tensor -> float64 numpy."""
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return g.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def device_weights(wl: Workload, layer_cls, chunk_experts: int = 16, stream=None):
+    """FP32 weights generated on the GPU and quantised there, in expert chunks
+    (bounded temporary memory).  Returns (w1q, w1s, w2q, w2s) on the device."""
+    E, H, I = wl.E, wl.H, wl.I
+    dev = torch.device("cuda")
+    w1q = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=dev)
+    w1s = torch.empty((E, 2 * I // 128, H // 128), dtype=torch.float32, device=dev)
+    w2q = torch.empty((E, H, I), dtype=torch.uint8, device=dev)
+    w2s = torch.empty((E, H // 128, I // 128), dtype=torch.float32, device=dev)
+    sp = (stream or torch.cuda.current_stream()).cuda_stream
+    n1, n2 = 2 * I * H, H * I
+    for e0 in range(0, E, chunk_experts):
+        ne = min(chunk_experts, E - e0)
+        f1 = torch.empty((ne, 2 * I, H), dtype=torch.float32, device=dev)
+        g.dev_normal_f32(wl.seed, g.STREAM_W1, e0 * n1, ne * n1, g.weight_sigma(H), f1.data_ptr(), sp)
+        q, s = layer_cls.quantize_weights(f1, stream)
+        w1q[e0:e0 + ne].copy_(q)
+        w1s[e0:e0 + ne].copy_(s)
+        del f1, q, s
+        f2 = torch.empty((ne, H, I), dtype=torch.float32, device=dev)
+        g.dev_normal_f32(wl.seed, g.STREAM_W2, e0 * n2, ne * n2, g.weight_sigma(I), f2.data_ptr(), sp)
+        q, s = layer_cls.quantize_weights(f2, stream)
+        w2q[e0:e0 + ne].copy_(q)
+        w2s[e0:e0 + ne].copy_(s)
+        del f2, q, s
+    return w1q, w1s, w2q, w2s
+
+
+def oracle_weights(orc, wl: Workload, experts=None):
+    """Oracle-side weights: host generator + the oracle's quantiser.
+    experts=None -> all experts; otherwise arrays hold only the listed experts
+    in the order given."""
+    w1q, w1s = orc.quant_weights(problem.w1_f32(wl, experts))
+    w2q, w2s = orc.quant_weights(problem.w2_f32(wl, experts))
+    return w1q, w1s, w2q, w2s
+
+
+def host_inputs(wl: Workload):
+    x = problem.x_bits(wl)
+    idx, w = wl.make_routes()
+    return x, idx, w
+
+
+def to_device(x_bits: np.ndarray, idx: np.ndarray, w: np.ndarray):
+    dev = torch.device("cuda")
+    xt = torch.from_numpy(x_bits.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+    it = torch.from_numpy(np.ascontiguousarray(idx, dtype=np.int32)).to(dev)
+    wt = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).to(dev)
+    return xt, it, wt
+
+
+def padded_rows(offsets: np.ndarray, pad_offsets: np.ndarray, R: int) -> np.ndarray:
+    """GEMM row of every unpadded sorted position p < R."""
+    E = len(offsets) - 1
+    pos = np.arange(R)
+    e = np.searchsorted(offsets, pos, side="right") - 1
+    e = np.clip(e, 0, E - 1)
+    return pad_offsets[e] + (pos - offsets[e])

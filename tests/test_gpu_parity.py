@@ -1,0 +1,356 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars (written here, derived from the layer definition):
+  * bit-exact: expert counts, offsets, perm, inv, the padded row map, every
+    quantised FP8 byte and E8M0 scale of the gathered activations, and the
+    library's FP8 weight quantiser;
+  * gate||up (FC1 pre-activation, BF16 vs the oracle's BF16): rel-L2 <= 1e-3;
+  * output (BF16): rel-L2 <= 1e-2 and max-abs <= 5e-2 * rms(reference);
+  * fused FC1 epilogue vs the unfused path: bit-equal (hq, scales, out).
+Where FP32 accumulation flips a BF16 rounding of gate||up, the re-quantised
+hq may differ by one E4M3 code: the flip count is reported, not gated.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gen import configs, problem
+from gen import inputs as g
+from tests import gpu_harness as gh
+
+pytestmark = pytest.mark.gpu
+
+GU_TOL = 1e-3
+OUT_TOL = 1e-2
+MAXABS_FRAC = 5e-2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as ge
+    ge.build()
+    import serving_route_gb300 as S
+    assert torch.cuda.is_available()
+    return S
+
+
+def make_layer(S, wl, weights, max_rows=None, fuse=False, emit=True, check=True, cf=1.0):
+    layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=max_rows or wl.T, fuse_fc1=fuse,
+                           emit_fc1=emit, check_routes=check, capacity_factor=cf)
+    layer.bind_weights(*weights)
+    return layer
+
+
+def check_routing(dbg, ref, T, K):
+    R = int(ref["offsets"][-1])
+    assert np.array_equal(dbg["counts"].cpu().numpy(), ref["counts"])
+    assert np.array_equal(dbg["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(dbg["perm"][:R].cpu().numpy(), ref["perm"])
+    assert np.array_equal(dbg["inv"][:T * K].cpu().numpy(), ref["inv"])
+    pad = dbg["pad_offsets"].cpu().numpy()
+    assert np.all(pad % 128 == 0)
+    assert np.array_equal(np.diff(pad), (ref["counts"] + 127) // 128 * 128)
+    rows = gh.padded_rows(ref["offsets"], pad, R)
+    inv_pad = dbg["inv_pad"][:T * K].cpu().numpy()
+    act = ref["inv"] >= 0
+    assert np.array_equal(inv_pad[act], rows[ref["inv"][act]])
+    assert np.all(inv_pad[~act] == -1)
+    return rows
+
+
+def check_quant(S, dbg, xq, xs, perm, rows, K):
+    """every routed row of A equals the oracle's quantised token row, byte for byte"""
+    R = len(perm)
+    if R == 0:
+        return
+    tok = perm // K
+    a = dbg["a"][torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert np.array_equal(a, xq[tok])
+    sf = S.sf_atom_rows(dbg["a_sf"], dbg["rows_alloc"]).cpu().numpy()[rows].astype(np.int64) - 127
+    assert np.array_equal(np.ldexp(1.0, sf).astype(np.float32), xs[tok])
+
+
+def run_full(S, orc, wl, fuse, emit=True, weights_dev=None, weights_orc=None):
+    x, idx, w = gh.host_inputs(wl)
+    ref = orc.forward(x, idx, w, *weights_orc)
+    assert ref["err"] == 0
+    layer = make_layer(S, wl, weights_dev, fuse=fuse, emit=emit)
+    xt, it, wt = gh.to_device(x, idx, w)
+    out = layer.forward(xt, it, wt)
+    st, bits = layer.read_status()
+    assert st == 0 and bits == 0, (st, bits)
+    return layer, layer.debug(), out, ref, x, idx, w
+
+
+def compare_outputs(dbg, out, ref, rows, check_gu=True):
+    R = len(rows)
+    stats = {}
+    if check_gu and "gu" in dbg and R:
+        gu = gh.bf16_np(dbg["gu"][torch.from_numpy(rows).cuda()])
+        stats["gu_rel_l2"] = gh.rel_l2(gu, gh.bits_to_f64(ref["gu"]))
+        assert stats["gu_rel_l2"] <= GU_TOL, stats
+    if R:
+        hq = dbg["hq"][torch.from_numpy(rows).cuda()].cpu().numpy()
+        stats["hq_code_flips"] = int(np.sum(hq != ref["hq"]))
+        y = gh.bf16_np(dbg["y"][torch.from_numpy(rows).cuda()])
+        stats["y_rel_l2"] = gh.rel_l2(y, gh.bits_to_f64(ref["y"]))
+    o = gh.bf16_np(out)
+    r = gh.bits_to_f64(ref["out"])
+    stats["out_rel_l2"] = gh.rel_l2(o, r)
+    rms = float(np.sqrt(np.mean(r * r))) if r.size else 0.0
+    stats["out_maxabs"] = float(np.max(np.abs(o - r))) if r.size else 0.0
+    assert stats["out_rel_l2"] <= OUT_TOL, stats
+    assert stats["out_maxabs"] <= MAXABS_FRAC * rms + 1e-30, (stats, rms)
+    return stats
+
+
+# ----------------------------------------------------------------------------
+# generator and weight quantiser
+# ----------------------------------------------------------------------------
+def test_device_generator_matches_host(lib):
+    n = 1 << 20
+    d = torch.empty(n, dtype=torch.float32, device="cuda")
+    g.dev_normal_f32(0, g.STREAM_W1, 12345, n, g.weight_sigma(7168), d.data_ptr(),
+                     torch.cuda.current_stream().cuda_stream)
+    h = g.host_normal_f32(0, g.STREAM_W1, 12345, n, g.weight_sigma(7168))
+    assert np.array_equal(d.cpu().numpy().view(np.uint32), h.view(np.uint32))
+    b = torch.empty(n, dtype=torch.int16, device="cuda")
+    g.dev_normal_bf16(3, g.STREAM_X, 777, n, b.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert np.array_equal(b.cpu().numpy().view(np.uint16), g.host_normal_bf16(3, g.STREAM_X, 777, n))
+
+
+def test_weight_quantiser_bit_exact(lib, orc):
+    S = lib
+    rng = np.random.default_rng(7)
+    w = (rng.standard_normal((3, 256, 384)) * 0.03).astype(np.float32)
+    w[1, :128, :128] = 0.0                     # all-zero block: scale 1
+    w[2, 128:, 256:] *= 2.0 ** 40              # large block
+    w[0, 128:, :128] *= 2.0 ** -100            # tiny block
+    q, s = S.MegaMoELayer.quantize_weights(torch.from_numpy(w).cuda())
+    rq, rs = orc.quant_weights(w)
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(s.cpu().numpy(), rs)
+
+
+# ----------------------------------------------------------------------------
+# tiny workload: whole-layer oracle comparison, fused and unfused
+# ----------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def tiny(lib, orc):
+    wl = configs.TINY
+    return wl, gh.device_weights(wl, lib.MegaMoELayer), gh.oracle_weights(orc, wl)
+
+
+def test_tiny_weights_match_oracle_quantiser(lib, tiny):
+    wl, wd, wo = tiny
+    for a, b in zip(wd, wo):
+        assert np.array_equal(a.cpu().numpy(), b)
+
+
+@pytest.mark.parametrize("fuse", [False, True])
+def test_tiny_layer_parity(lib, orc, tiny, fuse):
+    wl, wd, wo = tiny
+    layer, dbg, out, ref, x, idx, w = run_full(lib, orc, wl, fuse, True, wd, wo)
+    rows = check_routing(dbg, ref, wl.T, wl.K)
+    check_quant(lib, dbg, ref["xq"], ref["xs"], ref["perm"], rows, wl.K)
+    stats = compare_outputs(dbg, out, ref, rows)
+    print("tiny", "fused" if fuse else "unfused", stats)
+
+
+def test_fused_epilogue_bit_equal_unfused(lib, orc, tiny):
+    """Routed rows only: padded GEMM rows hold whatever the workspace held."""
+    wl, wd, _ = tiny
+    x, idx, w = gh.host_inputs(wl)
+    xt, it, wt = gh.to_device(x, idx, w)
+    res = []
+    for fuse in (False, True):
+        layer = make_layer(lib, wl, wd, fuse=fuse, emit=True)
+        out = layer.forward(xt, it, wt).clone()
+        d = layer.debug()
+        off = d["offsets"].cpu().numpy()
+        rows = torch.from_numpy(gh.padded_rows(off, d["pad_offsets"].cpu().numpy(), int(off[-1]))).cuda()
+        sf = lib.sf_atom_rows(d["h_sf"], d["rows_alloc"])[rows]
+        res.append((out.view(torch.int16), d["hq"][rows], sf, d["gu"][rows].view(torch.int16),
+                    d["y"][rows].view(torch.int16)))
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+
+
+# ----------------------------------------------------------------------------
+# edge cases on small shapes
+# ----------------------------------------------------------------------------
+def small_problem(orc, T, H, I, E, K, seed, mask=0.0, empty=()):
+    rng = np.random.default_rng(seed)
+    x = g.normal_bf16_bits(seed, g.STREAM_X, np.arange(T * H, dtype=np.uint64)).reshape(T, H)
+    pool = np.array([e for e in range(E) if e not in empty])
+    idx = np.stack([rng.permutation(pool)[:K] for _ in range(T)]).astype(np.int32) if T else \
+        np.zeros((0, K), np.int32)
+    if mask and T:
+        idx[rng.random(idx.shape) < mask] = -1
+    w = (rng.random((T, K)) + 0.05).astype(np.float32)
+    w1 = (rng.standard_normal((E, 2 * I, H)) / np.sqrt(H)).astype(np.float32)
+    w2 = (rng.standard_normal((E, H, I)) / np.sqrt(I)).astype(np.float32)
+    return x, idx, w, w1, w2
+
+
+def layer_from_float(S, orc, T, H, I, E, K, w1, w2, fuse=True, emit=True, max_rows=None, cf=1.0):
+    q1, s1 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w1).cuda())
+    q2, s2 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w2).cuda())
+    wo = orc.quant_weights(w1) + orc.quant_weights(w2)
+    layer = S.MegaMoELayer(H, I, E, K, max_rows=max_rows or max(T, 1), fuse_fc1=fuse,
+                           emit_fc1=emit, capacity_factor=cf)
+    layer.bind_weights(q1, s1, q2, s2)
+    return layer, wo
+
+
+@pytest.mark.parametrize("T,H,I,E,K,mask,empty,fuse", [
+    (77, 256, 384, 6, 2, 0.0, (), True),        # ragged T, odd I/128, H/256 with a half tile
+    (77, 384, 256, 6, 2, 0.0, (), False),       # H % 256 == 128: FC2's last N tile is half
+    (300, 512, 256, 16, 4, 0.25, (3, 7, 11), True),   # masked slots and empty experts
+    (1, 256, 128, 4, 1, 0.0, (), True),         # one token, top-1
+    (130, 256, 256, 64, 8, 0.1, tuple(range(40)), False),  # many empty experts, top-8
+    (513, 1024, 512, 8, 6, 0.05, (), True),     # several m-tiles per expert
+])
+def test_edge_shapes(lib, orc, T, H, I, E, K, mask, empty, fuse):
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=T + H, mask=mask, empty=empty)
+    layer, wo = layer_from_float(lib, orc, T, H, I, E, K, w1, w2, fuse=fuse)
+    ref = orc.forward(x, idx, w, *wo)
+    xt, it, wt = gh.to_device(x, idx, w)
+    out = layer.forward(xt, it, wt)
+    st, bits = layer.read_status()
+    assert st == 0 and bits == 0
+    dbg = layer.debug()
+    rows = check_routing(dbg, ref, T, K)
+    check_quant(lib, dbg, ref["xq"], ref["xs"], ref["perm"], rows, K)
+    compare_outputs(dbg, out, ref, rows)
+    for e in empty:
+        assert int(dbg["counts"][e].item()) == 0
+
+
+def test_all_masked_and_nan_masked_weights(lib, orc):
+    T, H, I, E, K = 40, 256, 256, 8, 2
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=5)
+    layer, wo = layer_from_float(lib, orc, T, H, I, E, K, w1, w2)
+    xt, it, wt = gh.to_device(x, np.full_like(idx, -1), w)
+    out = layer.forward(xt, it, wt)
+    assert layer.read_status() == (0, 0)
+    assert torch.count_nonzero(out.view(torch.int16)).item() == 0   # +0 everywhere
+    idxm = idx.copy()
+    idxm[::2, 1] = -1
+    wn = w.copy()
+    wn[::2, 1] = np.nan
+    ref = orc.forward(x, idxm, wn, *wo)
+    xt, it, wt = gh.to_device(x, idxm, wn)
+    out = layer.forward(xt, it, wt)
+    assert layer.read_status() == (0, 0)
+    compare_outputs(layer.debug(), out, ref, np.zeros(0, np.int64), check_gu=False)
+
+
+def test_route_errors_set_status(lib, orc):
+    import serving_route_gb300.binding as B
+    T, H, I, E, K = 16, 256, 128, 4, 2
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=9)
+    layer, _ = layer_from_float(lib, orc, T, H, I, E, K, w1, w2)
+    cases = []
+    bad = idx.copy(); bad[3, 0] = E; cases.append((bad, w, B.MOE_DEV_ROUTE_RANGE))
+    bad = idx.copy(); bad[4, 0] = -7; cases.append((bad, w, B.MOE_DEV_ROUTE_RANGE))
+    bad = idx.copy(); bad[5, 1] = bad[5, 0]; cases.append((bad, w, B.MOE_DEV_ROUTE_DUP))
+    wb = w.copy(); wb[6, 1] = np.inf; cases.append((idx, wb, B.MOE_DEV_ROUTE_NONFINITE))
+    for bi, bw, bit in cases:
+        xt, it, wt = gh.to_device(x, bi, bw)
+        layer.forward(xt, it, wt)
+        st, bits = layer.read_status()
+        assert st == B.MOE_ERR_BAD_ROUTE and bits == bit, (st, bits, bit)
+        assert orc.route(bi, bw, E)["err"] == bit
+    # a clean forward clears the word again
+    xt, it, wt = gh.to_device(x, idx, w)
+    layer.forward(xt, it, wt)
+    assert layer.read_status() == (0, 0)
+
+
+def test_host_errors_and_zero_tokens(lib, orc):
+    import serving_route_gb300.binding as B
+    T, H, I, E, K = 8, 256, 128, 4, 2
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=10)
+    layer, _ = layer_from_float(lib, orc, T, H, I, E, K, w1, w2)
+    xt, it, wt = gh.to_device(x, idx, w)
+    sp = torch.cuda.current_stream().cuda_stream
+    assert B.moe_forward_status(layer.handle, xt.data_ptr(), it.data_ptr(), wt.data_ptr(), T + 1,
+                                sp) == B.MOE_ERR_CAPACITY
+    assert B.moe_forward_status(layer.handle, xt.data_ptr(), it.data_ptr(), wt.data_ptr(), -1,
+                                sp) == B.MOE_ERR_INVALID_ARG
+    before = layer.out.clone()
+    assert B.moe_forward_status(layer.handle, 0, 0, 0, 0, sp) == B.MOE_OK
+    torch.cuda.synchronize()
+    assert torch.equal(before.view(torch.int16), layer.out.view(torch.int16))
+    # unbound weights
+    fresh = lib.MegaMoELayer(H, I, E, K, max_rows=T)
+    assert B.moe_forward_status(fresh.handle, xt.data_ptr(), it.data_ptr(), wt.data_ptr(), T,
+                                sp) == B.MOE_ERR_NOT_BOUND
+    # non power-of-two scale refused at bind time
+    q = torch.zeros((E, 2 * I, H), dtype=torch.uint8, device="cuda")
+    s1 = torch.ones((E, 2 * I // 128, H // 128), dtype=torch.float32, device="cuda")
+    q2 = torch.zeros((E, H, I), dtype=torch.uint8, device="cuda")
+    s2 = torch.ones((E, H // 128, I // 128), dtype=torch.float32, device="cuda")
+    s2[1, 0, 0] = 3.0
+    with pytest.raises(B.MoEError) as ei:
+        fresh.bind_weights(q, s1, q2, s2)
+    assert ei.value.status == B.MOE_ERR_BAD_SCALE
+
+
+def test_capacity_overflow_is_reported(lib, orc):
+    import serving_route_gb300.binding as B
+    T, H, I, E, K = 256, 256, 128, 2, 2
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=11)
+    layer, _ = layer_from_float(lib, orc, T, H, I, E, K, w1, w2, cf=0.25)
+    xt, it, wt = gh.to_device(x, idx, w)
+    layer.forward(xt, it, wt)
+    st, bits = layer.read_status()
+    assert st == B.MOE_ERR_CAPACITY and bits == B.MOE_DEV_CAPACITY
+
+
+def test_cuda_graph_replay_with_tail_masking(lib, orc):
+    T, H, I, E, K = 96, 512, 256, 8, 2
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=12)
+    layer, wo = layer_from_float(lib, orc, T, H, I, E, K, w1, w2, fuse=True, emit=False)
+    xt, it, wt = gh.to_device(x, idx, w)
+    layer.forward(xt, it, wt)        # warm-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s, capture_error_mode="global"):
+            layer.forward(xt, it, wt, stream=s)
+    for live in (T, 50, 1):
+        idx2 = idx.copy()
+        idx2[live:] = -1                                   # tail masking
+        it.copy_(torch.from_numpy(idx2).cuda())
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = orc.forward(x, idx2, w, *wo)
+        o = gh.bf16_np(layer.out[:T])
+        r = gh.bits_to_f64(ref["out"])
+        assert gh.rel_l2(o, r) <= OUT_TOL
+        assert np.all(o[live:] == 0)
+    # a replay observes the routing checker on the rebound inputs
+    idx3 = idx.copy()
+    idx3[0, 0] = E + 3
+    it.copy_(torch.from_numpy(idx3).cuda())
+    graph.replay()
+    st, bits = layer.read_status(stream=s)
+    assert bits & 0x1
+
+
+def test_token_permutation_and_pow2_weight_scaling(lib, orc):
+    T, H, I, E, K = 64, 256, 256, 8, 2
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=13)
+    layer, _ = layer_from_float(lib, orc, T, H, I, E, K, w1, w2)
+    xt, it, wt = gh.to_device(x, idx, w)
+    base = layer.forward(xt, it, wt).clone()
+    p = np.random.default_rng(1).permutation(T)
+    xt2, it2, wt2 = gh.to_device(x[p], idx[p], w[p])
+    perm_out = layer.forward(xt2, it2, wt2).clone()
+    assert torch.equal(perm_out.view(torch.int16), base[torch.from_numpy(p).cuda()].view(torch.int16))
+    xt3, it3, wt3 = gh.to_device(x, idx, w * 2)
+    dbl = layer.forward(xt3, it3, wt3).clone()
+    assert torch.equal(dbl.float(), base.float() * 2)
