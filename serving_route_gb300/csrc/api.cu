@@ -366,6 +366,8 @@ moe_status moe_set_profile_events(moe_handle* h, void* const* events, int32_t n)
     return MOE_OK;
   }
   if (n != 10 || !events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 10; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
   for (int i = 0; i < 10; ++i) h->ev[i] = reinterpret_cast<cudaEvent_t>(events[i]);
   h->n_ev = 10;
   return MOE_OK;

@@ -87,7 +87,12 @@ __device__ __forceinline__ float swiglu(float g, float u) {
 // Profiling events are recorded as external event nodes when the stream is
 // being captured, so per-kernel timing also works inside CUDA graphs.
 static inline void record_event(cudaEvent_t ev, cudaStream_t s) {
-  cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
 }
 
 __device__ __forceinline__ void record_status(uint32_t* status, uint32_t bits) {

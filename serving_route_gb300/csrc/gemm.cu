@@ -31,7 +31,8 @@
 namespace mm {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                       // two per TMEM lane quadrant
+constexpr int kThreads = 64 + 32 * kEpiWarps;      // producer, MMA, epilogue
 constexpr uint32_t kOffA = 0;                    // 128 rows x 128 B
 constexpr uint32_t kOffB = 16384;                // 256 rows x 128 B
 constexpr uint32_t kOffSfa = 49152;              // one 512 B atom
@@ -39,7 +40,13 @@ constexpr uint32_t kOffSfb = 49664;              // two 512 B atoms
 constexpr uint32_t kStageBytes = 51200;          // multiple of 1024
 constexpr uint32_t kTxBytes = 16384 + 32768 + 512;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColSfa = 256, kColSfb0 = 260, kColSfb1 = 264;
+// Scale factors live in TMEM after the accumulator (columns 0-255): one
+// 16-column slot per pipeline stage (A atom at +0, B atoms at +8 and +12), so
+// the copy for stage s+1 never overwrites scales the MMAs of stage s still read.
+constexpr uint32_t kColSf = 256, kSfSlotCols = 16;
+// One M=128 x N=256 MMA per 32-wide K chunk (B scales of the two 128-row
+// blocks in adjacent 4-column groups); false issues two N=128 MMAs instead.
+constexpr bool kSingleN256 = true;
 constexpr size_t kDynSmem = (size_t)kStages * kStageBytes + 1024;
 
 template <int MODE>
@@ -50,9 +57,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ __align__(8) uint64_t accf_bar, acce_bar, drain_bar;
+  __shared__ __align__(8) uint64_t amax_bar[4];  // per quadrant: both column halves posted
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ uint8_t sfb_sm[2][2][128];
+  __shared__ float amax_sh[2][2][128];  // [tile parity][column half][row] (fused epilogue)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -68,8 +77,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     mbar_init(smem_u32(&accf_bar), 1);
-    mbar_init(smem_u32(&acce_bar), 4);
+    mbar_init(smem_u32(&acce_bar), kEpiWarps);
     mbar_init(smem_u32(&drain_bar), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&amax_bar[i]), 2);
     abort_sh = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmA);
@@ -87,11 +97,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Per tile the producer needs the expert id (a global table) and the
+    // tile's weight-scale bytes.  Both are fetched ahead: the expert id two
+    // tiles ahead, the scale bytes one tile ahead, so no dependent global load
+    // stalls the producer at a tile boundary.
+    auto expert_of = [&](int tile) -> int {
+      return tile < total ? g.mtile_expert[tile / g.NT] : 0;
+    };
     uint32_t nb0[4], nb1[4];
-    auto fetch_sfb = [&](int tile) {
+    auto fetch_sfb = [&](int tile, int e) {
       if (tile < total) {
-        const int mt = tile / g.NT, nt = tile - (tile / g.NT) * g.NT;
-        const int e = g.mtile_expert[mt];
+        const int nt = tile - (tile / g.NT) * g.NT;
         const uint8_t* p = g.sfb + ((int64_t)e * g.NB + 2 * nt) * g.KB;
         const bool has1 = 2 * nt + 1 < g.NB;
 #pragma unroll
@@ -110,17 +126,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
+    // weight rows of a tile: expert e, 256-row n-tile
+    auto b_row = [&](int tile, int e) { return e * g.N + (tile - (tile / g.NT) * g.NT) * 256; };
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued at least once, parity of last issue
     int buf = 0;
-    fetch_sfb(blockIdx.x);
+    const int G = gridDim.x;
+    int e_cur = expert_of(blockIdx.x);
+    int e_next = expert_of(blockIdx.x + G);
+    fetch_sfb(blockIdx.x, e_cur);
     stash_sfb(0);
-    for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
-      const int mt = tile / g.NT, nt = tile - (tile / g.NT) * g.NT;
-      const int e = g.mtile_expert[mt];
-      fetch_sfb(tile + gridDim.x);  // next tile's weight scales, consumed after this loop
-      const int y_b = e * g.N + nt * 256;
+    for (int tile = blockIdx.x; tile < total && !*abort; tile += G) {
+      const int mt = tile / g.NT;
+      const int e = e_cur;
+      const int e_after = expert_of(tile + 2 * G);  // needed one tile from now
+      fetch_sfb(tile + G, e_next);                  // consumed after this tile's k loop
+      const int y_b = b_row(tile, e);
       bool ok = true;
       for (int kb = 0; kb < g.KB; ++kb) {
         if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort, g.status)) {
@@ -154,6 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       buf ^= 1;
       stash_sfb(buf);
+      e_cur = e_next;
+      e_next = e_after;
     }
     // Drain: every copy this warp issued must have landed before the CTA exits.
     if (lane == 0) {
@@ -170,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_mxf8_e4m3(128, 128);
+      const uint32_t idesc = idesc_mxf8_e4m3(128, kSingleN256 ? 256 : 128);
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -184,9 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t st = sbase + stage * kStageBytes;
-          tc_cp_sf_atom(tmem + kColSfa, sdesc_sf_atom(st + kOffSfa));
-          tc_cp_sf_atom(tmem + kColSfb0, sdesc_sf_atom(st + kOffSfb));
-          tc_cp_sf_atom(tmem + kColSfb1, sdesc_sf_atom(st + kOffSfb + 512));
+          const uint32_t sf = tmem + kColSf + stage * kSfSlotCols;
+          tc_cp_sf_atom(sf, sdesc_sf_atom(st + kOffSfa));
+          tc_cp_sf_atom(sf + 8, sdesc_sf_atom(st + kOffSfb));
+          tc_cp_sf_atom(sf + 12, sdesc_sf_atom(st + kOffSfb + 512));
           const uint64_t ad = sdesc_k_sw128(st + kOffA);
           const uint64_t bd0 = sdesc_k_sw128(st + kOffB);
           const uint64_t bd1 = sdesc_k_sw128(st + kOffB + 16384);
@@ -194,10 +219,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 4; ++k) {
             const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
             // +32 bytes along K inside the 128-byte swizzle atom = +2 in the address field
-            tc_mma_mxf8(tmem + 0, ad + 2 * k, bd0 + 2 * k, idesc, tmem + kColSfa, tmem + kColSfb0,
-                        acc);
-            tc_mma_mxf8(tmem + 128, ad + 2 * k, bd1 + 2 * k, idesc, tmem + kColSfa,
-                        tmem + kColSfb1, acc);
+            if constexpr (kSingleN256) {
+              tc_mma_mxf8(tmem + 0, ad + 2 * k, bd0 + 2 * k, idesc, sf, sf + 8, acc);
+            } else {
+              tc_mma_mxf8(tmem + 0, ad + 2 * k, bd0 + 2 * k, idesc, sf, sf + 8, acc);
+              tc_mma_mxf8(tmem + 128, ad + 2 * k, bd1 + 2 * k, idesc, sf, sf + 12, acc);
+            }
           }
           tc_commit(smem_u32(&empty_bar[stage]));
           if (++stage == kStages) {
@@ -218,7 +245,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    // Eight warps, two per TMEM lane quadrant; thread = accumulator row, and
+    // the two warps of a quadrant split the columns: FC2 -> columns
+    // [128h, 128h+128); FC1 -> gate [64h, 64h+64) with the matching up
+    // columns [128+64h, 192+64h), i.e. h columns [64h, 64h+64).
+    // Phase 1 drains those 128 FP32 columns into BF16 pairs in registers (one
+    // TMEM wait) and frees the accumulator at once, so the next tile's MMAs
+    // overlap phase 2 (SwiGLU, quantisation, stores).  Every mode rounds the
+    // accumulator to BF16 first: y and gate||up are stored as BF16, and the
+    // fused SwiGLU reads gate/up after the same rounding as the unfused kernel.
+    const int q = warp & 3;          // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;
     const uint32_t tlane = tmem + ((uint32_t)(q * 32) << 16);
     const int row_in_tile = q * 32 + lane;
     uint32_t acc_phase = 0;
@@ -227,108 +264,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(smem_u32(&accf_bar), acc_phase, abort, g.status)) break;
       tc_fence_after();
       const int64_t row = (int64_t)mt * 128 + row_in_tile;
+      // FC2: the second column half of a tile past H holds no output
+      const bool active = !(MODE == kModeY && half == 1 && nt * 256 + 128 >= g.N);
+      uint32_t pk[64];  // BF16 pairs of this warp's 128 accumulator columns
+      if (active) {
+        uint32_t r[4][32];
+        if constexpr (MODE == kModeY) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(tlane + half * 128 + c * 32, r[c]);
+        } else {
+          tmem_ld32(tlane + half * 64, r[0]);
+          tmem_ld32(tlane + half * 64 + 32, r[1]);
+          tmem_ld32(tlane + 128 + half * 64, r[2]);
+          tmem_ld32(tlane + 128 + half * 64 + 32, r[3]);
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[c * 16 + j] =
+                pack_bf16x2(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acce_bar));
+      const uint32_t tile_par = acc_phase;  // alternates per tile
+      acc_phase ^= 1u;
+
       if constexpr (MODE == kModeY) {
-        uint16_t* orow = g.out + row * g.ld_out + (int64_t)nt * 256;
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          if (nt * 256 + c * 32 < g.N) {
-            uint32_t r[32];
-            tmem_ld32(tlane + c * 32, r);
-            tmem_ld_wait();
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        if (active) {
+          uint4* dst = reinterpret_cast<uint4*>(g.out + row * g.ld_out + (int64_t)nt * 256 + half * 128);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-              o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-              o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-              o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-              dst[v] = o;
-            }
-          }
+          for (int v = 0; v < 16; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&acce_bar));
-      } else if constexpr (MODE == kModeGU) {
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tlane + c * 32, r);
-          tmem_ld_wait();
-          const int64_t col = (c < 4) ? ((int64_t)nt * 128 + c * 32)
-                                      : ((int64_t)g.inter + (int64_t)nt * 128 + (c - 4) * 32);
-          uint4* dst = reinterpret_cast<uint4*>(g.out + row * g.ld_out + col);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-            o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-            o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-            o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-            dst[v] = o;
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&acce_bar));
-      } else {
-        float h[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t rg[32], ru[32];
-          tmem_ld32(tlane + c * 32, rg);
-          tmem_ld32(tlane + 128 + c * 32, ru);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float gv = bf16_round(__uint_as_float(rg[j]));
-            const float uv = bf16_round(__uint_as_float(ru[j]));
-            h[c * 32 + j] = swiglu(gv, uv);
-          }
-          if constexpr (MODE == kModeFusedGU) {
-            uint4* dg = reinterpret_cast<uint4*>(g.out + row * g.ld_out + (int64_t)nt * 128 + c * 32);
-            uint4* du = reinterpret_cast<uint4*>(g.out + row * g.ld_out + g.inter +
-                                                 (int64_t)nt * 128 + c * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(rg[8 * v + 0]), __uint_as_float(rg[8 * v + 1]));
-              o.y = pack_bf16x2(__uint_as_float(rg[8 * v + 2]), __uint_as_float(rg[8 * v + 3]));
-              o.z = pack_bf16x2(__uint_as_float(rg[8 * v + 4]), __uint_as_float(rg[8 * v + 5]));
-              o.w = pack_bf16x2(__uint_as_float(rg[8 * v + 6]), __uint_as_float(rg[8 * v + 7]));
-              dg[v] = o;
-              o.x = pack_bf16x2(__uint_as_float(ru[8 * v + 0]), __uint_as_float(ru[8 * v + 1]));
-              o.y = pack_bf16x2(__uint_as_float(ru[8 * v + 2]), __uint_as_float(ru[8 * v + 3]));
-              o.z = pack_bf16x2(__uint_as_float(ru[8 * v + 4]), __uint_as_float(ru[8 * v + 5]));
-              o.w = pack_bf16x2(__uint_as_float(ru[8 * v + 6]), __uint_as_float(ru[8 * v + 7]));
-              du[v] = o;
-            }
-          }
-        }
-        // the accumulator is free as soon as it has been read
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&acce_bar));
-        float amax = 0.f;
-#pragma unroll
-        for (int j = 0; j < 128; ++j) amax = fmaxf(amax, fabsf(h[j]));
-        const int e = pow2_scale_exp(amax);
-        const float inv = pow2_neg(e);
-        uint4* dq = reinterpret_cast<uint4*>(g.hq + row * (int64_t)g.inter + (int64_t)nt * 128);
+      }
+      if constexpr (MODE == kModeGU || MODE == kModeFusedGU) {
+        uint16_t* base = g.out + row * g.ld_out + (int64_t)nt * 128 + half * 64;
+        uint4* dg = reinterpret_cast<uint4*>(base);
+        uint4* du = reinterpret_cast<uint4*>(base + g.inter);
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          uint4 o;
-          o.x = e4m3x4(h[16 * v + 0] * inv, h[16 * v + 1] * inv, h[16 * v + 2] * inv, h[16 * v + 3] * inv);
-          o.y = e4m3x4(h[16 * v + 4] * inv, h[16 * v + 5] * inv, h[16 * v + 6] * inv, h[16 * v + 7] * inv);
-          o.z = e4m3x4(h[16 * v + 8] * inv, h[16 * v + 9] * inv, h[16 * v + 10] * inv, h[16 * v + 11] * inv);
-          o.w = e4m3x4(h[16 * v + 12] * inv, h[16 * v + 13] * inv, h[16 * v + 14] * inv, h[16 * v + 15] * inv);
-          dq[v] = o;
+          dg[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          du[v] = make_uint4(pk[32 + 4 * v], pk[32 + 4 * v + 1], pk[32 + 4 * v + 2], pk[32 + 4 * v + 3]);
         }
-        *reinterpret_cast<uint32_t*>(g.h_sf + sf_atom_offset(row, nt, g.IB)) =
-            (uint32_t)(e + 127) * 0x01010101u;
       }
-      acc_phase ^= 1u;
+      if constexpr (MODE == kModeFused || MODE == kModeFusedGU) {
+        // gate pairs pk[0..31], up pairs pk[32..63] -> h[0..63]
+        float h[64];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          h[2 * i] = swiglu(bf16_bits_to_float(pk[i] & 0xFFFFu), bf16_bits_to_float(pk[32 + i] & 0xFFFFu));
+          h[2 * i + 1] = swiglu(bf16_bits_to_float(pk[i] >> 16), bf16_bits_to_float(pk[32 + i] >> 16));
+          amax = fmaxf(amax, fmaxf(fabsf(h[2 * i]), fabsf(h[2 * i + 1])));
+        }
+        // row amax over both column halves (the two warps of this quadrant),
+        // exchanged through shared memory, double-buffered by tile parity
+        amax_sh[tile_par][half][row_in_tile] = amax;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&amax_bar[q]));
+        if (!mbar_wait_bounded(smem_u32(&amax_bar[q]), tile_par, abort, g.status)) break;
+        amax = fmaxf(amax, amax_sh[tile_par][half ^ 1][row_in_tile]);
+        const int e = pow2_scale_exp(amax);
+        const float inv = pow2_neg(e);
+        uint4* dq = reinterpret_cast<uint4*>(g.hq + row * (int64_t)g.inter + (int64_t)nt * 128 + half * 64);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = 16 * v + 4 * u;
+            w[u] = e4m3x4(h[j] * inv, h[j + 1] * inv, h[j + 2] * inv, h[j + 3] * inv);
+          }
+          dq[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (half == 0)
+          *reinterpret_cast<uint32_t*>(g.h_sf + sf_atom_offset(row, nt, g.IB)) =
+              (uint32_t)(e + 127) * 0x01010101u;
+      }
     }
   }
 

@@ -66,6 +66,12 @@ class MegaMoELayer:
         return B.moe_read_status(self.handle, _stream_ptr(stream))
 
     def set_profile_events(self, events) -> None:
+        """torch.cuda.Event objects (created with enable_timing=True); torch
+        creates the CUDA event lazily, so each is recorded once here first."""
+        if events:
+            for e in events:
+                e.record()
+            torch.cuda.current_stream().synchronize()
         B.moe_set_profile_events(self.handle, [e.cuda_event for e in events] if events else [])
 
     # -- introspection -------------------------------------------------------------
