@@ -194,9 +194,44 @@ MOE_API moe_status moe_debug_views(moe_handle* h, moe_debug_view* out);
  * caller) before its i-th kernel and events[n-1] after the last one, on the
  * forward's stream.  Kernel order: 0 status reset, 1 route_count,
  * 2 route_scan, 3 route_scatter, 4 quant_dispatch, 5 fc1, 6 swiglu_quant
- * (skipped when fused), 7 fc2, 8 combine, 9 end.  n must be 0 or 10.
+ * (skipped when fused), 7 fc2, 8 combine, 9 end.  n must be 0 (profiling off)
+ * or 10, with every handle non-NULL.
  */
 MOE_API moe_status moe_set_profile_events(moe_handle* h, void* const* events, int32_t n);
+
+/*
+ * moe_route_noalloc -- the routing step alone, allocating nothing.  The pages
+ * have no counterpart to this call; it exists for callers that cannot
+ * allocate device memory and have no workspace to offer, for example a plugin
+ * run from inside another runtime's enqueue callback, where cudaMalloc would
+ * synchronise the device and is not allowed, or code that must not grow the
+ * host framework's memory pool.
+ *
+ * Computes what moe_forward's routing kernels compute, into the caller's
+ * buffers: route validation (bits OR-ed into *d_status, which this call first
+ * clears), per-expert counts d_counts [E], the exclusive scan d_offsets
+ * [E+1], and the stable permutation d_perm [num_tokens*top_k] (first
+ * offsets[E] entries meaningful) with its inverse d_inv [num_tokens*top_k]
+ * (-1 for masked slots).  Inputs as for moe_forward.  check_routes != 0 adds
+ * the duplicate and finite-weight checks.
+ *
+ * Scratch: a fixed file-scope device array of about 0.9 MiB, present on every
+ * GPU that loads the library until the process exits.  Limits:
+ * num_tokens * top_k <= 131072, ceil(num_tokens / 128) * num_experts <= 32768,
+ * num_experts <= 1024; larger inputs return MOE_ERR_CAPACITY before anything
+ * is enqueued.  The first call made with a given device current looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it: make that
+ * first call before any stream capture.  Every call uses the same array, so
+ * calls that overlap on the GPU (other streams, other threads) race and
+ * corrupt each other's results: order them on one stream.  The array keeps
+ * the last call's contents; nothing in it needs to start at zero.
+ * num_tokens == 0 returns MOE_OK and writes nothing.  Asynchronous on stream.
+ */
+MOE_API moe_status moe_route_noalloc(const int32_t* d_topk_idx, const float* d_topk_w,
+                                     int64_t num_tokens, int32_t top_k, int32_t num_experts,
+                                     int32_t check_routes, int32_t* d_counts, int32_t* d_offsets,
+                                     int32_t* d_perm, int32_t* d_inv, uint32_t* d_status,
+                                     struct CUstream_st* stream);
 
 MOE_API void moe_destroy(moe_handle* h);
 MOE_API const char* moe_status_str(moe_status s);
