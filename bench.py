@@ -42,6 +42,7 @@ def parse():
     p.add_argument("--config", default="v2lite")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--unfused", action="store_true", help="time the unfused reference path")
+    p.add_argument("--gemm", default="auto", choices=["auto", "single", "pair"])
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
@@ -203,7 +204,7 @@ def main():
     fused = not args.unfused
 
     layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, expected_m=wl.T,
-                           fuse_fc1=fused, check_routes=True)
+                           fuse_fc1=fused, check_routes=True, gemm=args.gemm)
     # weights: generated and quantised on the GPU, bound once
     w1q = torch.empty((wl.E, 2 * wl.I, wl.H), dtype=torch.uint8, device=dev)
     w1s = torch.empty((wl.E, 2 * wl.I // 128, wl.H // 128), dtype=torch.float32, device=dev)
@@ -241,6 +242,7 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
+    dbg = layer.debug()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
     layer.set_profile_events(ev)
 
@@ -388,6 +390,7 @@ def main():
                    "fc1_epilogue": "fused" if fused else "unfused",
                    "l2": "flushed before every step (256 MiB write, untimed)",
                    "launch": "cuda graph replay" if graph is not None else "direct launches",
+                   "gemm": ("cta pairs" if dbg["gemm_pair"] else "single cta") + f" x{dbg['gemm_ctas']}",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": world * wl.T * K / (total_ms * 1e-3),
         "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,

@@ -65,6 +65,13 @@ typedef enum moe_status {
 #define MOE_FLAG_FUSE_FC1_EPILOGUE 0x1u /* SwiGLU + 1x128 quant inside the FC1 epilogue (opt-in) */
 #define MOE_FLAG_CHECK_ROUTES 0x2u      /* duplicate / finite-weight checks (range check always on) */
 #define MOE_FLAG_EMIT_FC1 0x4u          /* also keep the BF16 gate||up FC1 output (debug) */
+/* GEMM tactic.  Default: one CTA per SM (expert segments padded to 128 rows).
+ * MOE_FLAG_GEMM_CTA_PAIR runs the GEMMs on CTA pairs (tcgen05 cta_group::2,
+ * M = 256, segments padded to 256 rows); it is correct but measured slower on
+ * GB300, and its padding needs a larger workspace (pass the same flags to the
+ * query and to moe_create).  expected_m never changes a buffer size. */
+#define MOE_FLAG_GEMM_SINGLE_CTA 0x8u
+#define MOE_FLAG_GEMM_CTA_PAIR 0x10u
 
 typedef struct moe_dims {
   int32_t hidden;      /* H: multiple of 128, 128..16384 */
@@ -184,6 +191,9 @@ typedef struct moe_debug_view {
   uint16_t* y;             /* [rows_alloc, H] BF16 FC2 output per padded row */
   int64_t rows_alloc;      /* padded-row capacity (multiple of 128) */
   int32_t sf_atom_bytes;   /* 512: 128 rows x 4 bytes, byte (r%32)*16 + (r/32)*4 + j */
+  int32_t gemm_pair;       /* 1: GEMMs run on CTA pairs (cta_group::2), 0: one CTA per SM */
+  int32_t gemm_ctas;       /* grid size of the GEMM launches */
+  int32_t pad_rows;        /* rows each expert's GEMM segment is padded to */
 } moe_debug_view;
 
 MOE_API moe_status moe_debug_views(moe_handle* h, moe_debug_view* out);

@@ -35,6 +35,8 @@ MOE_DEV_BAD_SCALE = 0x20
 MOE_FLAG_FUSE_FC1_EPILOGUE = 0x1
 MOE_FLAG_CHECK_ROUTES = 0x2
 MOE_FLAG_EMIT_FC1 = 0x4
+MOE_FLAG_GEMM_SINGLE_CTA = 0x8
+MOE_FLAG_GEMM_CTA_PAIR = 0x10
 
 # every function the header declares (checked against include/megamoe.h by a test)
 API_NAMES = ("moe_workspace_query", "moe_create", "moe_quantize_weights", "moe_bind_weights",
@@ -54,7 +56,9 @@ class moe_debug_view(ctypes.Structure):
                 ("perm", ctypes.c_void_p), ("inv", ctypes.c_void_p), ("inv_pad", ctypes.c_void_p),
                 ("a", ctypes.c_void_p), ("a_sf", ctypes.c_void_p), ("gu", ctypes.c_void_p),
                 ("hq", ctypes.c_void_p), ("h_sf", ctypes.c_void_p), ("y", ctypes.c_void_p),
-                ("rows_alloc", ctypes.c_int64), ("sf_atom_bytes", ctypes.c_int32)]
+                ("rows_alloc", ctypes.c_int64), ("sf_atom_bytes", ctypes.c_int32),
+                ("gemm_pair", ctypes.c_int32), ("gemm_ctas", ctypes.c_int32),
+                ("pad_rows", ctypes.c_int32)]
 
 
 class MoEError(RuntimeError):

@@ -23,7 +23,10 @@ struct moe_handle {
   int64_t expected_m;
   Workspace ws;
   WeightStore wst;
-  CUtensorMap tm_a, tm_hq, tm_w1, tm_w2;
+  CUtensorMap tm_a, tm_hq, tm_w1, tm_w2;   // weight maps: 256-row boxes (single CTA)
+  CUtensorMap tm_w1p, tm_w2p;               // weight maps: 128-row boxes (CTA pairs)
+  CUtensorMap tm_asf, tm_hsf;               // scale atoms as 2-D uint32 tensors (CTA pairs)
+  int pair_ctas;                            // grid of the CTA-pair GEMMs
   bool bound;
   uint16_t* out;
   int num_sms;
@@ -74,12 +77,29 @@ bool encode_u8_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale atoms [n_atoms][512 B] as a 2-D uint32 tensor [n_atoms, 128]; one
+// atom per box, no swizzle.
+bool encode_atom_map(CUtensorMap* m, const void* base, uint64_t n_atoms) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, n_atoms};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 namespace mm {
 
-moe_status compute_layout(const moe_dims* d, int64_t max_rows, float cf, Layout* L) {
+moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_rows, float cf,
+                          Layout* L) {
   if (!valid_dims(d)) return MOE_ERR_UNSUPPORTED;
+  if ((d->flags & MOE_FLAG_GEMM_SINGLE_CTA) && (d->flags & MOE_FLAG_GEMM_CTA_PAIR))
+    return MOE_ERR_INVALID_ARG;
   if (max_rows < 1 || max_rows > (int64_t)1 << 24) return MOE_ERR_INVALID_ARG;
   if (!(cf > 0.f) || !(cf <= 64.f)) return MOE_ERR_INVALID_ARG;
   memset(L, 0, sizeof(*L));
@@ -88,13 +108,25 @@ moe_status compute_layout(const moe_dims* d, int64_t max_rows, float cf, Layout*
   L->E = d->num_experts;
   L->K = d->top_k;
   L->max_rows = max_rows;
+  // tactic (flashinfer PR #4069, Contracts: expected_m selects the tactic and
+  // max_rows / capacity_factor the memory bound, independently)
+  // Measured on GB300: a CTA pair runs each SM's share of an M256 MMA no
+  // faster than one CTA runs M128, and pays cross-SM hand-offs, so the
+  // automatic choice is one CTA per SM for every expected_m; pairs are opt-in.
+  (void)expected_m;
+  L->pair = (d->flags & MOE_FLAG_GEMM_CTA_PAIR) != 0;
+  L->pad_rows = L->pair ? 256 : 128;
   const int64_t rk = max_rows * L->K;
   int64_t cap = (int64_t)std::ceil((double)cf * (double)rk);
   if (cap > rk) cap = rk;
   if (cap < 1) cap = 1;
   L->cap_rows = cap;
-  const int64_t pad = cap + 127 * (cap < L->E ? cap : (int64_t)L->E);
-  L->rows_alloc = (int64_t)align_up((size_t)(pad < 128 ? 128 : pad), 128);
+  // capacity: routed rows plus at most pad_rows - 1 padding rows per non-empty
+  // expert (buffer sizes depend on max_rows, capacity_factor and the flags,
+  // never on expected_m)
+  const int64_t pad = cap + (L->pad_rows - 1) * (cap < L->E ? cap : (int64_t)L->E);
+  L->rows_alloc = (int64_t)align_up((size_t)(pad < L->pad_rows ? L->pad_rows : pad),
+                                    (size_t)L->pad_rows);
   if (L->rows_alloc > ((int64_t)1 << 31) - 256) return MOE_ERR_INVALID_ARG;
   L->nb_max = (max_rows + 127) / 128;
   L->keep_gu = !(d->flags & MOE_FLAG_FUSE_FC1_EPILOGUE) || (d->flags & MOE_FLAG_EMIT_FC1);
@@ -142,7 +174,7 @@ moe_status moe_workspace_query(const moe_dims* dims, int64_t expected_m, int64_t
   if (!dims || !workspace_bytes || !weight_bytes) return MOE_ERR_INVALID_ARG;
   if (expected_m < 1) return MOE_ERR_INVALID_ARG;
   Layout L;
-  const moe_status st = compute_layout(dims, max_rows, capacity_factor, &L);
+  const moe_status st = compute_layout(dims, expected_m, max_rows, capacity_factor, &L);
   if (st != MOE_OK) return st;
   *workspace_bytes = L.ws_bytes;
   *weight_bytes = L.w_bytes;
@@ -156,7 +188,7 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   *out = nullptr;
   if (!dims || !d_workspace || !d_weight_store || expected_m < 1) return MOE_ERR_INVALID_ARG;
   Layout L;
-  moe_status st = compute_layout(dims, max_rows, capacity_factor, &L);
+  moe_status st = compute_layout(dims, expected_m, max_rows, capacity_factor, &L);
   if (st != MOE_OK) return st;
   if (workspace_bytes < L.ws_bytes || weight_bytes < L.w_bytes) return MOE_ERR_WORKSPACE;
   int dev = 0, major = 0, minor = 0, sms = 0;
@@ -202,9 +234,18 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   h->wst.w1_sf = wb + L.o_w1_sf;
   h->wst.w2_sf = wb + L.o_w2_sf;
   if (!encode_u8_map(&h->tm_a, w.a, L.H, L.rows_alloc, 128) ||
-      !encode_u8_map(&h->tm_hq, w.hq, L.I, L.rows_alloc, 128)) {
+      !encode_u8_map(&h->tm_hq, w.hq, L.I, L.rows_alloc, 128) ||
+      !encode_atom_map(&h->tm_asf, w.a_sf, (uint64_t)(L.rows_alloc / 128) * (L.H / 128)) ||
+      !encode_atom_map(&h->tm_hsf, w.h_sf, (uint64_t)(L.rows_alloc / 128) * (L.I / 128))) {
     delete h;
     return MOE_ERR_CUDA;
+  }
+  if (h->L.pair) {
+    const int pairs = gemm_max_pairs();
+    if (pairs <= 0)
+      h->L.pair = false;  // no co-resident CTA pairs: single-CTA kernel on the same layout
+    else
+      h->pair_ctas = 2 * pairs;
   }
   *out = h;
   return MOE_OK;
@@ -238,7 +279,9 @@ moe_status moe_bind_weights(moe_handle* h, const uint8_t* d_w1, const float* d_w
     return MOE_ERR_CUDA;
   if (st & MOE_DEV_BAD_SCALE) return MOE_ERR_BAD_SCALE;
   if (!encode_u8_map(&h->tm_w1, h->wst.w1, L.H, (uint64_t)L.E * 2 * L.I, 256) ||
-      !encode_u8_map(&h->tm_w2, h->wst.w2, L.I, (uint64_t)L.E * L.H, 256))
+      !encode_u8_map(&h->tm_w2, h->wst.w2, L.I, (uint64_t)L.E * L.H, 256) ||
+      !encode_u8_map(&h->tm_w1p, h->wst.w1, L.H, (uint64_t)L.E * 2 * L.I, 128) ||
+      !encode_u8_map(&h->tm_w2p, h->wst.w2, L.I, (uint64_t)L.E * L.H, 128))
     return MOE_ERR_CUDA;
   h->bound = true;
   return MOE_OK;
@@ -296,7 +339,11 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g1.status = ws.status;
   const GemmMode m1 = fused ? (emit ? kModeFusedGU : kModeFused) : kModeGU;
   if (ev) record_event(ev[5], s);
-  if (launch_gemm(m1, &h->tm_a, &h->tm_w1, g1, h->num_sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const bool pair = L.pair;
+  const int ctas = pair ? h->pair_ctas : h->num_sms;
+  if (launch_gemm(m1, pair, &h->tm_a, pair ? &h->tm_w1p : &h->tm_w1, &h->tm_asf, g1, ctas, s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
   if (ev) record_event(ev[6], s);
   if (!fused && launch_swiglu_quant(ws, L, h->num_sms, s) != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -315,7 +362,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.ld_out = L.H;
   g2.status = ws.status;
   if (ev) record_event(ev[7], s);
-  if (launch_gemm(kModeY, &h->tm_hq, &h->tm_w2, g2, h->num_sms, s) != cudaSuccess)
+  if (launch_gemm(kModeY, pair, &h->tm_hq, pair ? &h->tm_w2p : &h->tm_w2, &h->tm_hsf, g2, ctas,
+                  s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[8], s);
   if (launch_combine(ws, L, d_topk_w, h->out, num_tokens, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -356,6 +404,9 @@ moe_status moe_debug_views(moe_handle* h, moe_debug_view* v) {
   v->y = w.y;
   v->rows_alloc = h->L.rows_alloc;
   v->sf_atom_bytes = kSfAtomBytes;
+  v->gemm_pair = h->L.pair ? 1 : 0;
+  v->gemm_ctas = h->L.pair ? h->pair_ctas : h->num_sms;
+  v->pad_rows = h->L.pad_rows;
   return MOE_OK;
 }
 

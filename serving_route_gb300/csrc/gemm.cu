@@ -10,16 +10,27 @@
 //    128x128 weight scale is one byte for 128 rows; the tensor core applies
 //    them exactly while it accumulates in FP32 in tensor memory.  No
 //    per-K-block promotion through registers is needed.
-//  * Persistent CTAs (one per SM) walk a static tile list: 128 padded rows of
-//    one expert x 256 output columns, expert-major, so the two-or-more
-//    m-tiles sharing a weight tile run at the same time and hit it in L2.
-//    The tile count and the m-tile -> expert table come from device memory:
-//    no host synchronisation, graph-capturable.
-//  * Warp roles (192 threads): warp 0 feeds a 4-stage shared-memory ring with
-//    TMA (A 128x128 B, B 256x128 B, 128-byte swizzle) plus a bulk copy of the
-//    A scale atom; it writes the B scale atoms itself.  One thread of warp 1
-//    copies the atoms into TMEM (tcgen05.cp) and issues the MMAs.  Warps 2-5
-//    drain the 128x256 FP32 accumulator from TMEM and run the epilogue.
+//  * Persistent CTAs walk a static tile list: 128 padded rows of one expert x
+//    256 output columns, expert-major, so the m-tiles sharing a weight tile
+//    run at the same time and hit it in L2.  The tile count and the m-tile ->
+//    expert table come from device memory: no host synchronisation,
+//    graph-capturable.
+//  * Two variants (template PAIR):
+//    - single CTA: one CTA per SM, M128 x N256 per MMA; a 4-stage ring of
+//      48 KB stages (A 128x128 B, B 256x128 B, 128-byte swizzle).
+//    - CTA pair (tcgen05 cta_group::2): two CTAs on the two SMs of a cluster
+//      compute M256 x N256; each stages its own 128 A rows and half of the
+//      256 B rows (32 KB per K block instead of 48 KB), which is what bounds
+//      the MMA rate here (the tensor core is limited by its shared-memory
+//      operand bytes), and allows a 6-stage ring.  Both producers' TMA loads
+//      complete on the leader CTA's barrier; the leader issues the scale
+//      copies and MMAs for the pair and multicasts its commits to both CTAs;
+//      each CTA drains its own 128 accumulator rows.  Expert segments are
+//      padded to 256 rows so a pair tile never straddles two experts.
+//  * Warp roles (320 threads): warp 0 producer (TMA + the B scale atoms it
+//    writes itself), one thread of warp 1 issues the scale copies
+//    (tcgen05.cp) and MMAs, warps 2-9 the epilogue (two per TMEM lane
+//    quadrant).
 //  * Epilogues: FC2 -> BF16 y; FC1 unfused -> BF16 gate||up; FC1 fused ->
 //    BF16-rounded gate/up, SwiGLU, 1x128 re-quantisation to E4M3 + E8M0 atoms
 //    (bit-equal to the unfused path, which runs the same device functions).
@@ -30,29 +41,34 @@
 
 namespace mm {
 
-constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;                       // two per TMEM lane quadrant
-constexpr int kThreads = 64 + 32 * kEpiWarps;      // producer, MMA, epilogue
-constexpr uint32_t kOffA = 0;                    // 128 rows x 128 B
-constexpr uint32_t kOffB = 16384;                // 256 rows x 128 B
-constexpr uint32_t kOffSfa = 49152;              // one 512 B atom
-constexpr uint32_t kOffSfb = 49664;              // two 512 B atoms
-constexpr uint32_t kStageBytes = 51200;          // multiple of 1024
-constexpr uint32_t kTxBytes = 16384 + 32768 + 512;
+constexpr int kEpiWarps = 8;                   // two per TMEM lane quadrant
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 constexpr uint32_t kTmemCols = 512;
 // Scale factors live in TMEM after the accumulator (columns 0-255): one
 // 16-column slot per pipeline stage (A atom at +0, B atoms at +8 and +12), so
 // the copy for stage s+1 never overwrites scales the MMAs of stage s still read.
 constexpr uint32_t kColSf = 256, kSfSlotCols = 16;
-// One M=128 x N=256 MMA per 32-wide K chunk (B scales of the two 128-row
-// blocks in adjacent 4-column groups); false issues two N=128 MMAs instead.
-constexpr bool kSingleN256 = true;
-constexpr size_t kDynSmem = (size_t)kStages * kStageBytes + 1024;
 
-template <int MODE>
+template <bool PAIR>
+struct StageCfg {
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr uint32_t kBRows = PAIR ? 128 : 256;       // B rows staged by this CTA
+  static constexpr uint32_t kOffA = 0;                       // 128 rows x 128 B
+  static constexpr uint32_t kOffB = 16384;                   // kBRows x 128 B
+  static constexpr uint32_t kOffSfa = kOffB + kBRows * 128;  // one 512 B atom
+  static constexpr uint32_t kOffSfb = kOffSfa + 512;         // two 512 B atoms
+  static constexpr uint32_t kStageBytes = (kOffSfb + 1024 + 1023) / 1024 * 1024;
+  static constexpr uint32_t kTxBytes = 16384 + kBRows * 128 + 512;  // per CTA
+  static constexpr size_t kDynSmem = (size_t)kStages * kStageBytes + 1024;
+};
+
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                            const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmSfa, const GemmArgs g) {
+  using C = StageCfg<PAIR>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -67,47 +83,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
   int mtiles = *g.total_mtiles;
   if (mtiles > g.max_mtiles) mtiles = g.max_mtiles;
-  const int total = mtiles * g.NT;
+  // work units: single CTA -> (m-tile, n-tile); pair -> (m-tile pair, n-tile)
+  const int total = (PAIR ? mtiles / 2 : mtiles) * g.NT;
+  const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ustride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  // this CTA's 128-row m-tile of work unit u
+  auto own_mtile = [&](int u) {
+    const int m = u / g.NT;
+    return PAIR ? 2 * m + (int)rank : m;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&full_bar[s]), PAIR ? 2 : 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     mbar_init(smem_u32(&accf_bar), 1);
-    mbar_init(smem_u32(&acce_bar), kEpiWarps);
+    mbar_init(smem_u32(&acce_bar), kEpiWarps * (PAIR ? 2 : 1));
     mbar_init(smem_u32(&drain_bar), 1);
     for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&amax_bar[i]), 2);
     abort_sh = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    if (PAIR) prefetch_tensormap(&tmSfa);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(&tmem_base_sh), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // the peer's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   volatile int* abort = &abort_sh;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Per tile the producer needs the expert id (a global table) and the
+    // Per unit the producer needs the expert id (a global table) and the
     // tile's weight-scale bytes.  Both are fetched ahead: the expert id two
-    // tiles ahead, the scale bytes one tile ahead, so no dependent global load
+    // units ahead, the scale bytes one unit ahead, so no dependent global load
     // stalls the producer at a tile boundary.
-    auto expert_of = [&](int tile) -> int {
-      return tile < total ? g.mtile_expert[tile / g.NT] : 0;
+    auto expert_of = [&](int u) -> int {
+      return u < total ? g.mtile_expert[(PAIR ? 2 : 1) * (u / g.NT)] : 0;
     };
     uint32_t nb0[4], nb1[4];
-    auto fetch_sfb = [&](int tile, int e) {
-      if (tile < total) {
-        const int nt = tile - (tile / g.NT) * g.NT;
+    auto fetch_sfb = [&](int u, int e) {
+      if (u < total) {
+        const int nt = u - (u / g.NT) * g.NT;
         const uint8_t* p = g.sfb + ((int64_t)e * g.NB + 2 * nt) * g.KB;
         const bool has1 = 2 * nt + 1 < g.NB;
 #pragma unroll
@@ -126,44 +159,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    // weight rows of a tile: expert e, 256-row n-tile
-    auto b_row = [&](int tile, int e) { return e * g.N + (tile - (tile / g.NT) * g.NT) * 256; };
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued at least once, parity of last issue
     int buf = 0;
-    const int G = gridDim.x;
-    int e_cur = expert_of(blockIdx.x);
-    int e_next = expert_of(blockIdx.x + G);
-    fetch_sfb(blockIdx.x, e_cur);
+    int e_cur = expert_of(unit0);
+    int e_next = expert_of(unit0 + ustride);
+    fetch_sfb(unit0, e_cur);
     stash_sfb(0);
-    for (int tile = blockIdx.x; tile < total && !*abort; tile += G) {
-      const int mt = tile / g.NT;
+    for (int u = unit0; u < total && !*abort; u += ustride) {
+      const int mt = own_mtile(u);
       const int e = e_cur;
-      const int e_after = expert_of(tile + 2 * G);  // needed one tile from now
-      fetch_sfb(tile + G, e_next);                  // consumed after this tile's k loop
-      const int y_b = b_row(tile, e);
+      const int e_after = expert_of(u + 2 * ustride);  // needed one unit from now
+      fetch_sfb(u + ustride, e_next);                  // consumed after this unit's k loop
+      // weight rows: expert e, 256-row n-tile; a pair CTA stages its half
+      const int y_b = e * g.N + (u - (u / g.NT) * g.NT) * 256 + (int)rank * (int)C::kBRows;
       bool ok = true;
       for (int kb = 0; kb < g.KB; ++kb) {
         if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort, g.status)) {
           ok = false;
           break;
         }
-        uint8_t* st = smem + stage * kStageBytes;
+        uint8_t* st = smem + stage * C::kStageBytes;
         const uint32_t v0 = (uint32_t)sfb_sm[buf][0][kb] * 0x01010101u;
         const uint32_t v1 = (uint32_t)sfb_sm[buf][1][kb] * 0x01010101u;
-        *reinterpret_cast<uint4*>(st + kOffSfb + lane * 16) = make_uint4(v0, v0, v0, v0);
-        *reinterpret_cast<uint4*>(st + kOffSfb + 512 + lane * 16) = make_uint4(v1, v1, v1, v1);
+        *reinterpret_cast<uint4*>(st + C::kOffSfb + lane * 16) = make_uint4(v0, v0, v0, v0);
+        *reinterpret_cast<uint4*>(st + C::kOffSfb + 512 + lane * 16) = make_uint4(v1, v1, v1, v1);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          const uint32_t fb = smem_u32(&full_bar[stage]);
-          const uint32_t sst = sbase + stage * kStageBytes;
-          mbar_arrive_expect_tx(fb, kTxBytes);
-          tma_load_2d(sst + kOffA, &tmA, fb, kb * 128, mt * 128);
-          tma_load_2d(sst + kOffB, &tmB, fb, kb * 128, y_b);
-          bulk_load(sst + kOffSfa, g.sfa + ((int64_t)mt * g.KB + kb) * kSfAtomBytes, kSfAtomBytes,
-                    fb);
+          const uint32_t sst = sbase + stage * C::kStageBytes;
+          if constexpr (PAIR) {
+            // both CTAs' bytes complete on the leader's full barrier
+            const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
+            mbar_arrive_expect_tx_cluster(fb, C::kTxBytes);
+            tma_load_2d_pair(sst + C::kOffA, &tmA, fb, kb * 128, mt * 128);
+            tma_load_2d_pair(sst + C::kOffB, &tmB, fb, kb * 128, y_b);
+            tma_load_2d_pair(sst + C::kOffSfa, &tmSfa, fb, 0, mt * g.KB + kb);
+          } else {
+            const uint32_t fb = smem_u32(&full_bar[stage]);
+            mbar_arrive_expect_tx(fb, C::kTxBytes);
+            tma_load_2d(sst + C::kOffA, &tmA, fb, kb * 128, mt * 128);
+            tma_load_2d(sst + C::kOffB, &tmB, fb, kb * 128, y_b);
+            bulk_load(sst + C::kOffSfa, g.sfa + ((int64_t)mt * g.KB + kb) * kSfAtomBytes,
+                      kSfAtomBytes, fb);
+          }
         }
         __syncwarp();
         issued_mask |= 1u << stage;
@@ -179,8 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       e_cur = e_next;
       e_next = e_after;
     }
-    // Drain: every copy this warp issued must have landed before the CTA exits.
-    if (lane == 0) {
+    // Drain: every copy this CTA issued must have landed before the CTA exits
+    // (the leader's full barriers also count the peer's bytes; the peer is
+    // held by the cluster barrier at the end until the leader has drained).
+    if (lane == 0 && leader) {
       for (int s = 0; s < kStages; ++s) {
         if (!(issued_mask & (1u << s))) continue;
         const uint32_t fb = smem_u32(&full_bar[s]);
@@ -193,51 +235,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_mxf8_e4m3(128, kSingleN256 ? 256 : 128);
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_mxf8_e4m3(PAIR ? 256 : 128, 256);
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        if (!mbar_wait_bounded(smem_u32(&acce_bar), acc_phase ^ 1u, abort, g.status)) break;
+      for (int u = unit0; u < total; u += ustride) {
+        if (!mbar_wait_bounded<PAIR>(smem_u32(&acce_bar), acc_phase ^ 1u, abort, g.status)) break;
         tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < g.KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full_bar[stage]), phase, abort, g.status)) {
+          if (!mbar_wait_bounded<PAIR>(smem_u32(&full_bar[stage]), phase, abort, g.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = sbase + stage * kStageBytes;
+          const uint32_t st = sbase + stage * C::kStageBytes;
           const uint32_t sf = tmem + kColSf + stage * kSfSlotCols;
-          tc_cp_sf_atom(sf, sdesc_sf_atom(st + kOffSfa));
-          tc_cp_sf_atom(sf + 8, sdesc_sf_atom(st + kOffSfb));
-          tc_cp_sf_atom(sf + 12, sdesc_sf_atom(st + kOffSfb + 512));
-          const uint64_t ad = sdesc_k_sw128(st + kOffA);
-          const uint64_t bd0 = sdesc_k_sw128(st + kOffB);
-          const uint64_t bd1 = sdesc_k_sw128(st + kOffB + 16384);
+          const uint64_t ad = sdesc_k_sw128(st + C::kOffA);
+          const uint64_t bd = sdesc_k_sw128(st + C::kOffB);
+          if constexpr (PAIR) {
+            tc_cp_sf_atom_pair(sf, sdesc_sf_atom(st + C::kOffSfa));
+            tc_cp_sf_atom_pair(sf + 8, sdesc_sf_atom(st + C::kOffSfb));
+            tc_cp_sf_atom_pair(sf + 12, sdesc_sf_atom(st + C::kOffSfb + 512));
+          } else {
+            tc_cp_sf_atom(sf, sdesc_sf_atom(st + C::kOffSfa));
+            tc_cp_sf_atom(sf + 8, sdesc_sf_atom(st + C::kOffSfb));
+            tc_cp_sf_atom(sf + 12, sdesc_sf_atom(st + C::kOffSfb + 512));
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
             // +32 bytes along K inside the 128-byte swizzle atom = +2 in the address field
-            if constexpr (kSingleN256) {
-              tc_mma_mxf8(tmem + 0, ad + 2 * k, bd0 + 2 * k, idesc, sf, sf + 8, acc);
-            } else {
-              tc_mma_mxf8(tmem + 0, ad + 2 * k, bd0 + 2 * k, idesc, sf, sf + 8, acc);
-              tc_mma_mxf8(tmem + 128, ad + 2 * k, bd1 + 2 * k, idesc, sf, sf + 12, acc);
-            }
+            if constexpr (PAIR)
+              tc_mma_mxf8_pair(tmem, ad + 2 * k, bd + 2 * k, idesc, sf, sf + 8, acc);
+            else
+              tc_mma_mxf8(tmem, ad + 2 * k, bd + 2 * k, idesc, sf, sf + 8, acc);
           }
-          tc_commit(smem_u32(&empty_bar[stage]));
+          if constexpr (PAIR)
+            tc_commit_pair_multicast(smem_u32(&empty_bar[stage]), 0x3);
+          else
+            tc_commit(smem_u32(&empty_bar[stage]));
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(smem_u32(&accf_bar));
+        if constexpr (PAIR)
+          tc_commit_pair_multicast(smem_u32(&accf_bar), 0x3);
+        else
+          tc_commit(smem_u32(&accf_bar));
         acc_phase ^= 1u;
       }
-      // Drain: all MMAs / TMEM copies of this CTA complete before TMEM is freed.
-      tc_commit(smem_u32(&drain_bar));
+      // Drain: all MMAs / TMEM copies complete before TMEM is freed.
+      if constexpr (PAIR)
+        tc_commit_pair(smem_u32(&drain_bar));
+      else
+        tc_commit(smem_u32(&drain_bar));
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(smem_u32(&drain_bar), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
       }
@@ -258,9 +312,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;
     const uint32_t tlane = tmem + ((uint32_t)(q * 32) << 16);
     const int row_in_tile = q * 32 + lane;
+    // the accumulator-empty barrier lives in the leader CTA
+    const uint32_t acce_addr = PAIR ? mapa_shared(smem_u32(&acce_bar), 0) : smem_u32(&acce_bar);
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const int mt = tile / g.NT, nt = tile - (tile / g.NT) * g.NT;
+    for (int u = unit0; u < total; u += ustride) {
+      const int mt = own_mtile(u);
+      const int nt = u - (u / g.NT) * g.NT;
       if (!mbar_wait_bounded(smem_u32(&accf_bar), acc_phase, abort, g.status)) break;
       tc_fence_after();
       const int64_t row = (int64_t)mt * 128 + row_in_tile;
@@ -288,13 +345,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acce_bar));
+      if (lane == 0) {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(acce_addr);
+        else
+          mbar_arrive(acce_addr);
+      }
       const uint32_t tile_par = acc_phase;  // alternates per tile
       acc_phase ^= 1u;
 
       if constexpr (MODE == kModeY) {
         if (active) {
-          uint4* dst = reinterpret_cast<uint4*>(g.out + row * g.ld_out + (int64_t)nt * 256 + half * 128);
+          uint4* dst =
+              reinterpret_cast<uint4*>(g.out + row * g.ld_out + (int64_t)nt * 256 + half * 128);
 #pragma unroll
           for (int v = 0; v < 16; ++v)
             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
@@ -307,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           dg[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          du[v] = make_uint4(pk[32 + 4 * v], pk[32 + 4 * v + 1], pk[32 + 4 * v + 2], pk[32 + 4 * v + 3]);
+          du[v] = make_uint4(pk[32 + 4 * v], pk[32 + 4 * v + 1], pk[32 + 4 * v + 2],
+                             pk[32 + 4 * v + 3]);
         }
       }
       if constexpr (MODE == kModeFused || MODE == kModeFusedGU) {
@@ -316,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          h[2 * i] = swiglu(bf16_bits_to_float(pk[i] & 0xFFFFu), bf16_bits_to_float(pk[32 + i] & 0xFFFFu));
+          h[2 * i] = swiglu(bf16_bits_to_float(pk[i] & 0xFFFFu),
+                            bf16_bits_to_float(pk[32 + i] & 0xFFFFu));
           h[2 * i + 1] = swiglu(bf16_bits_to_float(pk[i] >> 16), bf16_bits_to_float(pk[32 + i] >> 16));
           amax = fmaxf(amax, fmaxf(fabsf(h[2 * i]), fabsf(h[2 * i + 1])));
         }
@@ -329,14 +394,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         amax = fmaxf(amax, amax_sh[tile_par][half ^ 1][row_in_tile]);
         const int e = pow2_scale_exp(amax);
         const float inv = pow2_neg(e);
-        uint4* dq = reinterpret_cast<uint4*>(g.hq + row * (int64_t)g.inter + (int64_t)nt * 128 + half * 64);
+        uint4* dq =
+            reinterpret_cast<uint4*>(g.hq + row * (int64_t)g.inter + (int64_t)nt * 128 + half * 64);
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           uint32_t w[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = 16 * v + 4 * u;
-            w[u] = e4m3x4(h[j] * inv, h[j + 1] * inv, h[j + 2] * inv, h[j + 3] * inv);
+          for (int uu = 0; uu < 4; ++uu) {
+            const int j = 16 * v + 4 * uu;
+            w[uu] = e4m3x4(h[j] * inv, h[j + 1] * inv, h[j + 2] * inv, h[j + 3] * inv);
           }
           dq[v] = make_uint4(w[0], w[1], w[2], w[3]);
         }
@@ -349,45 +415,85 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // neither CTA frees TMEM the pair still uses
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+template <int MODE, bool PAIR>
+static cudaError_t set_attr() {
+  return cudaFuncSetAttribute(fp8_grouped_gemm_kernel<MODE, PAIR>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)StageCfg<PAIR>::kDynSmem);
 }
 
 cudaError_t gemm_set_attributes() {
   cudaError_t e;
-  e = cudaFuncSetAttribute(fp8_grouped_gemm_kernel<kModeY>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fp8_grouped_gemm_kernel<kModeGU>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fp8_grouped_gemm_kernel<kModeFused>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(fp8_grouped_gemm_kernel<kModeFusedGU>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
+  if ((e = set_attr<kModeY, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<kModeGU, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<kModeFused, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<kModeFusedGU, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<kModeY, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<kModeGU, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<kModeFused, true>()) != cudaSuccess) return e;
+  return set_attr<kModeFusedGU, true>();
 }
 
-cudaError_t launch_gemm(GemmMode mode, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const GemmArgs& g, int num_sms, cudaStream_t s) {
-  const dim3 grid(num_sms), block(kThreads);
-  switch (mode) {
-    case kModeY:
-      fp8_grouped_gemm_kernel<kModeY><<<grid, block, kDynSmem, s>>>(*tmA, *tmB, g);
-      break;
-    case kModeGU:
-      fp8_grouped_gemm_kernel<kModeGU><<<grid, block, kDynSmem, s>>>(*tmA, *tmB, g);
-      break;
-    case kModeFused:
-      fp8_grouped_gemm_kernel<kModeFused><<<grid, block, kDynSmem, s>>>(*tmA, *tmB, g);
-      break;
-    case kModeFusedGU:
-      fp8_grouped_gemm_kernel<kModeFusedGU><<<grid, block, kDynSmem, s>>>(*tmA, *tmB, g);
-      break;
+static void pair_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int ctas,
+                        cudaStream_t s) {
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg->gridDim = dim3(ctas);
+  cfg->blockDim = dim3(kThreads);
+  cfg->dynamicSmemBytes = StageCfg<true>::kDynSmem;
+  cfg->stream = s;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
+// Largest number of CTA pairs that can be resident at once (0 if none).
+int gemm_max_pairs() {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  pair_config(&cfg, attr, 2, nullptr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fp8_grouped_gemm_kernel<kModeY, true>, &cfg) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <int MODE>
+static cudaError_t launch_mode(bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                               const CUtensorMap* tmSfa, const GemmArgs& g, int ctas,
+                               cudaStream_t s) {
+  if (!pair) {
+    fp8_grouped_gemm_kernel<MODE, false><<<ctas, kThreads, StageCfg<false>::kDynSmem, s>>>(
+        *tmA, *tmB, *tmA, g);
+    return cudaGetLastError();
   }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  pair_config(&cfg, attr, ctas, s);
+  return cudaLaunchKernelEx(&cfg, fp8_grouped_gemm_kernel<MODE, true>, *tmA, *tmB, *tmSfa, g);
+}
+
+cudaError_t launch_gemm(GemmMode mode, bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                        const CUtensorMap* tmSfa, const GemmArgs& g, int ctas, cudaStream_t s) {
+  switch (mode) {
+    case kModeY: return launch_mode<kModeY>(pair, tmA, tmB, tmSfa, g, ctas, s);
+    case kModeGU: return launch_mode<kModeGU>(pair, tmA, tmB, tmSfa, g, ctas, s);
+    case kModeFused: return launch_mode<kModeFused>(pair, tmA, tmB, tmSfa, g, ctas, s);
+    case kModeFusedGU: return launch_mode<kModeFusedGU>(pair, tmA, tmB, tmSfa, g, ctas, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace mm

@@ -41,6 +41,8 @@ struct WeightStore {
 
 struct Layout {
   int H, I, E, K;
+  int pad_rows;        // expert segments padded to this many rows (128, or 256 for CTA pairs)
+  bool pair;           // GEMMs run on CTA pairs (tcgen05 cta_group::2)
   int64_t max_rows;
   int64_t cap_rows;    // routed-row capacity before padding
   int64_t rows_alloc;  // padded GEMM rows (multiple of 128)
@@ -54,7 +56,8 @@ struct Layout {
 };
 
 // layout.cpp-style pure host arithmetic (api.cu)
-moe_status compute_layout(const moe_dims* d, int64_t max_rows, float capacity_factor, Layout* L);
+moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_rows,
+                          float capacity_factor, Layout* L);
 
 // route.cu
 cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* topk_idx,
@@ -92,8 +95,12 @@ struct GemmArgs {
   uint32_t* status;
 };
 cudaError_t gemm_set_attributes();
-cudaError_t launch_gemm(GemmMode mode, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const GemmArgs& g, int num_sms, cudaStream_t s);
+int gemm_max_pairs();
+// pair: CTA-pair kernel (tmB boxes of 128 rows, tmSfa = the A scale atoms as a
+// 2-D uint32 tensor); otherwise the single-CTA kernel (tmB boxes of 256 rows).
+// ctas: grid size (an even number for pairs).
+cudaError_t launch_gemm(GemmMode mode, bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                        const CUtensorMap* tmSfa, const GemmArgs& g, int ctas, cudaStream_t s);
 
 // combine.cu
 cudaError_t launch_combine(const Workspace& ws, const Layout& L, const float* topk_w,

@@ -41,43 +41,63 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 p, float (&v)[8]) {
   }
 }
 
-// One warp handles two 128-column blocks of one token per iteration (one per
-// half-warp); each lane owns 8 consecutive columns.
+// One warp handles two 128-column blocks of one token per unit (one per
+// half-warp); each lane owns 8 consecutive columns.  Each iteration processes
+// two units whose loads are issued together, so every warp keeps two 512-byte
+// reads in flight.
+__device__ __forceinline__ void quant_dispatch_unit(const uint4 raw, bool valid, int p_lane,
+                                                    int64_t t, int b, int H, int K, int l16,
+                                                    uint8_t* __restrict__ a,
+                                                    uint8_t* __restrict__ a_sf) {
+  float v[8];
+  if (valid) {
+    unpack_bf16x8(raw, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = half_warp_max(amax);
+  const int e = pow2_scale_exp(amax);
+  const uint2 q = quant8(v, e);
+  const uint32_t sf4 = (uint32_t)(e + 127) * 0x01010101u;
+  const int KB = H >> 7;
+  for (int k = 0; k < K; ++k) {
+    const int p = __shfl_sync(0xFFFFFFFFu, p_lane, k);
+    if (p >= 0 && valid) {
+      *reinterpret_cast<uint2*>(a + (int64_t)p * H + b * 128 + l16 * 8) = q;
+      if (l16 == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_atom_offset(p, b, KB)) = sf4;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pad, int64_t T, int H, int K,
     uint8_t* __restrict__ a, uint8_t* __restrict__ a_sf) {
   const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
   const int KB = H >> 7;
   const int units = (KB + 1) >> 1;
+  const int64_t total = T * units;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < T * units;
-       u += nwarps) {
-    const int64_t t = u / units;
-    const int b = (int)(u - t * units) * 2 + half;
-    const bool valid = b < KB;
-    const int p_lane = (lane < K) ? inv_pad[t * K + lane] : -1;
-    float v[8];
-    if (valid) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(x + t * H + b * 128 + l16 * 8);
-      unpack_bf16x8(raw, v);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.f;
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    amax = half_warp_max(amax);
-    const int e = pow2_scale_exp(amax);
-    const uint2 q = quant8(v, e);
-    const uint32_t sf4 = (uint32_t)(e + 127) * 0x01010101u;
-    for (int k = 0; k < K; ++k) {
-      const int p = __shfl_sync(0xFFFFFFFFu, p_lane, k);
-      if (p >= 0 && valid) {
-        *reinterpret_cast<uint2*>(a + (int64_t)p * H + b * 128 + l16 * 8) = q;
-        if (l16 == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_atom_offset(p, b, KB)) = sf4;
-      }
-    }
+  for (int64_t u0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u0 < total;
+       u0 += 2 * nwarps) {
+    const int64_t u1 = u0 + nwarps;
+    const bool has1 = u1 < total;
+    const int64_t t0 = u0 / units, t1 = has1 ? u1 / units : t0;
+    const int b0 = (int)(u0 - t0 * units) * 2 + half;
+    const int b1 = has1 ? (int)(u1 - t1 * units) * 2 + half : b0;
+    const bool v0 = b0 < KB, v1 = has1 && b1 < KB;
+    // both units' loads first
+    const uint4 r0 = v0 ? *reinterpret_cast<const uint4*>(x + t0 * H + b0 * 128 + l16 * 8)
+                        : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 r1 = v1 ? *reinterpret_cast<const uint4*>(x + t1 * H + b1 * 128 + l16 * 8)
+                        : make_uint4(0u, 0u, 0u, 0u);
+    const int p0 = (lane < K) ? inv_pad[t0 * K + lane] : -1;
+    const int p1 = (lane < K && has1) ? inv_pad[t1 * K + lane] : -1;
+    quant_dispatch_unit(r0, v0, p0, t0, b0, H, K, l16, a, a_sf);
+    quant_dispatch_unit(r1, v1, p1, t1, b1, H, K, l16, a, a_sf);
   }
 }
 

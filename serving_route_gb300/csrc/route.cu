@@ -7,8 +7,9 @@
 //
 // Three small kernels, no host synchronisation:
 //   route_count   per 128-token block: validate, per-block expert histogram
-//   route_scan    one CTA: expert totals, unpadded and 128-padded exclusive
-//                 scans, per-block bases, the m-tile -> expert table
+//   route_scan    one CTA: expert totals, unpadded and padded (128 or 256
+//                 rows per GEMM segment) exclusive scans, per-block bases,
+//                 the 128-row m-tile -> expert table
 //   route_scatter per 128-token block: stable rank of every route inside its
 //                 expert (flat route id order, via warp match + per-warp
 //                 prefix), writing perm / inv / inv_pad
@@ -87,7 +88,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
 }
 
 __global__ void __launch_bounds__(1024) route_scan_kernel(
-    const int32_t* __restrict__ block_counts, int nb, int E, int64_t rows_alloc, int max_mtiles,
+    const int32_t* __restrict__ block_counts, int nb, int E, int pad_rows, int64_t rows_alloc,
+    int max_mtiles,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ pad_offsets,
     int32_t* __restrict__ base_u, int32_t* __restrict__ base_p, int32_t* __restrict__ mtile_expert,
     int32_t* __restrict__ total_mtiles, uint32_t* __restrict__ status) {
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
   int c = 0;
   if (e < E)
     for (int b = 0; b < nb; ++b) c += block_counts[(int64_t)b * E + e];
-  const int cp = (c + 127) & ~127;
+  const int cp = (c + pad_rows - 1) / pad_rows * pad_rows;  // GEMM segment of the expert
   const int off_u = block_exclusive_scan(c, warp_sums, &tot_u);
   const int off_p = block_exclusive_scan(cp, warp_sums, &tot_p);
   if (e < E) {
@@ -197,7 +199,9 @@ cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* to
   route_count_kernel<<<nb, kRouteTokens, sizeof(int32_t) * E, s>>>(
       topk_idx, topk_w, (int)T, L.K, E, check ? 1 : 0, ws.block_counts, ws.status);
   if (ev) record_event(ev[1], s);
-  route_scan_kernel<<<1, 1024, 0, s>>>(ws.block_counts, nb, E, L.rows_alloc, max_mtiles, ws.counts,
+  const int pad_rows = L.pad_rows > 0 ? L.pad_rows : 128;
+  route_scan_kernel<<<1, 1024, 0, s>>>(ws.block_counts, nb, E, pad_rows, L.rows_alloc, max_mtiles,
+                                       ws.counts,
                                        ws.offsets, ws.pad_offsets, ws.base_u, ws.base_p,
                                        ws.mtile_expert, ws.total_mtiles, ws.status);
   if (ev) record_event(ev[2], s);

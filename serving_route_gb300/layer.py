@@ -16,12 +16,16 @@ class MegaMoELayer:
     def __init__(self, hidden: int, inter: int, num_experts: int, top_k: int, *, max_rows: int,
                  expected_m: int | None = None, capacity_factor: float = 1.0,
                  fuse_fc1: bool = False, check_routes: bool = True, emit_fc1: bool = False,
-                 device="cuda"):
+                 gemm: str = "auto", device="cuda"):
+        """gemm: "auto" (tactic from expected_m), "single" (one CTA per SM) or
+        "pair" (CTA pairs, tcgen05 cta_group::2)."""
         self.H, self.I, self.E, self.K = hidden, inter, num_experts, top_k
         self.max_rows = max_rows
         self.flags = ((B.MOE_FLAG_FUSE_FC1_EPILOGUE if fuse_fc1 else 0)
                       | (B.MOE_FLAG_CHECK_ROUTES if check_routes else 0)
-                      | (B.MOE_FLAG_EMIT_FC1 if emit_fc1 else 0))
+                      | (B.MOE_FLAG_EMIT_FC1 if emit_fc1 else 0)
+                      | {"auto": 0, "single": B.MOE_FLAG_GEMM_SINGLE_CTA,
+                         "pair": B.MOE_FLAG_GEMM_CTA_PAIR}[gemm])
         em = expected_m if expected_m is not None else max_rows
         ws, wb = B.moe_workspace_query(hidden, inter, num_experts, top_k, self.flags, em, max_rows,
                                        capacity_factor)
@@ -101,6 +105,9 @@ class MegaMoELayer:
             h_sf=view(v.h_sf, (R // 128) * (I // 128) * 512, torch.uint8, (R // 128, I // 128, 512)),
             y=view(v.y, R * H * 2, torch.bfloat16, (R, H)),
             rows_alloc=R,
+            gemm_pair=bool(v.gemm_pair),
+            gemm_ctas=int(v.gemm_ctas),
+            pad_rows=int(v.pad_rows),
         )
         if v.gu:
             d["gu"] = view(v.gu, R * 2 * I * 2, torch.bfloat16, (R, 2 * I))

@@ -34,9 +34,10 @@ def lib():
     return S
 
 
-def make_layer(S, wl, weights, max_rows=None, fuse=False, emit=True, check=True, cf=1.0):
+def make_layer(S, wl, weights, max_rows=None, fuse=False, emit=True, check=True, cf=1.0,
+               gemm="auto"):
     layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=max_rows or wl.T, fuse_fc1=fuse,
-                           emit_fc1=emit, check_routes=check, capacity_factor=cf)
+                           emit_fc1=emit, check_routes=check, capacity_factor=cf, gemm=gemm)
     layer.bind_weights(*weights)
     return layer
 
@@ -48,8 +49,8 @@ def check_routing(dbg, ref, T, K):
     assert np.array_equal(dbg["perm"][:R].cpu().numpy(), ref["perm"])
     assert np.array_equal(dbg["inv"][:T * K].cpu().numpy(), ref["inv"])
     pad = dbg["pad_offsets"].cpu().numpy()
-    assert np.all(pad % 128 == 0)
-    assert np.array_equal(np.diff(pad), (ref["counts"] + 127) // 128 * 128)
+    # GEMM segments are padded to 128 rows (single CTA) or 256 rows (CTA pairs)
+    assert any(np.array_equal(np.diff(pad), (ref["counts"] + g - 1) // g * g) for g in (128, 256))
     rows = gh.padded_rows(ref["offsets"], pad, R)
     inv_pad = dbg["inv_pad"][:T * K].cpu().numpy()
     act = ref["inv"] >= 0
@@ -70,11 +71,11 @@ def check_quant(S, dbg, xq, xs, perm, rows, K):
     assert np.array_equal(np.ldexp(1.0, sf).astype(np.float32), xs[tok])
 
 
-def run_full(S, orc, wl, fuse, emit=True, weights_dev=None, weights_orc=None):
+def run_full(S, orc, wl, fuse, emit=True, weights_dev=None, weights_orc=None, gemm="auto"):
     x, idx, w = gh.host_inputs(wl)
     ref = orc.forward(x, idx, w, *weights_orc)
     assert ref["err"] == 0
-    layer = make_layer(S, wl, weights_dev, fuse=fuse, emit=emit)
+    layer = make_layer(S, wl, weights_dev, fuse=fuse, emit=emit, gemm=gemm)
     xt, it, wt = gh.to_device(x, idx, w)
     out = layer.forward(xt, it, wt)
     st, bits = layer.read_status()
@@ -147,14 +148,15 @@ def test_tiny_weights_match_oracle_quantiser(lib, tiny):
         assert np.array_equal(a.cpu().numpy(), b)
 
 
+@pytest.mark.parametrize("gemm", ["single", "pair"])
 @pytest.mark.parametrize("fuse", [False, True])
-def test_tiny_layer_parity(lib, orc, tiny, fuse):
+def test_tiny_layer_parity(lib, orc, tiny, fuse, gemm):
     wl, wd, wo = tiny
-    layer, dbg, out, ref, x, idx, w = run_full(lib, orc, wl, fuse, True, wd, wo)
+    layer, dbg, out, ref, x, idx, w = run_full(lib, orc, wl, fuse, True, wd, wo, gemm=gemm)
     rows = check_routing(dbg, ref, wl.T, wl.K)
     check_quant(lib, dbg, ref["xq"], ref["xs"], ref["perm"], rows, wl.K)
     stats = compare_outputs(dbg, out, ref, rows)
-    print("tiny", "fused" if fuse else "unfused", stats)
+    print("tiny", gemm, "fused" if fuse else "unfused", stats)
 
 
 def test_fused_epilogue_bit_equal_unfused(lib, orc, tiny):
@@ -193,12 +195,13 @@ def small_problem(orc, T, H, I, E, K, seed, mask=0.0, empty=()):
     return x, idx, w, w1, w2
 
 
-def layer_from_float(S, orc, T, H, I, E, K, w1, w2, fuse=True, emit=True, max_rows=None, cf=1.0):
+def layer_from_float(S, orc, T, H, I, E, K, w1, w2, fuse=True, emit=True, max_rows=None, cf=1.0,
+                     gemm="auto"):
     q1, s1 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w1).cuda())
     q2, s2 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w2).cuda())
     wo = orc.quant_weights(w1) + orc.quant_weights(w2)
     layer = S.MegaMoELayer(H, I, E, K, max_rows=max_rows or max(T, 1), fuse_fc1=fuse,
-                           emit_fc1=emit, capacity_factor=cf)
+                           emit_fc1=emit, capacity_factor=cf, gemm=gemm)
     layer.bind_weights(q1, s1, q2, s2)
     return layer, wo
 
@@ -211,9 +214,10 @@ def layer_from_float(S, orc, T, H, I, E, K, w1, w2, fuse=True, emit=True, max_ro
     (130, 256, 256, 64, 8, 0.1, tuple(range(40)), False),  # many empty experts, top-8
     (513, 1024, 512, 8, 6, 0.05, (), True),     # several m-tiles per expert
 ])
-def test_edge_shapes(lib, orc, T, H, I, E, K, mask, empty, fuse):
+@pytest.mark.parametrize("gemm", ["single", "pair"])
+def test_edge_shapes(lib, orc, T, H, I, E, K, mask, empty, fuse, gemm):
     x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=T + H, mask=mask, empty=empty)
-    layer, wo = layer_from_float(lib, orc, T, H, I, E, K, w1, w2, fuse=fuse)
+    layer, wo = layer_from_float(lib, orc, T, H, I, E, K, w1, w2, fuse=fuse, gemm=gemm)
     ref = orc.forward(x, idx, w, *wo)
     xt, it, wt = gh.to_device(x, idx, w)
     out = layer.forward(xt, it, wt)
@@ -300,9 +304,10 @@ def test_host_errors_and_zero_tokens(lib, orc):
 
 def test_capacity_overflow_is_reported(lib, orc):
     import serving_route_gb300.binding as B
-    T, H, I, E, K = 256, 256, 128, 2, 2
+    T, H, I, E, K = 1024, 256, 128, 2, 2
     x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=11)
-    layer, _ = layer_from_float(lib, orc, T, H, I, E, K, w1, w2, cf=0.25)
+    # capacity for 10% of the routes (plus segment padding): 2048 routed rows overflow it
+    layer, _ = layer_from_float(lib, orc, T, H, I, E, K, w1, w2, cf=0.1)
     xt, it, wt = gh.to_device(x, idx, w)
     layer.forward(xt, it, wt)
     st, bits = layer.read_status()
