@@ -95,6 +95,15 @@ static inline void record_event(cudaEvent_t ev, cudaStream_t s) {
     cudaEventRecord(ev, s);
 }
 
+// 32-byte global store (one full sector); dst must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* dst, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                             uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0),
+               "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
 __device__ __forceinline__ void record_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }

@@ -354,24 +354,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tile_par = acc_phase;  // alternates per tile
       acc_phase ^= 1u;
 
+      // Stores are 32 bytes per thread per instruction (whole sectors): every
+      // destination below is 32-byte aligned (row pitches and tile offsets are
+      // multiples of 64 bytes, buffers 1024-byte aligned).
       if constexpr (MODE == kModeY) {
         if (active) {
-          uint4* dst =
-              reinterpret_cast<uint4*>(g.out + row * g.ld_out + (int64_t)nt * 256 + half * 128);
+          uint16_t* dst = g.out + row * g.ld_out + (int64_t)nt * 256 + half * 128;
 #pragma unroll
-          for (int v = 0; v < 16; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int v = 0; v < 8; ++v)
+            st_global_v8(dst + 16 * v, pk[8 * v], pk[8 * v + 1], pk[8 * v + 2], pk[8 * v + 3],
+                         pk[8 * v + 4], pk[8 * v + 5], pk[8 * v + 6], pk[8 * v + 7]);
         }
       }
       if constexpr (MODE == kModeGU || MODE == kModeFusedGU) {
-        uint16_t* base = g.out + row * g.ld_out + (int64_t)nt * 128 + half * 64;
-        uint4* dg = reinterpret_cast<uint4*>(base);
-        uint4* du = reinterpret_cast<uint4*>(base + g.inter);
+        uint16_t* dg = g.out + row * g.ld_out + (int64_t)nt * 128 + half * 64;
+        uint16_t* du = dg + g.inter;
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          dg[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          du[v] = make_uint4(pk[32 + 4 * v], pk[32 + 4 * v + 1], pk[32 + 4 * v + 2],
-                             pk[32 + 4 * v + 3]);
+        for (int v = 0; v < 4; ++v) {
+          st_global_v8(dg + 16 * v, pk[8 * v], pk[8 * v + 1], pk[8 * v + 2], pk[8 * v + 3],
+                       pk[8 * v + 4], pk[8 * v + 5], pk[8 * v + 6], pk[8 * v + 7]);
+          st_global_v8(du + 16 * v, pk[32 + 8 * v], pk[32 + 8 * v + 1], pk[32 + 8 * v + 2],
+                       pk[32 + 8 * v + 3], pk[32 + 8 * v + 4], pk[32 + 8 * v + 5],
+                       pk[32 + 8 * v + 6], pk[32 + 8 * v + 7]);
         }
       }
       if constexpr (MODE == kModeFused || MODE == kModeFusedGU) {
@@ -394,17 +398,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         amax = fmaxf(amax, amax_sh[tile_par][half ^ 1][row_in_tile]);
         const int e = pow2_scale_exp(amax);
         const float inv = pow2_neg(e);
-        uint4* dq =
-            reinterpret_cast<uint4*>(g.hq + row * (int64_t)g.inter + (int64_t)nt * 128 + half * 64);
+        uint8_t* dq = g.hq + row * (int64_t)g.inter + (int64_t)nt * 128 + half * 64;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint32_t w[4];
+        for (int v = 0; v < 2; ++v) {
+          uint32_t w[8];
 #pragma unroll
-          for (int uu = 0; uu < 4; ++uu) {
-            const int j = 16 * v + 4 * uu;
+          for (int uu = 0; uu < 8; ++uu) {
+            const int j = 32 * v + 4 * uu;
             w[uu] = e4m3x4(h[j] * inv, h[j + 1] * inv, h[j + 2] * inv, h[j + 3] * inv);
           }
-          dq[v] = make_uint4(w[0], w[1], w[2], w[3]);
+          st_global_v8(dq + 32 * v, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
         }
         if (half == 0)
           *reinterpret_cast<uint32_t*>(g.h_sf + sf_atom_offset(row, nt, g.IB)) =
