@@ -26,6 +26,7 @@ struct moe_handle {
   CUtensorMap tm_a, tm_hq, tm_w1, tm_w2;   // weight maps: 256-row boxes (single CTA)
   CUtensorMap tm_w1p, tm_w2p;               // weight maps: 128-row boxes (CTA pairs)
   CUtensorMap tm_asf, tm_hsf;               // scale atoms as 2-D uint32 tensors (CTA pairs)
+  CUtensorMap tm_y;                         // FC2 output, 32x32 BF16 boxes (TMA stores)
   int pair_ctas;                            // grid of the CTA-pair GEMMs
   bool bound;
   uint16_t* out;
@@ -74,6 +75,20 @@ bool encode_u8_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// BF16 matrix [rows, cols] for TMA stores of 32-row x 32-column boxes,
+// 64-byte swizzle.
+bool encode_bf16_store_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -236,7 +251,8 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   if (!encode_u8_map(&h->tm_a, w.a, L.H, L.rows_alloc, 128) ||
       !encode_u8_map(&h->tm_hq, w.hq, L.I, L.rows_alloc, 128) ||
       !encode_atom_map(&h->tm_asf, w.a_sf, (uint64_t)(L.rows_alloc / 128) * (L.H / 128)) ||
-      !encode_atom_map(&h->tm_hsf, w.h_sf, (uint64_t)(L.rows_alloc / 128) * (L.I / 128))) {
+      !encode_atom_map(&h->tm_hsf, w.h_sf, (uint64_t)(L.rows_alloc / 128) * (L.I / 128)) ||
+      !encode_bf16_store_map(&h->tm_y, w.y, L.H, L.rows_alloc)) {
     delete h;
     return MOE_ERR_CUDA;
   }
@@ -341,8 +357,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   if (ev) record_event(ev[5], s);
   const bool pair = L.pair;
   const int ctas = pair ? h->pair_ctas : h->num_sms;
-  if (launch_gemm(m1, pair, &h->tm_a, pair ? &h->tm_w1p : &h->tm_w1, &h->tm_asf, g1, ctas, s) !=
-      cudaSuccess)
+  if (launch_gemm(m1, pair, &h->tm_a, pair ? &h->tm_w1p : &h->tm_w1, &h->tm_asf, &h->tm_y, g1,
+                  ctas, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[6], s);
   if (!fused && launch_swiglu_quant(ws, L, h->num_sms, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -362,8 +378,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.ld_out = L.H;
   g2.status = ws.status;
   if (ev) record_event(ev[7], s);
-  if (launch_gemm(kModeY, pair, &h->tm_hq, pair ? &h->tm_w2p : &h->tm_w2, &h->tm_hsf, g2, ctas,
-                  s) != cudaSuccess)
+  if (launch_gemm(kModeY, pair, &h->tm_hq, pair ? &h->tm_w2p : &h->tm_w2, &h->tm_hsf, &h->tm_y, g2,
+                  ctas, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[8], s);
   if (launch_combine(ws, L, d_topk_w, h->out, num_tokens, s) != cudaSuccess) return MOE_ERR_CUDA;

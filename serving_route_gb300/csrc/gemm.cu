@@ -59,14 +59,20 @@ struct StageCfg {
   static constexpr uint32_t kOffSfb = kOffSfa + 512;         // two 512 B atoms
   static constexpr uint32_t kStageBytes = (kOffSfb + 1024 + 1023) / 1024 * 1024;
   static constexpr uint32_t kTxBytes = 16384 + kBRows * 128 + 512;  // per CTA
-  static constexpr size_t kDynSmem = (size_t)kStages * kStageBytes + 1024;
+  // FC2 output staging for TMA stores (single CTA only): 2 KB per epilogue
+  // warp, one 32-row x 32-column BF16 box, 64-byte swizzle
+  static constexpr bool kTmaStoreY = !PAIR;
+  static constexpr uint32_t kOffYStage = (uint32_t)kStages * kStageBytes;
+  static constexpr uint32_t kYStageBytes = kTmaStoreY ? 2048u * kEpiWarps : 0u;
+  static constexpr size_t kDynSmem = (size_t)kStages * kStageBytes + kYStageBytes + 1024;
 };
 
 template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
-                            const __grid_constant__ CUtensorMap tmSfa, const GemmArgs g) {
+                            const __grid_constant__ CUtensorMap tmSfa,
+                            const __grid_constant__ CUtensorMap tmY, const GemmArgs g) {
   using C = StageCfg<PAIR>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t dsmem[];
@@ -357,7 +363,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Stores are 32 bytes per thread per instruction (whole sectors): every
       // destination below is 32-byte aligned (row pitches and tile offsets are
       // multiples of 64 bytes, buffers 1024-byte aligned).
-      if constexpr (MODE == kModeY) {
+      if constexpr (MODE == kModeY && C::kTmaStoreY) {
+        // TMA stores: the warp's 32 rows x 128 columns leave in four 32x32
+        // boxes through its 2 KB staging buffer; row r's 16-byte chunk j sits
+        // at r*64 + ((j ^ ((r >> 1) & 3)) * 16) (the 64-byte swizzle).
+        if (active) {
+          const uint32_t buf = sbase + C::kOffYStage + (uint32_t)(warp - 2) * 2048u;
+          uint8_t* bufp = smem + C::kOffYStage + (warp - 2) * 2048;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (lane == 0) bulk_wait_group_read0();  // previous box has left the buffer
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int pj = j ^ ((lane >> 1) & 3);
+              *reinterpret_cast<uint4*>(bufp + lane * 64 + pj * 16) =
+                  make_uint4(pk[c * 16 + 4 * j], pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2],
+                             pk[c * 16 + 4 * j + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmY, buf, nt * 256 + half * 128 + c * 32, mt * 128 + q * 32);
+              bulk_commit_group();
+            }
+          }
+        }
+      } else if constexpr (MODE == kModeY) {
         if (active) {
           uint16_t* dst = g.out + row * g.ld_out + (int64_t)nt * 256 + half * 128;
 #pragma unroll
@@ -416,6 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if constexpr (MODE == kModeY && StageCfg<PAIR>::kTmaStoreY) {
+    if (warp >= 2 && lane == 0) bulk_wait_group0();  // this warp's output boxes are written
+  }
   tc_fence_before();
   __syncthreads();
   if constexpr (PAIR) cluster_sync_all();  // neither CTA frees TMEM the pair still uses
@@ -475,26 +510,28 @@ int gemm_max_pairs() {
 
 template <int MODE>
 static cudaError_t launch_mode(bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                               const CUtensorMap* tmSfa, const GemmArgs& g, int ctas,
-                               cudaStream_t s) {
+                               const CUtensorMap* tmSfa, const CUtensorMap* tmY,
+                               const GemmArgs& g, int ctas, cudaStream_t s) {
   if (!pair) {
     fp8_grouped_gemm_kernel<MODE, false><<<ctas, kThreads, StageCfg<false>::kDynSmem, s>>>(
-        *tmA, *tmB, *tmA, g);
+        *tmA, *tmB, *tmA, *tmY, g);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   pair_config(&cfg, attr, ctas, s);
-  return cudaLaunchKernelEx(&cfg, fp8_grouped_gemm_kernel<MODE, true>, *tmA, *tmB, *tmSfa, g);
+  return cudaLaunchKernelEx(&cfg, fp8_grouped_gemm_kernel<MODE, true>, *tmA, *tmB, *tmSfa, *tmY,
+                            g);
 }
 
 cudaError_t launch_gemm(GemmMode mode, bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const CUtensorMap* tmSfa, const GemmArgs& g, int ctas, cudaStream_t s) {
+                        const CUtensorMap* tmSfa, const CUtensorMap* tmY, const GemmArgs& g,
+                        int ctas, cudaStream_t s) {
   switch (mode) {
-    case kModeY: return launch_mode<kModeY>(pair, tmA, tmB, tmSfa, g, ctas, s);
-    case kModeGU: return launch_mode<kModeGU>(pair, tmA, tmB, tmSfa, g, ctas, s);
-    case kModeFused: return launch_mode<kModeFused>(pair, tmA, tmB, tmSfa, g, ctas, s);
-    case kModeFusedGU: return launch_mode<kModeFusedGU>(pair, tmA, tmB, tmSfa, g, ctas, s);
+    case kModeY: return launch_mode<kModeY>(pair, tmA, tmB, tmSfa, tmY, g, ctas, s);
+    case kModeGU: return launch_mode<kModeGU>(pair, tmA, tmB, tmSfa, tmY, g, ctas, s);
+    case kModeFused: return launch_mode<kModeFused>(pair, tmA, tmB, tmSfa, tmY, g, ctas, s);
+    case kModeFusedGU: return launch_mode<kModeFusedGU>(pair, tmA, tmB, tmSfa, tmY, g, ctas, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -98,9 +98,11 @@ cudaError_t gemm_set_attributes();
 int gemm_max_pairs();
 // pair: CTA-pair kernel (tmB boxes of 128 rows, tmSfa = the A scale atoms as a
 // 2-D uint32 tensor); otherwise the single-CTA kernel (tmB boxes of 256 rows).
-// ctas: grid size (an even number for pairs).
+// tmY: the FC2 output [rows, H] BF16 with 32x32 boxes and 64-byte swizzle (TMA
+// stores of the single-CTA kModeY kernel).  ctas: grid size (even for pairs).
 cudaError_t launch_gemm(GemmMode mode, bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const CUtensorMap* tmSfa, const GemmArgs& g, int ctas, cudaStream_t s);
+                        const CUtensorMap* tmSfa, const CUtensorMap* tmY, const GemmArgs& g,
+                        int ctas, cudaStream_t s);
 
 // combine.cu
 cudaError_t launch_combine(const Workspace& ws, const Layout& L, const float* topk_w,
