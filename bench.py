@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--unfused", action="store_true", help="time the unfused reference path")
     p.add_argument("--gemm", default="auto", choices=["auto", "single", "pair"])
+    p.add_argument("--experts", type=int, default=0,
+                   help="profiling only: the workload with this many experts (smaller weights)")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
@@ -55,6 +57,31 @@ def peaks():
         d = json.load(open(path))
         return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
     return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def gemm_source_hash() -> str:
+    """sha256 over the sources the grouped-GEMM kernel is compiled from."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "serving_route_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes (read + write) per launch from the committed ncu record, or
+    None when there is none for this workload or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    if rec.get("source_sha256") != gemm_source_hash():
+        return None
+    for e in rec.get("entries", []):
+        if e["workload"] == workload and e["kernel"] == kernel:
+            return e["dram_bytes_per_launch"]
+    return None
 
 
 def algorithmic_bytes(wl, counts):
@@ -198,6 +225,10 @@ def main():
     from gen import inputs as g
 
     wl = configs.WORKLOADS[args.config]
+    if args.experts:
+        from gen.configs import Workload
+        wl = Workload(f"{wl.name}_E{args.experts}", wl.T, wl.H, wl.I, args.experts, wl.K,
+                      wl.routing, wl.seed)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream()
     sp = stream.cuda_stream
@@ -379,7 +410,9 @@ def main():
     else:
         roof = {"bound": "hbm", "achieved": fc1_bytes / (fc1_ms * 1e-3) / 1e9, "peak": hbm,
                 "unit": "GB/s"}
-    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "kernel": "fc1",
+    roof.update({"frac": roof["achieved"] / roof["peak"],
+                 "traffic": recorded_traffic(wl.name, "fc1"), "kernel": "fc1",
+                 "algorithmic_bytes": fc1_bytes,
                  "peak_source": f"{src}: FP8 = 2 x bf16 burst" if roof["bound"] == "tensor"
                  else f"{src}: hbm copy"})
     line = {
