@@ -72,6 +72,12 @@ typedef enum moe_status {
  * query and to moe_create).  expected_m never changes a buffer size. */
 #define MOE_FLAG_GEMM_SINGLE_CTA 0x8u
 #define MOE_FLAG_GEMM_CTA_PAIR 0x10u
+/* Test only: exercises the device watchdog.  Every kernel wait is bounded
+ * (1 s); with this flag the bound is 20 ms and the first GEMM CTA withholds one
+ * pipeline stage, so its wait expires: the forward records MOE_DEV_TIMEOUT,
+ * the kernel winds down (drains its copies, frees tensor memory) and the
+ * context stays usable.  Single-CTA GEMM tactic only. */
+#define MOE_FLAG_WATCHDOG_TEST 0x20u
 
 typedef struct moe_dims {
   int32_t hidden;      /* H: multiple of 128, 128..16384 */

@@ -37,6 +37,7 @@ MOE_FLAG_CHECK_ROUTES = 0x2
 MOE_FLAG_EMIT_FC1 = 0x4
 MOE_FLAG_GEMM_SINGLE_CTA = 0x8
 MOE_FLAG_GEMM_CTA_PAIR = 0x10
+MOE_FLAG_WATCHDOG_TEST = 0x20
 
 # every function the header declares (checked against include/megamoe.h by a test)
 API_NAMES = ("moe_workspace_query", "moe_create", "moe_quantize_weights", "moe_bind_weights",

@@ -353,6 +353,9 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g1.h_sf = ws.h_sf;
   g1.IB = L.I / 128;
   g1.status = ws.status;
+  const bool wd_test = (h->dims.flags & MOE_FLAG_WATCHDOG_TEST) != 0;
+  g1.wait_limit_ns = wd_test ? 20000000ull : 1000000000ull;
+  g1.watchdog_test = wd_test ? 1 : 0;
   const GemmMode m1 = fused ? (emit ? kModeFusedGU : kModeFused) : kModeGU;
   if (ev) record_event(ev[5], s);
   const bool pair = L.pair;
@@ -377,6 +380,7 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.out = ws.y;
   g2.ld_out = L.H;
   g2.status = ws.status;
+  g2.wait_limit_ns = g1.wait_limit_ns;
   if (ev) record_event(ev[7], s);
   if (launch_gemm(kModeY, pair, &h->tm_hq, pair ? &h->tm_w2p : &h->tm_w2, &h->tm_hsf, &h->tm_y, g2,
                   ctas, s) != cudaSuccess)

@@ -171,7 +171,8 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort, uint32_t* status) {
+                                                  volatile int* abort, uint32_t* status,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   auto try_once = [&]() {
     return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   };
@@ -180,7 +181,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   while (true) {
     if (try_once()) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       record_status(status, MOE_DEV_TIMEOUT);
       return false;

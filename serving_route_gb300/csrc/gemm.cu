@@ -182,9 +182,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int y_b = e * g.N + (u - (u / g.NT) * g.NT) * 256 + (int)rank * (int)C::kBRows;
       bool ok = true;
       for (int kb = 0; kb < g.KB; ++kb) {
-        if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort, g.status)) {
+        if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort, g.status, g.wait_limit_ns)) {
           ok = false;
           break;
+        }
+        if (g.watchdog_test && blockIdx.x == 0 && u == unit0 && kb == 2) {
+          // watchdog test: this stage is never filled, so the MMA wait on it
+          // expires; it is not counted as in flight for the drain below
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
         }
         uint8_t* st = smem + stage * C::kStageBytes;
         const uint32_t v0 = (uint32_t)sfb_sm[buf][0][kb] * 0x01010101u;
@@ -234,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t fb = smem_u32(&full_bar[s]);
         const uint32_t par = (last_parity >> s) & 1u;
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(fb, par) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        while (!mbar_try_wait(fb, par) && globaltimer_ns() - t0 < g.wait_limit_ns) {
         }
       }
     }
@@ -246,11 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       for (int u = unit0; u < total; u += ustride) {
-        if (!mbar_wait_bounded<PAIR>(smem_u32(&acce_bar), acc_phase ^ 1u, abort, g.status)) break;
+        if (!mbar_wait_bounded<PAIR>(smem_u32(&acce_bar), acc_phase ^ 1u, abort, g.status, g.wait_limit_ns)) break;
         tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < g.KB; ++kb) {
-          if (!mbar_wait_bounded<PAIR>(smem_u32(&full_bar[stage]), phase, abort, g.status)) {
+          if (!mbar_wait_bounded<PAIR>(smem_u32(&full_bar[stage]), phase, abort, g.status, g.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -299,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         tc_commit(smem_u32(&drain_bar));
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(smem_u32(&drain_bar), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      while (!mbar_try_wait(smem_u32(&drain_bar), 0) && globaltimer_ns() - t0 < g.wait_limit_ns) {
       }
     }
     __syncwarp();
@@ -324,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = unit0; u < total; u += ustride) {
       const int mt = own_mtile(u);
       const int nt = u - (u / g.NT) * g.NT;
-      if (!mbar_wait_bounded(smem_u32(&accf_bar), acc_phase, abort, g.status)) break;
+      if (!mbar_wait_bounded(smem_u32(&accf_bar), acc_phase, abort, g.status, g.wait_limit_ns)) break;
       tc_fence_after();
       const int64_t row = (int64_t)mt * 128 + row_in_tile;
       // FC2: the second column half of a tile past H holds no output
@@ -426,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         amax_sh[tile_par][half][row_in_tile] = amax;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&amax_bar[q]));
-        if (!mbar_wait_bounded(smem_u32(&amax_bar[q]), tile_par, abort, g.status)) break;
+        if (!mbar_wait_bounded(smem_u32(&amax_bar[q]), tile_par, abort, g.status, g.wait_limit_ns)) break;
         amax = fmaxf(amax, amax_sh[tile_par][half ^ 1][row_in_tile]);
         const int e = pow2_scale_exp(amax);
         const float inv = pow2_neg(e);

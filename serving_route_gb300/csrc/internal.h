@@ -93,6 +93,8 @@ struct GemmArgs {
   uint8_t* h_sf;               // fused: scale atoms [mblocks][I/128][512]
   int IB;                      // I / 128
   uint32_t* status;
+  uint64_t wait_limit_ns;      // bound of every mbarrier wait (1 s; 20 ms in the watchdog test)
+  int watchdog_test;           // 1: CTA 0 withholds one stage so its MMA wait expires
 };
 cudaError_t gemm_set_attributes();
 int gemm_max_pairs();

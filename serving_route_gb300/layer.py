@@ -16,7 +16,7 @@ class MegaMoELayer:
     def __init__(self, hidden: int, inter: int, num_experts: int, top_k: int, *, max_rows: int,
                  expected_m: int | None = None, capacity_factor: float = 1.0,
                  fuse_fc1: bool = False, check_routes: bool = True, emit_fc1: bool = False,
-                 gemm: str = "auto", device="cuda"):
+                 gemm: str = "auto", watchdog_test: bool = False, device="cuda"):
         """gemm: "auto" (tactic from expected_m), "single" (one CTA per SM) or
         "pair" (CTA pairs, tcgen05 cta_group::2)."""
         self.H, self.I, self.E, self.K = hidden, inter, num_experts, top_k
@@ -25,7 +25,8 @@ class MegaMoELayer:
                       | (B.MOE_FLAG_CHECK_ROUTES if check_routes else 0)
                       | (B.MOE_FLAG_EMIT_FC1 if emit_fc1 else 0)
                       | {"auto": 0, "single": B.MOE_FLAG_GEMM_SINGLE_CTA,
-                         "pair": B.MOE_FLAG_GEMM_CTA_PAIR}[gemm])
+                         "pair": B.MOE_FLAG_GEMM_CTA_PAIR}[gemm]
+                      | (B.MOE_FLAG_WATCHDOG_TEST if watchdog_test else 0))
         em = expected_m if expected_m is not None else max_rows
         ws, wb = B.moe_workspace_query(hidden, inter, num_experts, top_k, self.flags, em, max_rows,
                                        capacity_factor)

@@ -1,0 +1,44 @@
+"""Device watchdog (failure detection without a GPU fault).
+
+Every wait inside the GEMM kernels is bounded.  With MOE_FLAG_WATCHDOG_TEST
+the first GEMM CTA withholds one pipeline stage -- a barrier that nothing
+completes -- and the wait bound drops to 20 ms: the kernel must record
+MOE_DEV_TIMEOUT, wind down (drain its copies and MMAs, free tensor memory) and
+return, and the context must stay usable for the next forward.  No trap, no
+fault, no hang.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests import gpu_harness as gh
+from tests.test_gpu_parity import compare_outputs, small_problem
+
+pytestmark = pytest.mark.gpu
+
+
+def test_watchdog_expires_with_status_and_context_survives(orc):
+    import __graft_entry__ as ge
+    ge.build()
+    import serving_route_gb300 as S
+    import serving_route_gb300.binding as B
+
+    T, H, I, E, K = 300, 512, 256, 8, 2
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=31)
+    q1, s1 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w1).cuda())
+    q2, s2 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w2).cuda())
+    xt, it, wt = gh.to_device(x, idx, w)
+
+    bad = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm="single", watchdog_test=True)
+    bad.bind_weights(q1, s1, q2, s2)
+    bad.forward(xt, it, wt)
+    st, bits = bad.read_status()
+    assert st == B.MOE_ERR_DEVICE_TIMEOUT and bits & B.MOE_DEV_TIMEOUT, (st, bits)
+
+    # the context is intact: a normal forward right after is correct
+    good = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm="single")
+    good.bind_weights(q1, s1, q2, s2)
+    out = good.forward(xt, it, wt)
+    assert good.read_status() == (0, 0)
+    ref = orc.forward(x, idx, w, *orc.quant_weights(w1), *orc.quant_weights(w2))
+    compare_outputs(good.debug(), out, ref, np.zeros(0, np.int64), check_gu=False)
