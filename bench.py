@@ -59,6 +59,23 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def reduce_max(value: float, device) -> float:
+    """max over the ranks of the initialised process group (value unchanged
+    without one).  Replicas only: this is timing, not a data-path collective."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(world: int, units_per_step: float, steps: int, max_total_ms: float) -> float:
+    """whole-job throughput: the units all ranks processed over the slowest rank's time"""
+    return world * units_per_step * steps / (max_total_ms * 1e-3)
+
+
 def gemm_source_hash() -> str:
     """sha256 over the sources the grouped-GEMM kernel is compiled from."""
     import hashlib
@@ -336,9 +353,7 @@ def main():
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(total_ms, dev)
     st, bits = layer.read_status(stream)
     if st != 0:
         raise RuntimeError(f"timed forwards reported device status {bits:#x}")
@@ -378,10 +393,7 @@ def main():
             t_end.record(stream)
         stream.synchronize()
         e2e_ms += t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e2e_ms, dev)
     st, bits = layer.read_status(stream)
     if st != 0:
         raise RuntimeError(f"e2e forwards reported device status {bits:#x}")
@@ -390,8 +402,8 @@ def main():
     K = args.steps
     flops = wl.routed_flops
     ms_step = total_ms / K
-    value = world * flops * K / (total_ms * 1e-3) / 1e12
-    e2e_value = world * flops * K / (e2e_ms * 1e-3) / 1e12
+    value = aggregate_rate(world, flops, K, total_ms) / 1e12
+    e2e_value = aggregate_rate(world, flops, K, e2e_ms) / 1e12
     hbm, bf16, bf16_sus, src = peaks()
     fp8_peak = 2.0 * bf16  # FP8 dense = 2x BF16 dense (nominal 4.5 vs 2.25 PFLOP/s)
     b_alg, touched = algorithmic_bytes(wl, counts)
@@ -425,7 +437,7 @@ def main():
                    "launch": "cuda graph replay" if graph is not None else "direct launches",
                    "gemm": ("cta pairs" if dbg["gemm_pair"] else "single cta") + f" x{dbg['gemm_ctas']}",
                    "parallelism": f"replicas x{world}"},
-        "tokens_per_s": world * wl.T * K / (total_ms * 1e-3),
+        "tokens_per_s": aggregate_rate(world, wl.T, K, total_ms),
         "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
                            "b_alg_bytes": b_alg, "experts_touched": touched,
                            "fp8_peak_tflops": fp8_peak, "hbm_gbs": hbm, "source": src},
