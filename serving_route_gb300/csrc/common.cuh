@@ -77,10 +77,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // SwiGLU of one gate/up pair: silu(g) * u = g / (1 + exp(-g)) * u, in float,
-// each operation rounded to nearest.  The fused FC1 epilogue and the unfused
-// kernel both call this one function, so they agree bit for bit.
+// with the hardware exponential and approximate divide (a few ulp of float,
+// far below the BF16 rounding of the gate/up inputs).  For g < -88 the
+// exponential overflows and the quotient is 0, the limit of silu.  The fused
+// FC1 epilogue and the unfused kernel both call this one function, so they
+// agree bit for bit.
 __device__ __forceinline__ float swiglu(float g, float u) {
-  float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+  const float s = __fdividef(g, __fadd_rn(1.0f, __expf(-g)));
   return __fmul_rn(s, u);
 }
 
