@@ -190,13 +190,14 @@ typedef struct moe_debug_view {
   int32_t* inv;            /* [T*K] unpadded position of route r, or -1 */
   int32_t* inv_pad;        /* [T*K] padded GEMM row of route r, or -1 */
   uint8_t* a;              /* [rows_alloc, H] E4M3 gathered activations (padded rows) */
-  uint8_t* a_sf;           /* E8M0 scale atoms of a: [rows_alloc/128][H/128][512] */
+  uint8_t* a_sf;           /* E8M0 scale atoms of a: [rows_alloc/128][ceil(H/512)][512] */
   uint16_t* gu;            /* [rows_alloc, 2I] BF16 gate||up (unfused or EMIT_FC1), else NULL */
   uint8_t* hq;             /* [rows_alloc, I] E4M3 re-quantised SwiGLU output */
-  uint8_t* h_sf;           /* E8M0 scale atoms of hq: [rows_alloc/128][I/128][512] */
+  uint8_t* h_sf;           /* E8M0 scale atoms of hq: [rows_alloc/128][ceil(I/512)][512] */
   uint16_t* y;             /* [rows_alloc, H] BF16 FC2 output per padded row */
   int64_t rows_alloc;      /* padded-row capacity (multiple of 128) */
-  int32_t sf_atom_bytes;   /* 512: 128 rows x 4 bytes, byte (r%32)*16 + (r/32)*4 + j */
+  int32_t sf_atom_bytes;   /* 512: 128 rows x 4 K blocks; the scale of row r, K block
+                              4q + j is byte (r%32)*16 + (r/32)*4 + j of atom q */
   int32_t gemm_pair;       /* 1: GEMMs run on CTA pairs (cta_group::2), 0: one CTA per SM */
   int32_t gemm_ctas;       /* grid size of the GEMM launches */
   int32_t pad_rows;        /* rows each expert's GEMM segment is padded to */

@@ -26,6 +26,7 @@ struct moe_handle {
   CUtensorMap tm_a, tm_hq, tm_w1, tm_w2;   // weight maps: 256-row boxes (single CTA)
   CUtensorMap tm_w1p, tm_w2p;               // weight maps: 128-row boxes (CTA pairs)
   CUtensorMap tm_asf, tm_hsf;               // scale atoms as 2-D uint32 tensors (CTA pairs)
+  CUtensorMap tm_w1sf, tm_w2sf;             // weight scale atoms, same form (CTA pairs)
   CUtensorMap tm_y;                         // FC2 output, 32x32 BF16 boxes (TMA stores)
   int pair_ctas;                            // grid of the CTA-pair GEMMs
   bool bound;
@@ -164,10 +165,10 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
   L->o_inv = take(4 * (size_t)rk);
   L->o_inv_pad = take(4 * (size_t)rk);
   L->o_a = take(R * H);
-  L->o_a_sf = take(MB * (H / 128) * kSfAtomBytes);
+  L->o_a_sf = take(MB * sf_kgroups(H / 128) * kSfAtomBytes);
   L->o_gu = L->keep_gu ? take(R * 2 * I * 2) : 0;
   L->o_hq = take(R * I);
-  L->o_h_sf = take(MB * (I / 128) * kSfAtomBytes);
+  L->o_h_sf = take(MB * sf_kgroups(I / 128) * kSfAtomBytes);
   L->o_y = take(R * H * 2);
   L->ws_bytes = o + kAlign;  // slack to align the caller's base
   o = 0;
@@ -175,6 +176,8 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
   L->o_w2 = take(E * H * I);
   L->o_w1_sf = take(E * (2 * I / 128) * (H / 128));
   L->o_w2_sf = take(E * (H / 128) * (I / 128));
+  L->o_w1_sfatoms = take(E * (2 * I / 128) * sf_kgroups(H / 128) * kSfAtomBytes);
+  L->o_w2_sfatoms = take(E * (H / 128) * sf_kgroups(I / 128) * kSfAtomBytes);
   L->w_bytes = o + kAlign;
   return MOE_OK;
 }
@@ -248,10 +251,16 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   h->wst.w2 = wb + L.o_w2;
   h->wst.w1_sf = wb + L.o_w1_sf;
   h->wst.w2_sf = wb + L.o_w2_sf;
+  h->wst.w1_sfatoms = wb + L.o_w1_sfatoms;
+  h->wst.w2_sfatoms = wb + L.o_w2_sfatoms;
   if (!encode_u8_map(&h->tm_a, w.a, L.H, L.rows_alloc, 128) ||
       !encode_u8_map(&h->tm_hq, w.hq, L.I, L.rows_alloc, 128) ||
-      !encode_atom_map(&h->tm_asf, w.a_sf, (uint64_t)(L.rows_alloc / 128) * (L.H / 128)) ||
-      !encode_atom_map(&h->tm_hsf, w.h_sf, (uint64_t)(L.rows_alloc / 128) * (L.I / 128)) ||
+      !encode_atom_map(&h->tm_asf, w.a_sf, (uint64_t)(L.rows_alloc / 128) * sf_kgroups(L.H / 128)) ||
+      !encode_atom_map(&h->tm_hsf, w.h_sf, (uint64_t)(L.rows_alloc / 128) * sf_kgroups(L.I / 128)) ||
+      !encode_atom_map(&h->tm_w1sf, h->wst.w1_sfatoms,
+                       (uint64_t)L.E * (2 * L.I / 128) * sf_kgroups(L.H / 128)) ||
+      !encode_atom_map(&h->tm_w2sf, h->wst.w2_sfatoms,
+                       (uint64_t)L.E * (L.H / 128) * sf_kgroups(L.I / 128)) ||
       !encode_bf16_store_map(&h->tm_y, w.y, L.H, L.rows_alloc)) {
     delete h;
     return MOE_ERR_CUDA;
@@ -338,10 +347,11 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   GemmArgs g1;
   memset(&g1, 0, sizeof(g1));
   g1.sfa = ws.a_sf;
-  g1.sfb = h->wst.w1_sf;
+  g1.sfb = h->wst.w1_sfatoms;
   g1.mtile_expert = ws.mtile_expert;
   g1.total_mtiles = ws.total_mtiles;
   g1.KB = L.H / 128;
+  g1.KQ = (int)sf_kgroups(g1.KB);
   g1.NT = L.I / 128;  // 256-wide tiles over 2I
   g1.N = 2 * L.I;
   g1.NB = 2 * L.I / 128;
@@ -360,8 +370,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   if (ev) record_event(ev[5], s);
   const bool pair = L.pair;
   const int ctas = pair ? h->pair_ctas : h->num_sms;
-  if (launch_gemm(m1, pair, &h->tm_a, pair ? &h->tm_w1p : &h->tm_w1, &h->tm_asf, &h->tm_y, g1,
-                  ctas, s) != cudaSuccess)
+  if (launch_gemm(m1, pair, &h->tm_a, pair ? &h->tm_w1p : &h->tm_w1, &h->tm_asf, &h->tm_w1sf,
+                  &h->tm_y, g1, ctas, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[6], s);
   if (!fused && launch_swiglu_quant(ws, L, h->num_sms, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -369,10 +379,11 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   GemmArgs g2;
   memset(&g2, 0, sizeof(g2));
   g2.sfa = ws.h_sf;
-  g2.sfb = h->wst.w2_sf;
+  g2.sfb = h->wst.w2_sfatoms;
   g2.mtile_expert = ws.mtile_expert;
   g2.total_mtiles = ws.total_mtiles;
   g2.KB = L.I / 128;
+  g2.KQ = (int)sf_kgroups(g2.KB);
   g2.NT = (L.H + 255) / 256;
   g2.N = L.H;
   g2.NB = L.H / 128;
@@ -382,8 +393,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.status = ws.status;
   g2.wait_limit_ns = g1.wait_limit_ns;
   if (ev) record_event(ev[7], s);
-  if (launch_gemm(kModeY, pair, &h->tm_hq, pair ? &h->tm_w2p : &h->tm_w2, &h->tm_hsf, &h->tm_y, g2,
-                  ctas, s) != cudaSuccess)
+  if (launch_gemm(kModeY, pair, &h->tm_hq, pair ? &h->tm_w2p : &h->tm_w2, &h->tm_hsf, &h->tm_w2sf,
+                  &h->tm_y, g2, ctas, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[8], s);
   if (launch_combine(ws, L, d_topk_w, h->out, num_tokens, s) != cudaSuccess) return MOE_ERR_CUDA;

@@ -22,17 +22,23 @@
 namespace mm {
 
 // ----------------------------------------------------------------------------
-// Scale atoms: E8M0 scale bytes of 128 rows x 4 consecutive 32-wide K chunks
-// (one 128-wide K block), 512 bytes, in the order the block-scaled MMA reads
-// them from TMEM after a 32x128b.warpx4 copy: row r of the 128-row tile sits
-// at byte (r % 32) * 16 + (r / 32) * 4 + j, j = K chunk.  A 1x128 scale is the
-// same for the 4 chunks, so each row stores its byte four times.
+// Scale atoms: the E8M0 scale bytes of 128 rows x 4 consecutive 128-wide K
+// blocks, 512 bytes, in the order the block-scaled MMA reads them from TMEM
+// after a 32x128b.warpx4 copy: row r of the 128-row tile sits at byte
+// (r % 32) * 16 + (r / 32) * 4 + j, where j is the K block within the group of
+// four.  A 1x128 (or 128x128) scale covers all four 32-wide K chunks of its
+// block, so the four MMAs of K block 4q + j all select byte j through the
+// scale-factor ids of the instruction descriptor, and one copy into TMEM
+// serves four K blocks.
 // ----------------------------------------------------------------------------
 constexpr int kSfAtomBytes = 512;
 
+__host__ __device__ __forceinline__ int64_t sf_kgroups(int64_t kblocks) { return (kblocks + 3) >> 2; }
+
 __host__ __device__ __forceinline__ int64_t sf_atom_offset(int64_t row, int64_t kblock,
                                                           int64_t kblocks) {
-  return ((row >> 7) * kblocks + kblock) * kSfAtomBytes + (row & 31) * 16 + ((row & 127) >> 5) * 4;
+  return ((row >> 7) * sf_kgroups(kblocks) + (kblock >> 2)) * kSfAtomBytes + (row & 31) * 16 +
+         ((row & 127) >> 5) * 4 + (kblock & 3);
 }
 
 // Smallest e with amax <= 448 * 2^e, kept in [-127, 127]; amax == 0 gives 0.
@@ -190,6 +196,47 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
       return false;
     }
   }
+}
+
+// Non-blocking probes of a phase: the fast path of every wait below.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+// The bounded wait kept out of line: inlined into the MMA issue loop, the
+// polling loop slows that loop even when it is never entered.
+template <bool CLUSTER>
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort,
+                                            uint32_t* status, uint64_t limit_ns) {
+  return mbar_wait_bounded<CLUSTER>(bar, parity, abort, status, limit_ns);
+}
+
+// Bounded wait: one non-blocking probe, then the out-of-line polling loop.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status, uint64_t limit_ns = kWaitLimitNs) {
+  const bool done = CLUSTER ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
+  return done || mbar_wait_slow<CLUSTER>(bar, parity, abort, status, limit_ns);
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -383,10 +430,12 @@ __device__ __forceinline__ uint64_t sdesc_sf_atom(uint32_t saddr) {
 
 // Instruction descriptor of tcgen05.mma kind::mxf8f6f4 with block scales:
 // A and B E4M3 (format 0, bits 7-9 / 10-12), both K-major (bits 15, 16 = 0),
-// N >> 3 (bits 17-22), scale type E8M0 (bit 23), M >> 7 (bits 27-28), scale
-// factor byte selectors 0 (bits 4-5 for B, 29-30 for A).
-__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N) {
-  return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 7) << 27);
+// N >> 3 (bits 17-22), scale type E8M0 (bit 23), M >> 7 (bits 27-28), and the
+// scale-factor ids (the byte of each 32-bit TMEM scale word the MMA uses):
+// bits 4-5 for B, 29-30 for A.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, uint32_t sf_id = 0) {
+  return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 7) << 27) | (sf_id << 4) |
+         (sf_id << 29);
 }
 
 // D[tmem] (+)= (A * 2^sfa) x (B * 2^sfb)^T, FP32 accumulation, K = 32.

@@ -20,17 +20,18 @@
 //      48 KB stages (A 128x128 B, B 256x128 B, 128-byte swizzle).
 //    - CTA pair (tcgen05 cta_group::2): two CTAs on the two SMs of a cluster
 //      compute M256 x N256; each stages its own 128 A rows and half of the
-//      256 B rows (32 KB per K block instead of 48 KB), which is what bounds
-//      the MMA rate here (the tensor core is limited by its shared-memory
-//      operand bytes), and allows a 6-stage ring.  Both producers' TMA loads
-//      complete on the leader CTA's barrier; the leader issues the scale
+//      256 B rows (32 KB per K block instead of 48 KB), so a 6-stage ring
+//      fits and more bytes are in flight per SM for the same MMA rate.  Both
+//      producers' TMA loads complete on the leader CTA's barrier, which only
+//      the leader arms (with both CTAs' bytes); the leader issues the scale
 //      copies and MMAs for the pair and multicasts its commits to both CTAs;
 //      each CTA drains its own 128 accumulator rows.  Expert segments are
 //      padded to 256 rows so a pair tile never straddles two experts.
-//  * Warp roles (320 threads): warp 0 producer (TMA + the B scale atoms it
-//    writes itself), one thread of warp 1 issues the scale copies
-//    (tcgen05.cp) and MMAs, warps 2-9 the epilogue (two per TMEM lane
-//    quadrant).
+//  * Warp roles (320 threads): warp 0 producer (TMA only: operand tiles, the
+//    A scale atom, and the two B scale atoms taken from a 256-entry table of
+//    constant atoms indexed by the weight block's E8M0 byte), one thread of
+//    warp 1 issues the scale copies (tcgen05.cp) and MMAs, warps 2-9 the
+//    epilogue (two per TMEM lane quadrant).
 //  * Epilogues: FC2 -> BF16 y; FC1 unfused -> BF16 gate||up; FC1 fused ->
 //    BF16-rounded gate/up, SwiGLU, 1x128 re-quantisation to E4M3 + E8M0 atoms
 //    (bit-equal to the unfused path, which runs the same device functions).
@@ -44,9 +45,10 @@ namespace mm {
 constexpr int kEpiWarps = 8;                   // two per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 constexpr uint32_t kTmemCols = 512;
-// Scale factors live in TMEM after the accumulator (columns 0-255): one
-// 16-column slot per pipeline stage (A atom at +0, B atoms at +8 and +12), so
-// the copy for stage s+1 never overwrites scales the MMAs of stage s still read.
+// Scale factors live in TMEM after the accumulator (columns 0-255): four
+// 16-column slots used in turn by successive groups of four K blocks (A atom
+// at +0, B atoms at +8 and +12), so a copy never overwrites scales that MMAs
+// of the previous three groups may still read.
 constexpr uint32_t kColSf = 256, kSfSlotCols = 16;
 
 template <bool PAIR>
@@ -58,10 +60,11 @@ struct StageCfg {
   static constexpr uint32_t kOffSfa = kOffB + kBRows * 128;  // one 512 B atom
   static constexpr uint32_t kOffSfb = kOffSfa + 512;         // two 512 B atoms
   static constexpr uint32_t kStageBytes = (kOffSfb + 1024 + 1023) / 1024 * 1024;
-  static constexpr uint32_t kTxBytes = 16384 + kBRows * 128 + 512;  // per CTA
-  // FC2 output staging for TMA stores (single CTA only): 2 KB per epilogue
-  // warp, one 32-row x 32-column BF16 box, 64-byte swizzle
-  static constexpr bool kTmaStoreY = !PAIR;
+  static constexpr uint32_t kTxBytes = 16384 + kBRows * 128;  // operand bytes per CTA
+  static constexpr uint32_t kTxAtomBytes = 3 * 512;            // + scale atoms, every 4th K block
+  // FC2 output staging for TMA stores: 2 KB per epilogue warp, one 32-row x
+  // 32-column BF16 box, 64-byte swizzle
+  static constexpr bool kTmaStoreY = true;
   static constexpr uint32_t kOffYStage = (uint32_t)kStages * kStageBytes;
   static constexpr uint32_t kYStageBytes = kTmaStoreY ? 2048u * kEpiWarps : 0u;
   static constexpr size_t kDynSmem = (size_t)kStages * kStageBytes + kYStageBytes + 1024;
@@ -72,6 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmSfa,
+                            const __grid_constant__ CUtensorMap tmSfb,
                             const __grid_constant__ CUtensorMap tmY, const GemmArgs g) {
   using C = StageCfg<PAIR>;
   constexpr int kStages = C::kStages;
@@ -82,7 +86,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t amax_bar[4];  // per quadrant: both column halves posted
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  __shared__ uint8_t sfb_sm[2][2][128];
   __shared__ float amax_sh[2][2][128];  // [tile parity][column half][row] (fused epilogue)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) &
@@ -105,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), PAIR ? 2 : 1);
+      mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     mbar_init(smem_u32(&accf_bar), 1);
@@ -116,7 +119,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
-    if (PAIR) prefetch_tensormap(&tmSfa);
+    if (PAIR) {
+      prefetch_tensormap(&tmSfa);
+      prefetch_tensormap(&tmSfb);
+    }
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -136,57 +142,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Per unit the producer needs the expert id (a global table) and the
-    // tile's weight-scale bytes.  Both are fetched ahead: the expert id two
-    // units ahead, the scale bytes one unit ahead, so no dependent global load
-    // stalls the producer at a tile boundary.
+    // Per unit the producer needs the expert id (a global table); it is
+    // fetched one unit ahead so no dependent global load stalls the producer
+    // at a tile boundary.  Every fourth K block the stage also carries the
+    // scale atoms of the next four K blocks (A: this m-tile; B: the two
+    // 128-row halves of the n-tile).
     auto expert_of = [&](int u) -> int {
       return u < total ? g.mtile_expert[(PAIR ? 2 : 1) * (u / g.NT)] : 0;
-    };
-    uint32_t nb0[4], nb1[4];
-    auto fetch_sfb = [&](int u, int e) {
-      if (u < total) {
-        const int nt = u - (u / g.NT) * g.NT;
-        const uint8_t* p = g.sfb + ((int64_t)e * g.NB + 2 * nt) * g.KB;
-        const bool has1 = 2 * nt + 1 < g.NB;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int kb = lane + 32 * i;
-          nb0[i] = (kb < g.KB) ? p[kb] : 127u;
-          nb1[i] = (has1 && kb < g.KB) ? p[g.KB + kb] : 127u;
-        }
-      }
-    };
-    auto stash_sfb = [&](int buf) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        sfb_sm[buf][0][lane + 32 * i] = (uint8_t)nb0[i];
-        sfb_sm[buf][1][lane + 32 * i] = (uint8_t)nb1[i];
-      }
-      __syncwarp();
     };
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued at least once, parity of last issue
-    int buf = 0;
-    int e_cur = expert_of(unit0);
-    int e_next = expert_of(unit0 + ustride);
-    fetch_sfb(unit0, e_cur);
-    stash_sfb(0);
+    int e_next = expert_of(unit0);
     for (int u = unit0; u < total && !*abort; u += ustride) {
       const int mt = own_mtile(u);
-      const int e = e_cur;
-      const int e_after = expert_of(u + 2 * ustride);  // needed one unit from now
-      fetch_sfb(u + ustride, e_next);                  // consumed after this unit's k loop
+      const int e = e_next;
+      e_next = expert_of(u + ustride);
+      const int nt = u - (u / g.NT) * g.NT;
       // weight rows: expert e, 256-row n-tile; a pair CTA stages its half
-      const int y_b = e * g.N + (u - (u / g.NT) * g.NT) * 256 + (int)rank * (int)C::kBRows;
+      const int y_b = e * g.N + nt * 256 + (int)rank * (int)C::kBRows;
+      // B scale atoms of the n-tile's two 128-row blocks (the second clamped
+      // to the first past N: those output columns are never stored)
+      const int nb0 = 2 * nt, nb1 = (2 * nt + 1 < g.NB) ? 2 * nt + 1 : 2 * nt;
+      const int64_t sfb0 = ((int64_t)e * g.NB + nb0) * g.KQ, sfb1 = ((int64_t)e * g.NB + nb1) * g.KQ;
+      const int64_t sfa0 = (int64_t)mt * g.KQ;
       bool ok = true;
       for (int kb = 0; kb < g.KB; ++kb) {
-        if (!mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort, g.status, g.wait_limit_ns)) {
+        if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort, g.status, g.wait_limit_ns)) {
           ok = false;
           break;
         }
-        if (g.watchdog_test && blockIdx.x == 0 && u == unit0 && kb == 2) {
+        if (!PAIR && g.watchdog_test && blockIdx.x == 0 && u == unit0 && kb == 2) {
           // watchdog test: this stage is never filled, so the MMA wait on it
           // expires; it is not counted as in flight for the drain below
           if (++stage == kStages) {
@@ -195,29 +181,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           continue;
         }
-        uint8_t* st = smem + stage * C::kStageBytes;
-        const uint32_t v0 = (uint32_t)sfb_sm[buf][0][kb] * 0x01010101u;
-        const uint32_t v1 = (uint32_t)sfb_sm[buf][1][kb] * 0x01010101u;
-        *reinterpret_cast<uint4*>(st + C::kOffSfb + lane * 16) = make_uint4(v0, v0, v0, v0);
-        *reinterpret_cast<uint4*>(st + C::kOffSfb + 512 + lane * 16) = make_uint4(v1, v1, v1, v1);
-        fence_proxy_async_smem();
-        __syncwarp();
         if (lane == 0) {
           const uint32_t sst = sbase + stage * C::kStageBytes;
+          const bool atoms = (kb & 3) == 0;
+          const int q = kb >> 2;
           if constexpr (PAIR) {
-            // both CTAs' bytes complete on the leader's full barrier
+            // Both CTAs' bytes complete on the leader's full barrier; only the
+            // leader arrives (expecting both shares), so the peer's copies
+            // may land before or after that arrival within the phase.
             const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
-            mbar_arrive_expect_tx_cluster(fb, C::kTxBytes);
+            if (leader)
+              mbar_arrive_expect_tx(smem_u32(&full_bar[stage]),
+                                    2 * (C::kTxBytes + (atoms ? C::kTxAtomBytes : 0u)));
             tma_load_2d_pair(sst + C::kOffA, &tmA, fb, kb * 128, mt * 128);
             tma_load_2d_pair(sst + C::kOffB, &tmB, fb, kb * 128, y_b);
-            tma_load_2d_pair(sst + C::kOffSfa, &tmSfa, fb, 0, mt * g.KB + kb);
+            if (atoms) {
+              tma_load_2d_pair(sst + C::kOffSfa, &tmSfa, fb, 0, (int)(sfa0 + q));
+              tma_load_2d_pair(sst + C::kOffSfb, &tmSfb, fb, 0, (int)(sfb0 + q));
+              tma_load_2d_pair(sst + C::kOffSfb + 512, &tmSfb, fb, 0, (int)(sfb1 + q));
+            }
           } else {
             const uint32_t fb = smem_u32(&full_bar[stage]);
-            mbar_arrive_expect_tx(fb, C::kTxBytes);
+            mbar_arrive_expect_tx(fb, C::kTxBytes + (atoms ? C::kTxAtomBytes : 0u));
             tma_load_2d(sst + C::kOffA, &tmA, fb, kb * 128, mt * 128);
             tma_load_2d(sst + C::kOffB, &tmB, fb, kb * 128, y_b);
-            bulk_load(sst + C::kOffSfa, g.sfa + ((int64_t)mt * g.KB + kb) * kSfAtomBytes,
-                      kSfAtomBytes, fb);
+            if (atoms) {
+              bulk_load(sst + C::kOffSfa, g.sfa + (sfa0 + q) * kSfAtomBytes, kSfAtomBytes, fb);
+              bulk_load(sst + C::kOffSfb, g.sfb + (sfb0 + q) * kSfAtomBytes, kSfAtomBytes, fb);
+              bulk_load(sst + C::kOffSfb + 512, g.sfb + (sfb1 + q) * kSfAtomBytes, kSfAtomBytes, fb);
+            }
           }
         }
         __syncwarp();
@@ -229,14 +221,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      buf ^= 1;
-      stash_sfb(buf);
-      e_cur = e_next;
-      e_next = e_after;
     }
     // Drain: every copy this CTA issued must have landed before the CTA exits
     // (the leader's full barriers also count the peer's bytes; the peer is
     // held by the cluster barrier at the end until the leader has drained).
+    // After an abort the two producers may have stopped at different stages,
+    // so the peer also gives its last copies a fixed 100 us to land.
+    if (PAIR && !leader && lane == 0 && *abort) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 100000ull) {
+      }
+    }
     if (lane == 0 && leader) {
       for (int s = 0; s < kStages; ++s) {
         if (!(issued_mask & (1u << s))) continue;
@@ -251,32 +246,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_mxf8_e4m3(PAIR ? 256 : 128, 256);
+      const uint32_t idesc0 = idesc_mxf8_e4m3(PAIR ? 256 : 128, 256);
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
+      uint32_t group = 0;  // running count of scale-atom groups: TMEM slot = group % 4
+      // Readiness of the next stage is probed right after the current
+      // stage's MMAs are issued, so the probe's latency overlaps them; only a
+      // stage found not ready goes through the (out-of-line) bounded wait.
+      // The loop issues as few tcgen05 instructions as it can: the scale
+      // atoms go to TMEM once per four K blocks.
+      auto probe = [&](int s, uint32_t ph) {
+        return PAIR ? mbar_test_wait_cluster(smem_u32(&full_bar[s]), ph)
+                    : mbar_test_wait(smem_u32(&full_bar[s]), ph);
+      };
+      bool ready = probe(0, 0);
+      uint32_t sf = tmem + kColSf;
       for (int u = unit0; u < total; u += ustride) {
-        if (!mbar_wait_bounded<PAIR>(smem_u32(&acce_bar), acc_phase ^ 1u, abort, g.status, g.wait_limit_ns)) break;
+        if (!mbar_wait<PAIR>(smem_u32(&acce_bar), acc_phase ^ 1u, abort, g.status, g.wait_limit_ns)) break;
         tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < g.KB; ++kb) {
-          if (!mbar_wait_bounded<PAIR>(smem_u32(&full_bar[stage]), phase, abort, g.status, g.wait_limit_ns)) {
+          if (!ready &&
+              !mbar_wait_slow<PAIR>(smem_u32(&full_bar[stage]), phase, abort, g.status, g.wait_limit_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t st = sbase + stage * C::kStageBytes;
-          const uint32_t sf = tmem + kColSf + stage * kSfSlotCols;
+          const uint32_t j = (uint32_t)kb & 3u;
+          if (j == 0) {
+            sf = tmem + kColSf + (group & 3u) * kSfSlotCols;
+            ++group;
+            if constexpr (PAIR) {
+              tc_cp_sf_atom_pair(sf, sdesc_sf_atom(st + C::kOffSfa));
+              tc_cp_sf_atom_pair(sf + 8, sdesc_sf_atom(st + C::kOffSfb));
+              tc_cp_sf_atom_pair(sf + 12, sdesc_sf_atom(st + C::kOffSfb + 512));
+            } else {
+              tc_cp_sf_atom(sf, sdesc_sf_atom(st + C::kOffSfa));
+              tc_cp_sf_atom(sf + 8, sdesc_sf_atom(st + C::kOffSfb));
+              tc_cp_sf_atom(sf + 12, sdesc_sf_atom(st + C::kOffSfb + 512));
+            }
+          }
+          const uint32_t idesc = idesc0 | (j << 4) | (j << 29);  // scale byte j of each word
           const uint64_t ad = sdesc_k_sw128(st + C::kOffA);
           const uint64_t bd = sdesc_k_sw128(st + C::kOffB);
-          if constexpr (PAIR) {
-            tc_cp_sf_atom_pair(sf, sdesc_sf_atom(st + C::kOffSfa));
-            tc_cp_sf_atom_pair(sf + 8, sdesc_sf_atom(st + C::kOffSfb));
-            tc_cp_sf_atom_pair(sf + 12, sdesc_sf_atom(st + C::kOffSfb + 512));
-          } else {
-            tc_cp_sf_atom(sf, sdesc_sf_atom(st + C::kOffSfa));
-            tc_cp_sf_atom(sf + 8, sdesc_sf_atom(st + C::kOffSfb));
-            tc_cp_sf_atom(sf + 12, sdesc_sf_atom(st + C::kOffSfb + 512));
-          }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
@@ -286,14 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               tc_mma_mxf8(tmem, ad + 2 * k, bd + 2 * k, idesc, sf, sf + 8, acc);
           }
-          if constexpr (PAIR)
-            tc_commit_pair_multicast(smem_u32(&empty_bar[stage]), 0x3);
-          else
-            tc_commit(smem_u32(&empty_bar[stage]));
+          const int done_stage = stage;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
+          ready = probe(stage, phase);
+          if constexpr (PAIR)
+            tc_commit_pair_multicast(smem_u32(&empty_bar[done_stage]), 0x3);
+          else
+            tc_commit(smem_u32(&empty_bar[done_stage]));
         }
         if (!ok) break;
         if constexpr (PAIR)
@@ -333,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = unit0; u < total; u += ustride) {
       const int mt = own_mtile(u);
       const int nt = u - (u / g.NT) * g.NT;
-      if (!mbar_wait_bounded(smem_u32(&accf_bar), acc_phase, abort, g.status, g.wait_limit_ns)) break;
+      if (!mbar_wait(smem_u32(&accf_bar), acc_phase, abort, g.status, g.wait_limit_ns)) break;
       tc_fence_after();
       const int64_t row = (int64_t)mt * 128 + row_in_tile;
       // FC2: the second column half of a tile past H holds no output
@@ -435,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         amax_sh[tile_par][half][row_in_tile] = amax;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&amax_bar[q]));
-        if (!mbar_wait_bounded(smem_u32(&amax_bar[q]), tile_par, abort, g.status, g.wait_limit_ns)) break;
+        if (!mbar_wait(smem_u32(&amax_bar[q]), tile_par, abort, g.status, g.wait_limit_ns)) break;
         amax = fmaxf(amax, amax_sh[tile_par][half ^ 1][row_in_tile]);
         const int e = pow2_scale_exp(amax);
         const float inv = pow2_neg(e);
@@ -450,9 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           st_global_v8(dq + 32 * v, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
         }
-        if (half == 0)
-          *reinterpret_cast<uint32_t*>(g.h_sf + sf_atom_offset(row, nt, g.IB)) =
-              (uint32_t)(e + 127) * 0x01010101u;
+        if (half == 0) g.h_sf[sf_atom_offset(row, nt, g.IB)] = (uint8_t)(e + 127);
       }
     }
   }
@@ -519,28 +532,29 @@ int gemm_max_pairs() {
 
 template <int MODE>
 static cudaError_t launch_mode(bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                               const CUtensorMap* tmSfa, const CUtensorMap* tmY,
+                               const CUtensorMap* tmSfa, const CUtensorMap* tmSfb,
+                               const CUtensorMap* tmY,
                                const GemmArgs& g, int ctas, cudaStream_t s) {
   if (!pair) {
     fp8_grouped_gemm_kernel<MODE, false><<<ctas, kThreads, StageCfg<false>::kDynSmem, s>>>(
-        *tmA, *tmB, *tmA, *tmY, g);
+        *tmA, *tmB, *tmA, *tmA, *tmY, g);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   pair_config(&cfg, attr, ctas, s);
-  return cudaLaunchKernelEx(&cfg, fp8_grouped_gemm_kernel<MODE, true>, *tmA, *tmB, *tmSfa, *tmY,
-                            g);
+  return cudaLaunchKernelEx(&cfg, fp8_grouped_gemm_kernel<MODE, true>, *tmA, *tmB, *tmSfa, *tmSfb,
+                            *tmY, g);
 }
 
 cudaError_t launch_gemm(GemmMode mode, bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const CUtensorMap* tmSfa, const CUtensorMap* tmY, const GemmArgs& g,
-                        int ctas, cudaStream_t s) {
+                        const CUtensorMap* tmSfa, const CUtensorMap* tmSfb, const CUtensorMap* tmY,
+                        const GemmArgs& g, int ctas, cudaStream_t s) {
   switch (mode) {
-    case kModeY: return launch_mode<kModeY>(pair, tmA, tmB, tmSfa, tmY, g, ctas, s);
-    case kModeGU: return launch_mode<kModeGU>(pair, tmA, tmB, tmSfa, tmY, g, ctas, s);
-    case kModeFused: return launch_mode<kModeFused>(pair, tmA, tmB, tmSfa, tmY, g, ctas, s);
-    case kModeFusedGU: return launch_mode<kModeFusedGU>(pair, tmA, tmB, tmSfa, tmY, g, ctas, s);
+    case kModeY: return launch_mode<kModeY>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s);
+    case kModeGU: return launch_mode<kModeGU>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s);
+    case kModeFused: return launch_mode<kModeFused>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s);
+    case kModeFusedGU: return launch_mode<kModeFusedGU>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s);
   }
   return cudaErrorInvalidValue;
 }

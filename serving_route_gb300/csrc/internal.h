@@ -25,10 +25,10 @@ struct Workspace {
   int32_t* inv;            // [max_rows*K]
   int32_t* inv_pad;        // [max_rows*K]
   uint8_t* a;              // [rows_alloc, H]
-  uint8_t* a_sf;           // atoms [rows_alloc/128][H/128][512]
+  uint8_t* a_sf;           // atoms [rows_alloc/128][ceil(H/512)][512]
   uint16_t* gu;            // [rows_alloc, 2I] or nullptr
   uint8_t* hq;             // [rows_alloc, I]
-  uint8_t* h_sf;           // atoms [rows_alloc/128][I/128][512]
+  uint8_t* h_sf;           // atoms [rows_alloc/128][ceil(I/512)][512]
   uint16_t* y;             // [rows_alloc, H]
 };
 
@@ -37,6 +37,8 @@ struct WeightStore {
   uint8_t* w2;     // [E, H, I]
   uint8_t* w1_sf;  // [E, 2I/128, H/128] E8M0, in the interleaved row-block order of w1
   uint8_t* w2_sf;  // [E, H/128, I/128] E8M0
+  uint8_t* w1_sfatoms;  // [E][2I/128][ceil(H/512)][512]: w1_sf as GEMM scale atoms
+  uint8_t* w2_sfatoms;  // [E][H/128][ceil(I/512)][512]
 };
 
 struct Layout {
@@ -52,7 +54,7 @@ struct Layout {
   // byte offsets inside the workspace / weight store
   size_t o_status, o_counts, o_offsets, o_pad_offsets, o_mtile_expert, o_block_counts, o_base_u,
       o_base_p, o_perm, o_inv, o_inv_pad, o_a, o_a_sf, o_gu, o_hq, o_h_sf, o_y;
-  size_t o_w1, o_w2, o_w1_sf, o_w2_sf;
+  size_t o_w1, o_w2, o_w1_sf, o_w2_sf, o_w1_sfatoms, o_w2_sfatoms;
 };
 
 // layout.cpp-style pure host arithmetic (api.cu)
@@ -77,11 +79,12 @@ cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const
 // gemm.cu
 enum GemmMode { kModeY = 0, kModeGU = 1, kModeFused = 2, kModeFusedGU = 3 };
 struct GemmArgs {
-  const uint8_t* sfa;          // scale atoms of A: [mblocks][KB][512]
-  const uint8_t* sfb;          // E8M0 bytes of B: [E][NB][KB]
+  const uint8_t* sfa;          // scale atoms of A: [mblocks][KQ][512]
+  const uint8_t* sfb;          // scale atoms of B: [E][NB][KQ][512]
   const int32_t* mtile_expert;
   const int32_t* total_mtiles;
   int KB;                      // K / 128
+  int KQ;                      // groups of four K blocks (one scale atom each)
   int NT;                      // 256-wide N tiles per expert
   int N;                       // B rows per expert
   int NB;                      // N / 128
@@ -98,13 +101,15 @@ struct GemmArgs {
 };
 cudaError_t gemm_set_attributes();
 int gemm_max_pairs();
-// pair: CTA-pair kernel (tmB boxes of 128 rows, tmSfa = the A scale atoms as a
-// 2-D uint32 tensor); otherwise the single-CTA kernel (tmB boxes of 256 rows).
-// tmY: the FC2 output [rows, H] BF16 with 32x32 boxes and 64-byte swizzle (TMA
-// stores of the single-CTA kModeY kernel).  ctas: grid size (even for pairs).
+// pair: CTA-pair kernel (tmB boxes of 128 rows, tmSfa / tmSfb = the A / B
+// scale atoms as 2-D uint32 tensors of 512-byte rows); otherwise the
+// single-CTA kernel (tmB boxes of 256 rows; scale atoms by bulk copy from
+// g.sfa / g.sfb).  tmY: the FC2 output [rows, H] BF16 with
+// 32x32 boxes and 64-byte swizzle (TMA stores of kModeY).  ctas: grid size
+// (even for pairs).
 cudaError_t launch_gemm(GemmMode mode, bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const CUtensorMap* tmSfa, const CUtensorMap* tmY, const GemmArgs& g,
-                        int ctas, cudaStream_t s);
+                        const CUtensorMap* tmSfa, const CUtensorMap* tmSfb, const CUtensorMap* tmY,
+                        const GemmArgs& g, int ctas, cudaStream_t s);
 
 // combine.cu
 cudaError_t launch_combine(const Workspace& ws, const Layout& L, const float* topk_w,

@@ -62,13 +62,12 @@ __device__ __forceinline__ void quant_dispatch_unit(const uint4 raw, bool valid,
   amax = half_warp_max(amax);
   const int e = pow2_scale_exp(amax);
   const uint2 q = quant8(v, e);
-  const uint32_t sf4 = (uint32_t)(e + 127) * 0x01010101u;
   const int KB = H >> 7;
   for (int k = 0; k < K; ++k) {
     const int p = __shfl_sync(0xFFFFFFFFu, p_lane, k);
     if (p >= 0 && valid) {
       *reinterpret_cast<uint2*>(a + (int64_t)p * H + b * 128 + l16 * 8) = q;
-      if (l16 == 0) *reinterpret_cast<uint32_t*>(a_sf + sf_atom_offset(p, b, KB)) = sf4;
+      if (l16 == 0) a_sf[sf_atom_offset(p, b, KB)] = (uint8_t)(e + 127);
     }
   }
 }
@@ -134,9 +133,7 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
     const int e = pow2_scale_exp(amax);
     if (valid) {
       *reinterpret_cast<uint2*>(hq + row * I + b * 128 + l16 * 8) = quant8(h, e);
-      if (l16 == 0)
-        *reinterpret_cast<uint32_t*>(h_sf + sf_atom_offset(row, b, IB)) =
-            (uint32_t)(e + 127) * 0x01010101u;
+      if (l16 == 0) h_sf[sf_atom_offset(row, b, IB)] = (uint8_t)(e + 127);
     }
   }
 }
@@ -266,6 +263,30 @@ cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int 
   return cudaGetLastError();
 }
 
+// Weight-scale atoms for the GEMM B operand: for every expert, 128-row block
+// nb and group q of four K blocks, one 512-byte atom whose rows all hold the
+// four E8M0 bytes sf[e][nb][4q .. 4q+3] (127, i.e. 2^0, past the last K
+// block).  One thread per 32-bit word.
+__global__ void sfb_atoms_kernel(const uint8_t* __restrict__ sf, int64_t nblocks, int KB,
+                                 uint32_t* __restrict__ atoms) {
+  const int KQ = (KB + 3) >> 2;
+  const int64_t words = nblocks * KQ * 128;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t atom = i >> 7;
+    const int64_t blk = atom / KQ;
+    const int q = (int)(atom - blk * KQ);
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int kb = 4 * q + j;
+      const uint32_t v = kb < KB ? sf[blk * KB + kb] : 127u;
+      w |= v << (8 * j);
+    }
+    atoms[i] = w;
+  }
+}
+
 cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const uint8_t* w1,
                                   const float* w1s, const uint8_t* w2, const float* w2s,
                                   uint32_t* status, cudaStream_t s) {
@@ -279,6 +300,11 @@ cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const
                                                             status);
   const int64_t n2 = (int64_t)E * (H / 128) * (I / 128);
   scale_convert_kernel<<<stream_grid(n2, 256), 256, 0, s>>>(w2s, wst.w2_sf, n2, status);
+  const int64_t nb1 = (int64_t)E * (2 * I / 128), nb2 = (int64_t)E * (H / 128);
+  sfb_atoms_kernel<<<stream_grid(nb1 * ((H / 128 + 3) / 4) * 128, 256), 256, 0, s>>>(
+      wst.w1_sf, nb1, H / 128, reinterpret_cast<uint32_t*>(wst.w1_sfatoms));
+  sfb_atoms_kernel<<<stream_grid(nb2 * ((I / 128 + 3) / 4) * 128, 256), 256, 0, s>>>(
+      wst.w2_sf, nb2, I / 128, reinterpret_cast<uint32_t*>(wst.w2_sfatoms));
   return cudaGetLastError();
 }
 

@@ -101,9 +101,9 @@ class MegaMoELayer:
             inv=view(v.inv, 4 * self.max_rows * K, torch.int32, (self.max_rows * K,)),
             inv_pad=view(v.inv_pad, 4 * self.max_rows * K, torch.int32, (self.max_rows * K,)),
             a=view(v.a, R * H, torch.uint8, (R, H)),
-            a_sf=view(v.a_sf, (R // 128) * (H // 128) * 512, torch.uint8, (R // 128, H // 128, 512)),
+            a_sf=view(v.a_sf, (R // 128) * kq(H) * 512, torch.uint8, (R // 128, kq(H), 512)),
             hq=view(v.hq, R * I, torch.uint8, (R, I)),
-            h_sf=view(v.h_sf, (R // 128) * (I // 128) * 512, torch.uint8, (R // 128, I // 128, 512)),
+            h_sf=view(v.h_sf, (R // 128) * kq(I) * 512, torch.uint8, (R // 128, kq(I), 512)),
             y=view(v.y, R * H * 2, torch.bfloat16, (R, H)),
             rows_alloc=R,
             gemm_pair=bool(v.gemm_pair),
@@ -126,10 +126,16 @@ class MegaMoELayer:
             pass
 
 
-def sf_atom_rows(atoms: torch.Tensor, rows: int) -> torch.Tensor:
-    """Decode scale atoms [mblocks, kblocks, 512] into E8M0 bytes [rows, kblocks]
-    (row r of an m-block at byte (r%32)*16 + (r//32)*4; the 4 copies are equal)."""
-    mb, kbn, _ = atoms.shape
-    a = atoms.view(mb, kbn, 32, 4, 4)            # [mb, kb, r%32, r//32, copy]
-    a = a[..., 0].permute(0, 3, 2, 1)            # [mb, r//32, r%32, kb]
-    return a.reshape(mb * 128, kbn)[:rows]
+def kq(k: int) -> int:
+    """Scale atoms along a K extent: one per four 128-wide K blocks."""
+    return (k // 128 + 3) // 4
+
+
+def sf_atom_rows(atoms: torch.Tensor, rows: int, kblocks: int) -> torch.Tensor:
+    """Decode scale atoms [mblocks, kgroups, 512] into E8M0 bytes [rows, kblocks]:
+    row r of an m-block, K block 4q + j, sits at byte (r%32)*16 + (r//32)*4 + j
+    of atom q."""
+    mb, kg, _ = atoms.shape
+    a = atoms.view(mb, kg, 32, 4, 4)             # [mb, q, r%32, r//32, j]
+    a = a.permute(0, 3, 2, 1, 4)                 # [mb, r//32, r%32, q, j]
+    return a.reshape(mb * 128, kg * 4)[:rows, :kblocks]

@@ -67,7 +67,7 @@ def check_quant(S, dbg, xq, xs, perm, rows, K):
     tok = perm // K
     a = dbg["a"][torch.from_numpy(rows).cuda()].cpu().numpy()
     assert np.array_equal(a, xq[tok])
-    sf = S.sf_atom_rows(dbg["a_sf"], dbg["rows_alloc"]).cpu().numpy()[rows].astype(np.int64) - 127
+    sf = S.sf_atom_rows(dbg["a_sf"], dbg["rows_alloc"], xq.shape[1] // 128).cpu().numpy()[rows].astype(np.int64) - 127
     assert np.array_equal(np.ldexp(1.0, sf).astype(np.float32), xs[tok])
 
 
@@ -171,7 +171,7 @@ def test_fused_epilogue_bit_equal_unfused(lib, orc, tiny):
         d = layer.debug()
         off = d["offsets"].cpu().numpy()
         rows = torch.from_numpy(gh.padded_rows(off, d["pad_offsets"].cpu().numpy(), int(off[-1]))).cuda()
-        sf = lib.sf_atom_rows(d["h_sf"], d["rows_alloc"])[rows]
+        sf = lib.sf_atom_rows(d["h_sf"], d["rows_alloc"], wl.I // 128)[rows]
         res.append((out.view(torch.int16), d["hq"][rows], sf, d["gu"][rows].view(torch.int16),
                     d["y"][rows].view(torch.int16)))
     for a, b in zip(*res):
