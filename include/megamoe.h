@@ -65,11 +65,15 @@ typedef enum moe_status {
 #define MOE_FLAG_FUSE_FC1_EPILOGUE 0x1u /* SwiGLU + 1x128 quant inside the FC1 epilogue (opt-in) */
 #define MOE_FLAG_CHECK_ROUTES 0x2u      /* duplicate / finite-weight checks (range check always on) */
 #define MOE_FLAG_EMIT_FC1 0x4u          /* also keep the BF16 gate||up FC1 output (debug) */
-/* GEMM tactic.  Default: one CTA per SM (expert segments padded to 128 rows).
- * MOE_FLAG_GEMM_CTA_PAIR runs the GEMMs on CTA pairs (tcgen05 cta_group::2,
- * M = 256, segments padded to 256 rows); it is correct but measured slower on
- * GB300, and its padding needs a larger workspace (pass the same flags to the
- * query and to moe_create).  expected_m never changes a buffer size. */
+/* GEMM tactic.  MOE_FLAG_GEMM_SINGLE_CTA: one CTA per SM, expert segments
+ * padded to 128 rows.  MOE_FLAG_GEMM_CTA_PAIR: CTA pairs (tcgen05
+ * cta_group::2, M = 256 over two SMs), segments padded to 256 rows.  Neither:
+ * chosen from expected_m -- with m = expected_m * top_k / num_experts routed
+ * rows per expert, pairs when ceil(m/256)*256 < 1.13 * ceil(m/128)*128 (a
+ * pair feeds its tensor cores ~13% better per row but pads more).  Buffers are
+ * sized for the padding of every tactic the flags allow (256 rows unless
+ * SINGLE_CTA is set), so expected_m never changes a buffer size; pass the same
+ * flags to the query and to moe_create. */
 #define MOE_FLAG_GEMM_SINGLE_CTA 0x8u
 #define MOE_FLAG_GEMM_CTA_PAIR 0x10u
 /* Test only: exercises the device watchdog.  Every kernel wait is bounded

@@ -319,6 +319,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_clust
                : "memory");
 }
 
+// Arrive on a barrier of either CTA of the pair with no memory ordering: for
+// signals that carry no data through memory (an accumulator whose TMEM reads
+// have already completed), where a cluster-scope release would wait for the
+// thread's outstanding global stores.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                : "memory");

@@ -373,11 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[c * 16 + j] =
                 pack_bf16x2(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1]));
       }
+      // The TMEM reads above have completed (tcgen05.wait::ld); the arrive
+      // passes no data through memory, so in the pair it is relaxed: a
+      // cluster-scope release would first wait for this thread's
+      // outstanding global stores of the previous tile.
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         if constexpr (PAIR)
-          mbar_arrive_cluster(acce_addr);
+          mbar_arrive_cluster_relaxed(acce_addr);
         else
           mbar_arrive(acce_addr);
       }
