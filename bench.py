@@ -5,6 +5,9 @@ FC1 with the fused SwiGLU/re-quantisation epilogue, FC2, combine -- over one
 batch of the workload, replayed from a CUDA graph.  L2 is flushed (a 256 MiB
 write, outside the timed span) before every timed step; each step is timed
 with CUDA events on the launching stream and the K step times are summed.
+The timed capture has no events between its kernels; per-kernel times come
+from a second capture with an event before every kernel, replayed for the
+same number of steps right after.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
@@ -292,53 +295,67 @@ def main():
 
     dbg = layer.debug()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
-    layer.set_profile_events(ev)
 
     def fwd():
         layer.forward(x, idx, wts, stream=stream)
 
     use_graph = not args.no_graph
-    graph = None
     with torch.cuda.stream(stream):
         fwd()
     stream.synchronize()
     st, bits = layer.read_status(stream)
     if st != 0:
         raise RuntimeError(f"forward reported device status {bits:#x}")
-    if use_graph:
+
+    def capture():
+        if not use_graph:
+            return None
         try:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
                 fwd()
             stream.synchronize()
+            return gr
         except Exception as e:  # fall back to direct launches
             print(f"# graph capture failed ({e}); timing direct launches", file=sys.stderr)
-            graph = None
+            return None
 
-    def step():
-        if graph is not None:
-            with torch.cuda.stream(stream):
-                graph.replay()
-        else:
-            with torch.cuda.stream(stream):
+    # Two captures of the same forward: the timed one has no events between
+    # its kernels (each kernel after the first launches as a programmatic
+    # dependent of the previous one); the profiled one records an event
+    # before every kernel, which gives the per-kernel times.
+    graph = capture()
+    layer.set_profile_events(ev)
+    graph_prof = capture()
+    layer.set_profile_events([])
+
+    def step(gr, profiled):
+        if profiled:
+            layer.set_profile_events(ev)
+        with torch.cuda.stream(stream):
+            if gr is not None:
+                gr.replay()
+            else:
                 fwd()
+        if profiled:
+            layer.set_profile_events([])
 
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
 
-    def timed_steps(n, record):
+    def timed_steps(n, profiled):
         tot = 0.0
         per_kernel = {k: 0.0 for k in KERNELS}
         for _ in range(n):
             with torch.cuda.stream(stream):
                 flush.zero_()
                 t_start.record(stream)
-            step()
+            step(graph_prof if profiled else graph, profiled)
             with torch.cuda.stream(stream):
                 t_end.record(stream)
             stream.synchronize()
             tot += t_start.elapsed_time(t_end)
-            if record:
+            if profiled:
                 for i, k in enumerate(KERNELS):
                     per_kernel[k] += ev[i].elapsed_time(ev[i + 1])
         return tot, per_kernel
@@ -348,12 +365,15 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
-    total_ms, per_kernel = timed_steps(args.steps, True)
+    total_ms, _ = timed_steps(args.steps, False)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
     total_ms = reduce_max(total_ms, dev)
+    # per-kernel times: the same number of steps of the profiled capture
+    timed_steps(min(args.warmup, 3), True)
+    prof_ms, per_kernel = timed_steps(args.steps, True)
     st, bits = layer.read_status(stream)
     if st != 0:
         raise RuntimeError(f"timed forwards reported device status {bits:#x}")
@@ -443,6 +463,9 @@ def main():
                            "fp8_peak_tflops": fp8_peak, "hbm_gbs": hbm, "source": src},
         "roofline": roof,
         "kernel_ms": kern_ms,
+        "kernel_ms_source": ("CUDA events before every kernel, a second capture of the same forward "
+                             f"replayed for the same {K} steps right after the timed ones "
+                             f"({prof_ms / K:.4f} ms per step with the events in place)"),
         "gpu_launches": K * (7 if fused else 8),
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

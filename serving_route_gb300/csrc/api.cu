@@ -353,7 +353,10 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
       cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[4], s);
-  if (launch_quant_dispatch(ws, L, d_x, num_tokens, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // Kernels after the first are programmatic dependents of their predecessor
+  // unless profiling events sit between them.
+  const bool pdl = ev == nullptr;
+  if (launch_quant_dispatch(ws, L, d_x, num_tokens, s, pdl) != cudaSuccess) return MOE_ERR_CUDA;
 
   GemmArgs g1;
   memset(&g1, 0, sizeof(g1));
@@ -382,10 +385,10 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   const bool pair = L.pair;
   const int ctas = pair ? h->pair_ctas : h->num_sms;
   if (launch_gemm(m1, pair, &h->tm_a, pair ? &h->tm_w1p : &h->tm_w1, &h->tm_asf, &h->tm_w1sf,
-                  &h->tm_y, g1, ctas, s) != cudaSuccess)
+                  &h->tm_y, g1, ctas, s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[6], s);
-  if (!fused && launch_swiglu_quant(ws, L, h->num_sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!fused && launch_swiglu_quant(ws, L, h->num_sms, s, pdl) != cudaSuccess) return MOE_ERR_CUDA;
 
   GemmArgs g2;
   memset(&g2, 0, sizeof(g2));
@@ -405,10 +408,10 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.wait_limit_ns = g1.wait_limit_ns;
   if (ev) record_event(ev[7], s);
   if (launch_gemm(kModeY, pair, &h->tm_hq, pair ? &h->tm_w2p : &h->tm_w2, &h->tm_hsf, &h->tm_w2sf,
-                  &h->tm_y, g2, ctas, s) != cudaSuccess)
+                  &h->tm_y, g2, ctas, s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[8], s);
-  if (launch_combine(ws, L, d_topk_w, h->out, num_tokens, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_combine(ws, L, d_topk_w, h->out, num_tokens, s, pdl) != cudaSuccess) return MOE_ERR_CUDA;
   if (ev) record_event(ev[9], s);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

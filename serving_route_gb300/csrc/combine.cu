@@ -23,6 +23,7 @@ template <int K>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_pad,
     const float* __restrict__ w, int64_t T, int H, int col_ctas, uint16_t* __restrict__ out) {
+  pdl_wait();
   const int64_t units = T * col_ctas;
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int64_t t = u / col_ctas;
@@ -60,23 +61,31 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     o.w = pack_bf16x2(acc[6], acc[7]);
     *reinterpret_cast<uint4*>(out + t * H + c) = o;
   }
+  pdl_trigger();
+}
+
+template <int K>
+static cudaError_t launch_k_combine(const Workspace& ws, const Layout& L, const float* topk_w,
+                                   uint16_t* out, int64_t T, int col_ctas, unsigned grid,
+                                   cudaStream_t s, bool pdl) {
+  return launch_k(combine_kernel<K>, dim3(grid), dim3(kCombineThreads), 0, s, pdl, nullptr,
+                  (const uint16_t*)ws.y, (const int32_t*)ws.inv_pad, topk_w, T, L.H, col_ctas, out);
 }
 
 cudaError_t launch_combine(const Workspace& ws, const Layout& L, const float* topk_w,
-                           uint16_t* out, int64_t T, cudaStream_t s) {
+                           uint16_t* out, int64_t T, cudaStream_t s, bool pdl) {
   const int col_ctas = (L.H + kColsPerCta - 1) / kColsPerCta;
   int64_t units = T * col_ctas;
   const int64_t cap = 152 * 16;
   const unsigned grid = (unsigned)(units < cap ? (units < 1 ? 1 : units) : cap);
   switch (L.K) {
-    case 1: combine_kernel<1><<<grid, kCombineThreads, 0, s>>>(ws.y, ws.inv_pad, topk_w, T, L.H, col_ctas, out); break;
-    case 2: combine_kernel<2><<<grid, kCombineThreads, 0, s>>>(ws.y, ws.inv_pad, topk_w, T, L.H, col_ctas, out); break;
-    case 4: combine_kernel<4><<<grid, kCombineThreads, 0, s>>>(ws.y, ws.inv_pad, topk_w, T, L.H, col_ctas, out); break;
-    case 6: combine_kernel<6><<<grid, kCombineThreads, 0, s>>>(ws.y, ws.inv_pad, topk_w, T, L.H, col_ctas, out); break;
-    case 8: combine_kernel<8><<<grid, kCombineThreads, 0, s>>>(ws.y, ws.inv_pad, topk_w, T, L.H, col_ctas, out); break;
+    case 1: return launch_k_combine<1>(ws, L, topk_w, out, T, col_ctas, grid, s, pdl);
+    case 2: return launch_k_combine<2>(ws, L, topk_w, out, T, col_ctas, grid, s, pdl);
+    case 4: return launch_k_combine<4>(ws, L, topk_w, out, T, col_ctas, grid, s, pdl);
+    case 6: return launch_k_combine<6>(ws, L, topk_w, out, T, col_ctas, grid, s, pdl);
+    case 8: return launch_k_combine<8>(ws, L, topk_w, out, T, col_ctas, grid, s, pdl);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace mm

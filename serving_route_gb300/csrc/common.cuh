@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -116,6 +117,47 @@ __device__ __forceinline__ void st_global_v8(void* dst, uint32_t a0, uint32_t a1
 __device__ __forceinline__ void record_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
+
+// ----------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of a forward after the first is
+// launched with programmatic stream serialisation: it may start while its
+// predecessor finishes, and executes pdl_wait() before it touches global
+// memory that any earlier kernel of the forward writes or reads (the wait
+// returns once the predecessor grid has completed and its writes are
+// visible; completion is transitive along the chain).  pdl_trigger() lets the
+// successor launch once every CTA of this grid has issued it or exited.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+#ifndef __CUDACC_RTC__
+// Launch `kernel` on `s`; when `pdl`, with programmatic stream serialisation
+// (plus up to one extra attribute, e.g. a cluster shape).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, bool pdl, const cudaLaunchAttribute* extra,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (extra) attr[n++] = *extra;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+#endif
 
 // ----------------------------------------------------------------------------
 // Shared memory, mbarriers, TMA.

@@ -94,10 +94,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
-  int mtiles = *g.total_mtiles;
-  if (mtiles > g.max_mtiles) mtiles = g.max_mtiles;
-  // work units: single CTA -> (m-tile, n-tile); pair -> (m-tile pair, n-tile)
-  const int total = (PAIR ? mtiles / 2 : mtiles) * g.NT;
   const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int ustride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   // this CTA's 128-row m-tile of work unit u
@@ -139,6 +135,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   volatile int* abort = &abort_sh;
+  // Everything above only touched this CTA's shared and tensor memory; the
+  // routing tables and operands come from the previous kernels.
+  pdl_wait();
+  int mtiles = *g.total_mtiles;
+  if (mtiles > g.max_mtiles) mtiles = g.max_mtiles;
+  // work units: single CTA -> (m-tile, n-tile); pair -> (m-tile pair, n-tile)
+  const int total = (PAIR ? mtiles / 2 : mtiles) * g.NT;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -479,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  pdl_trigger();
   if constexpr (PAIR) cluster_sync_all();  // neither CTA frees TMEM the pair still uses
   if (warp == 1) {
     tc_fence_after();
@@ -508,25 +512,24 @@ cudaError_t gemm_set_attributes() {
   return set_attr<kModeFusedGU, true>();
 }
 
-static void pair_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int ctas,
-                        cudaStream_t s) {
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg->gridDim = dim3(ctas);
-  cfg->blockDim = dim3(kThreads);
-  cfg->dynamicSmemBytes = StageCfg<true>::kDynSmem;
-  cfg->stream = s;
-  cfg->attrs = attr;
-  cfg->numAttrs = 1;
+static cudaLaunchAttribute pair_cluster_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeClusterDimension;
+  a.val.clusterDim.x = 2;
+  a.val.clusterDim.y = 1;
+  a.val.clusterDim.z = 1;
+  return a;
 }
 
 // Largest number of CTA pairs that can be resident at once (0 if none).
 int gemm_max_pairs() {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  pair_config(&cfg, attr, 2, nullptr);
+  cudaLaunchAttribute attr = pair_cluster_attr();
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = StageCfg<true>::kDynSmem;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, fp8_grouped_gemm_kernel<kModeY, true>, &cfg) !=
       cudaSuccess)
@@ -537,28 +540,25 @@ int gemm_max_pairs() {
 template <int MODE>
 static cudaError_t launch_mode(bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
                                const CUtensorMap* tmSfa, const CUtensorMap* tmSfb,
-                               const CUtensorMap* tmY,
-                               const GemmArgs& g, int ctas, cudaStream_t s) {
-  if (!pair) {
-    fp8_grouped_gemm_kernel<MODE, false><<<ctas, kThreads, StageCfg<false>::kDynSmem, s>>>(
-        *tmA, *tmB, *tmA, *tmA, *tmY, g);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  pair_config(&cfg, attr, ctas, s);
-  return cudaLaunchKernelEx(&cfg, fp8_grouped_gemm_kernel<MODE, true>, *tmA, *tmB, *tmSfa, *tmSfb,
-                            *tmY, g);
+                               const CUtensorMap* tmY, const GemmArgs& g, int ctas,
+                               cudaStream_t s, bool pdl) {
+  if (!pair)
+    return launch_k(fp8_grouped_gemm_kernel<MODE, false>, dim3(ctas), dim3(kThreads),
+                    StageCfg<false>::kDynSmem, s, pdl, nullptr, *tmA, *tmB, *tmA, *tmA, *tmY, g);
+  const cudaLaunchAttribute cluster = pair_cluster_attr();
+  return launch_k(fp8_grouped_gemm_kernel<MODE, true>, dim3(ctas), dim3(kThreads),
+                  StageCfg<true>::kDynSmem, s, pdl, &cluster, *tmA, *tmB, *tmSfa, *tmSfb, *tmY, g);
 }
 
 cudaError_t launch_gemm(GemmMode mode, bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         const CUtensorMap* tmSfa, const CUtensorMap* tmSfb, const CUtensorMap* tmY,
-                        const GemmArgs& g, int ctas, cudaStream_t s) {
+                        const GemmArgs& g, int ctas, cudaStream_t s, bool pdl) {
   switch (mode) {
-    case kModeY: return launch_mode<kModeY>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s);
-    case kModeGU: return launch_mode<kModeGU>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s);
-    case kModeFused: return launch_mode<kModeFused>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s);
-    case kModeFusedGU: return launch_mode<kModeFusedGU>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s);
+    case kModeY: return launch_mode<kModeY>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s, pdl);
+    case kModeGU: return launch_mode<kModeGU>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s, pdl);
+    case kModeFused: return launch_mode<kModeFused>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s, pdl);
+    case kModeFusedGU:
+      return launch_mode<kModeFusedGU>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s, pdl);
   }
   return cudaErrorInvalidValue;
 }

@@ -67,9 +67,11 @@ cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* to
                          cudaEvent_t const* ev);
 
 // quant.cu
+// pdl: launch as a programmatic dependent of the previous kernel on `s`
 cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
-                                  int64_t T, cudaStream_t s);
-cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int num_sms, cudaStream_t s);
+                                  int64_t T, cudaStream_t s, bool pdl);
+cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int num_sms, cudaStream_t s,
+                                bool pdl);
 cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
                                     float* scale, cudaStream_t s);
 cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const uint8_t* w1,
@@ -109,10 +111,10 @@ int gemm_max_pairs();
 // (even for pairs).
 cudaError_t launch_gemm(GemmMode mode, bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         const CUtensorMap* tmSfa, const CUtensorMap* tmSfb, const CUtensorMap* tmY,
-                        const GemmArgs& g, int ctas, cudaStream_t s);
+                        const GemmArgs& g, int ctas, cudaStream_t s, bool pdl);
 
 // combine.cu
 cudaError_t launch_combine(const Workspace& ws, const Layout& L, const float* topk_w,
-                           uint16_t* out, int64_t T, cudaStream_t s);
+                           uint16_t* out, int64_t T, cudaStream_t s, bool pdl);
 
 }  // namespace mm

@@ -75,6 +75,7 @@ __device__ __forceinline__ void quant_dispatch_unit(const uint4 raw, bool valid,
 __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pad, int64_t T, int H, int K,
     uint8_t* __restrict__ a, uint8_t* __restrict__ a_sf) {
+  pdl_wait();
   const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
   const int KB = H >> 7;
   const int units = (KB + 1) >> 1;
@@ -98,12 +99,14 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     quant_dispatch_unit(r0, v0, p0, t0, b0, H, K, l16, a, a_sf);
     quant_dispatch_unit(r1, v1, p1, t1, b1, H, K, l16, a, a_sf);
   }
+  pdl_trigger();
 }
 
 // Unfused SwiGLU + re-quantisation over the padded GEMM rows of this forward.
 __global__ void __launch_bounds__(256) swiglu_quant_kernel(
     const uint16_t* __restrict__ gu, const int32_t* __restrict__ total_mtiles, int I,
     uint8_t* __restrict__ hq, uint8_t* __restrict__ h_sf) {
+  pdl_wait();
   const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
   const int IB = I >> 7;
   const int units = (IB + 1) >> 1;
@@ -136,6 +139,7 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
       if (l16 == 0) h_sf[sf_atom_offset(row, b, IB)] = (uint8_t)(e + 127);
     }
   }
+  pdl_trigger();
 }
 
 // 128x128 block quantisation of float weights: one CTA per block, each thread
@@ -238,20 +242,18 @@ static int stream_grid(int64_t work, int per_block) {
 }
 
 cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
-                                  int64_t T, cudaStream_t s) {
+                                  int64_t T, cudaStream_t s, bool pdl) {
   const int64_t warps = T * ((L.H / 128 + 1) / 2);
-  quant_dispatch_kernel<<<stream_grid(warps, 8), 256, 0, s>>>(x, ws.inv_pad, T, L.H, L.K, ws.a,
-                                                              ws.a_sf);
-  return cudaGetLastError();
+  return launch_k(quant_dispatch_kernel, dim3(stream_grid(warps, 8)), dim3(256), 0, s, pdl, nullptr,
+                  x, (const int32_t*)ws.inv_pad, T, L.H, L.K, ws.a, ws.a_sf);
 }
 
 cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int num_sms,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool pdl) {
   (void)num_sms;
   const int64_t warps = (L.rows_alloc) * ((L.I / 128 + 1) / 2);
-  swiglu_quant_kernel<<<stream_grid(warps, 8), 256, 0, s>>>(ws.gu, ws.total_mtiles, L.I, ws.hq,
-                                                            ws.h_sf);
-  return cudaGetLastError();
+  return launch_k(swiglu_quant_kernel, dim3(stream_grid(warps, 8)), dim3(256), 0, s, pdl, nullptr,
+                  (const uint16_t*)ws.gu, (const int32_t*)ws.total_mtiles, L.I, ws.hq, ws.h_sf);
 }
 
 cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,

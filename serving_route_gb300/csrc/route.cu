@@ -5,7 +5,9 @@
 // MegaMoE forward preparation": expert-id bounds, no duplicate routes, finite
 // scores on active routes, masked slots (-1) may carry any score).
 //
-// Three small kernels, no host synchronisation:
+// Three small kernels, no host synchronisation (the second and third are
+// launched as programmatic dependents, so their launch overlaps the previous
+// kernel):
 //   route_count   per 128-token block: validate, per-block expert histogram
 //   route_scan    one CTA: expert totals, unpadded and padded (128 or 256
 //                 rows per GEMM segment) exclusive scans, per-block bases,
@@ -25,6 +27,7 @@ constexpr int kRouteTokens = 128;  // tokens per block (one per thread in route_
 __global__ void __launch_bounds__(kRouteTokens) route_count_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ w, int T, int K, int E, int check,
     int32_t* __restrict__ block_counts, uint32_t* __restrict__ status) {
+  pdl_trigger();  // the scan may launch now; it waits for this grid to complete
   extern __shared__ int32_t hist[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -93,6 +96,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ pad_offsets,
     int32_t* __restrict__ base_u, int32_t* __restrict__ base_p, int32_t* __restrict__ mtile_expert,
     int32_t* __restrict__ total_mtiles, uint32_t* __restrict__ status) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int warp_sums[32];
   __shared__ int tot_u, tot_p;
   const int e = threadIdx.x;
@@ -131,6 +136,8 @@ __global__ void __launch_bounds__(kRouteTokens) route_scatter_kernel(
     const int32_t* __restrict__ idx, int T, int K, int E, int64_t rows_alloc,
     const int32_t* __restrict__ base_u, const int32_t* __restrict__ base_p,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ inv_pad) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int32_t wh[];  // [4 warps][E]: per-warp counts, then running bases
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kWarps = kRouteTokens / 32;
@@ -196,18 +203,21 @@ cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* to
   const int E = L.E;
   const int max_mtiles = (int)(L.rows_alloc / 128);
   if (ev) record_event(ev[0], s);
-  route_count_kernel<<<nb, kRouteTokens, sizeof(int32_t) * E, s>>>(
-      topk_idx, topk_w, (int)T, L.K, E, check ? 1 : 0, ws.block_counts, ws.status);
+  cudaError_t err = launch_k(route_count_kernel, dim3(nb), dim3(kRouteTokens), sizeof(int32_t) * E, s,
+                             false, nullptr, topk_idx, topk_w, (int)T, L.K, E, check ? 1 : 0,
+                             ws.block_counts, ws.status);
+  if (err != cudaSuccess) return err;
   if (ev) record_event(ev[1], s);
   const int pad_rows = L.pad_rows > 0 ? L.pad_rows : 128;
-  route_scan_kernel<<<1, 1024, 0, s>>>(ws.block_counts, nb, E, pad_rows, L.rows_alloc, max_mtiles,
-                                       ws.counts,
-                                       ws.offsets, ws.pad_offsets, ws.base_u, ws.base_p,
-                                       ws.mtile_expert, ws.total_mtiles, ws.status);
+  err = launch_k(route_scan_kernel, dim3(1), dim3(1024), 0, s, ev == nullptr, nullptr,
+                 (const int32_t*)ws.block_counts, nb, E, pad_rows, L.rows_alloc, max_mtiles, ws.counts,
+                 ws.offsets, ws.pad_offsets, ws.base_u, ws.base_p, ws.mtile_expert, ws.total_mtiles,
+                 ws.status);
+  if (err != cudaSuccess) return err;
   if (ev) record_event(ev[2], s);
-  route_scatter_kernel<<<nb, kRouteTokens, sizeof(int32_t) * 4 * E, s>>>(
-      topk_idx, (int)T, L.K, E, L.rows_alloc, ws.base_u, ws.base_p, ws.perm, ws.inv, ws.inv_pad);
-  return cudaGetLastError();
+  return launch_k(route_scatter_kernel, dim3(nb), dim3(kRouteTokens), sizeof(int32_t) * 4 * E, s,
+                  ev == nullptr, nullptr, topk_idx, (int)T, L.K, E, L.rows_alloc,
+                  (const int32_t*)ws.base_u, (const int32_t*)ws.base_p, ws.perm, ws.inv, ws.inv_pad);
 }
 
 }  // namespace mm
