@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--gemm", default="auto", choices=["auto", "single", "pair"])
     p.add_argument("--experts", type=int, default=0,
                    help="profiling only: the workload with this many experts (smaller weights)")
+    p.add_argument("--tokens", type=int, default=0,
+                   help="profiling only: the workload with this many tokens")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
@@ -245,10 +247,12 @@ def main():
     from gen import inputs as g
 
     wl = configs.WORKLOADS[args.config]
-    if args.experts:
+    if args.experts or args.tokens:
         from gen.configs import Workload
-        wl = Workload(f"{wl.name}_E{args.experts}", wl.T, wl.H, wl.I, args.experts, wl.K,
-                      wl.routing, wl.seed)
+        E = args.experts or wl.E
+        T = args.tokens or wl.T
+        name = wl.name + (f"_E{E}" if args.experts else "") + (f"_T{T}" if args.tokens else "")
+        wl = Workload(name, T, wl.H, wl.I, E, wl.K, wl.routing, wl.seed)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream()
     sp = stream.cuda_stream
