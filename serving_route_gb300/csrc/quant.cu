@@ -41,33 +41,52 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 p, float (&v)[8]) {
   }
 }
 
-// One warp handles two 128-column blocks of one token per unit (one per
-// half-warp); each lane owns 8 consecutive columns.  Each iteration processes
-// two units whose loads are issued together, so every warp keeps two 512-byte
-// reads in flight.
-__device__ __forceinline__ void quant_dispatch_unit(const uint4 raw, bool valid, int p_lane,
-                                                    int64_t t, int b, int H, int K, int l16,
+// One warp handles four 128-column blocks of one token per unit: eight lanes
+// per block, each lane owning 16 consecutive columns (two 16-byte loads, one
+// 16-byte store per route).  Each iteration processes two units whose loads
+// are issued together, so every warp keeps 2 KB of reads in flight, and each
+// store instruction of the warp writes four whole 128-byte lines.
+__device__ __forceinline__ float group8_max(float v) {
+#pragma unroll
+  for (int o = 4; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ void quant_dispatch_unit(const uint4 (&raw)[2], bool valid, int p_lane,
+                                                    int b, int H, int K, int l8,
                                                     uint8_t* __restrict__ a,
                                                     uint8_t* __restrict__ a_sf) {
-  float v[8];
+  float v[16];
   if (valid) {
-    unpack_bf16x8(raw, v);
+    float lo[8], hi[8];
+    unpack_bf16x8(raw[0], lo);
+    unpack_bf16x8(raw[1], hi);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = lo[i];
+      v[8 + i] = hi[i];
+    }
   } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    for (int i = 0; i < 16; ++i) v[i] = 0.f;
   }
   float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  amax = half_warp_max(amax);
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = group8_max(amax);
   const int e = pow2_scale_exp(amax);
-  const uint2 q = quant8(v, e);
+  const float inv = pow2_neg(e);
+  uint4 q;
+  q.x = e4m3x4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+  q.y = e4m3x4(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
+  q.z = e4m3x4(v[8] * inv, v[9] * inv, v[10] * inv, v[11] * inv);
+  q.w = e4m3x4(v[12] * inv, v[13] * inv, v[14] * inv, v[15] * inv);
   const int KB = H >> 7;
   for (int k = 0; k < K; ++k) {
     const int p = __shfl_sync(0xFFFFFFFFu, p_lane, k);
     if (p >= 0 && valid) {
-      *reinterpret_cast<uint2*>(a + (int64_t)p * H + b * 128 + l16 * 8) = q;
-      if (l16 == 0) a_sf[sf_atom_offset(p, b, KB)] = (uint8_t)(e + 127);
+      *reinterpret_cast<uint4*>(a + (int64_t)p * H + b * 128 + l8 * 16) = q;
+      if (l8 == 0) a_sf[sf_atom_offset(p, b, KB)] = (uint8_t)(e + 127);
     }
   }
 }
@@ -76,9 +95,9 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pad, int64_t T, int H, int K,
     uint8_t* __restrict__ a, uint8_t* __restrict__ a_sf) {
   pdl_wait();
-  const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
+  const int lane = threadIdx.x & 31, grp = lane >> 3, l8 = lane & 7;
   const int KB = H >> 7;
-  const int units = (KB + 1) >> 1;
+  const int units = (KB + 3) >> 2;
   const int64_t total = T * units;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t u0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u0 < total;
@@ -86,18 +105,22 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     const int64_t u1 = u0 + nwarps;
     const bool has1 = u1 < total;
     const int64_t t0 = u0 / units, t1 = has1 ? u1 / units : t0;
-    const int b0 = (int)(u0 - t0 * units) * 2 + half;
-    const int b1 = has1 ? (int)(u1 - t1 * units) * 2 + half : b0;
+    const int b0 = (int)(u0 - t0 * units) * 4 + grp;
+    const int b1 = has1 ? (int)(u1 - t1 * units) * 4 + grp : b0;
     const bool v0 = b0 < KB, v1 = has1 && b1 < KB;
     // both units' loads first
-    const uint4 r0 = v0 ? *reinterpret_cast<const uint4*>(x + t0 * H + b0 * 128 + l16 * 8)
-                        : make_uint4(0u, 0u, 0u, 0u);
-    const uint4 r1 = v1 ? *reinterpret_cast<const uint4*>(x + t1 * H + b1 * 128 + l16 * 8)
-                        : make_uint4(0u, 0u, 0u, 0u);
+    uint4 r0[2], r1[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      r0[h] = v0 ? *reinterpret_cast<const uint4*>(x + t0 * H + b0 * 128 + l8 * 16 + h * 8)
+                 : make_uint4(0u, 0u, 0u, 0u);
+      r1[h] = v1 ? *reinterpret_cast<const uint4*>(x + t1 * H + b1 * 128 + l8 * 16 + h * 8)
+                 : make_uint4(0u, 0u, 0u, 0u);
+    }
     const int p0 = (lane < K) ? inv_pad[t0 * K + lane] : -1;
     const int p1 = (lane < K && has1) ? inv_pad[t1 * K + lane] : -1;
-    quant_dispatch_unit(r0, v0, p0, t0, b0, H, K, l16, a, a_sf);
-    quant_dispatch_unit(r1, v1, p1, t1, b1, H, K, l16, a, a_sf);
+    quant_dispatch_unit(r0, v0, p0, b0, H, K, l8, a, a_sf);
+    quant_dispatch_unit(r1, v1, p1, b1, H, K, l8, a, a_sf);
   }
   pdl_trigger();
 }
@@ -243,7 +266,7 @@ static int stream_grid(int64_t work, int per_block) {
 
 cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
                                   int64_t T, cudaStream_t s, bool pdl) {
-  const int64_t warps = T * ((L.H / 128 + 1) / 2);
+  const int64_t warps = T * ((L.H / 128 + 3) / 4);
   return launch_k(quant_dispatch_kernel, dim3(stream_grid(warps, 8)), dim3(256), 0, s, pdl, nullptr,
                   x, (const int32_t*)ws.inv_pad, T, L.H, L.K, ws.a, ws.a_sf);
 }
