@@ -383,44 +383,92 @@ def main():
         raise RuntimeError(f"timed forwards reported device status {bits:#x}")
 
     # ---------------------------------------------------------------- e2e
-    # the public call a user makes with host buffers: pinned H2D of x and the
-    # routes, the forward, D2H of the output; all inside the timed span
+    # The public call a user makes with host buffers: every step copies its x
+    # and routes from pinned host memory and reads its output back, all inside
+    # the timed span.  Two figures: (1) serial -- copy in, forward, copy out,
+    # one step after the other on one stream; (2) pipelined, the way a serving
+    # loop runs it -- two device slots, copies on their own streams, so step
+    # i+1's inputs and step i-1's output move while step i computes.  The
+    # value is the pipelined figure; the serial one is reported beside it.
     x_host = torch.from_numpy(problem.x_bits(wl).view(np.int16).copy()).view(torch.bfloat16).pin_memory()
     idx_host = torch.from_numpy(idx_np).pin_memory()
     w_host = torch.from_numpy(w_np).pin_memory()
-    out_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
-    x_d = torch.empty_like(x)
-    idx_d = torch.empty_like(idx)
-    w_d = torch.empty_like(wts)
+    out_host = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_d = [torch.empty_like(x) for _ in range(2)]
+    idx_d = [torch.empty_like(idx) for _ in range(2)]
+    w_d = [torch.empty_like(wts) for _ in range(2)]
+    out_d = [layer.out, torch.empty_like(layer.out)]
     h2d = x_host.numel() * 2 + idx_host.numel() * 4 + w_host.numel() * 4
-    d2h = out_host.numel() * 2
+    d2h = out_host[0].numel() * 2
     layer.set_profile_events([])
 
-    def e2e_step():
+    def e2e_serial_step():
         with torch.cuda.stream(stream):
-            x_d.copy_(x_host, non_blocking=True)
-            idx_d.copy_(idx_host, non_blocking=True)
-            w_d.copy_(w_host, non_blocking=True)
-            out = layer.forward(x_d, idx_d, w_d, stream=stream)
-            out_host.copy_(out, non_blocking=True)
+            x_d[0].copy_(x_host, non_blocking=True)
+            idx_d[0].copy_(idx_host, non_blocking=True)
+            w_d[0].copy_(w_host, non_blocking=True)
+            out = layer.forward(x_d[0], idx_d[0], w_d[0], stream=stream)
+            out_host[0].copy_(out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
-        e2e_step()
+        e2e_serial_step()
     stream.synchronize()
-    e2e_ms = 0.0
+    e2e_serial_ms = 0.0
     for _ in range(args.steps):
         with torch.cuda.stream(stream):
             flush.zero_()
             t_start.record(stream)
-        e2e_step()
+        e2e_serial_step()
         with torch.cuda.stream(stream):
             t_end.record(stream)
         stream.synchronize()
-        e2e_ms += t_start.elapsed_time(t_end)
-    e2e_ms = reduce_max(e2e_ms, dev)
+        e2e_serial_ms += t_start.elapsed_time(t_end)
+    e2e_serial_ms = reduce_max(e2e_serial_ms, dev)
+
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_h2d = [torch.cuda.Event() for _ in range(2)]
+    ev_fwd = [torch.cuda.Event() for _ in range(2)]
+    ev_d2h = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_pipelined(n):
+        for e in ev_fwd + ev_d2h:
+            e.record(stream)
+        for i in range(n):
+            s = i & 1
+            with torch.cuda.stream(h2d_stream):
+                h2d_stream.wait_event(ev_fwd[s])      # the slot's previous forward has read it
+                x_d[s].copy_(x_host, non_blocking=True)
+                idx_d[s].copy_(idx_host, non_blocking=True)
+                w_d[s].copy_(w_host, non_blocking=True)
+                ev_h2d[s].record(h2d_stream)
+            stream.wait_event(ev_h2d[s])
+            stream.wait_event(ev_d2h[s])               # the slot's previous output is on the host
+            layer.stage_output(out_d[s])
+            layer.forward(x_d[s], idx_d[s], w_d[s], stream=stream)
+            ev_fwd[s].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(ev_fwd[s])
+                out_host[s].copy_(out_d[s][:wl.T], non_blocking=True)
+                ev_d2h[s].record(d2h_stream)
+        stream.wait_event(ev_d2h[(n - 1) & 1])
+        stream.wait_event(ev_d2h[n & 1])
+
+    with torch.cuda.stream(stream):
+        e2e_pipelined(max(2, args.warmup))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        flush.zero_()
+        t_start.record(stream)
+        e2e_pipelined(args.steps)
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(t_start.elapsed_time(t_end), dev)
+    layer.stage_output(out_d[0])
     st, bits = layer.read_status(stream)
     if st != 0:
         raise RuntimeError(f"e2e forwards reported device status {bits:#x}")
+    if not torch.equal(out_host[0], out_host[1]):
+        raise RuntimeError("pipelined end-to-end outputs differ between the two slots")
 
     # ---------------------------------------------------------------- report
     K = args.steps
@@ -473,7 +521,11 @@ def main():
         "gpu_launches": K * (7 if fused else 8),
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / K},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / K,
+                "copies": "pipelined: two device slots; H2D and D2H on their own streams overlap the "
+                          "neighbouring steps' forwards",
+                "serial": {"value": aggregate_rate(world, flops, K, e2e_serial_ms) / 1e12,
+                           "ms_per_step": e2e_serial_ms / K}},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x_bits = x_host.view(torch.int16).numpy().view(np.uint16)

@@ -23,8 +23,8 @@ struct moe_handle {
   int64_t expected_m;
   Workspace ws;
   WeightStore wst;
-  CUtensorMap tm_a, tm_hq, tm_w1, tm_w2;   // weight maps: 256-row boxes (single CTA)
-  CUtensorMap tm_w1p, tm_w2p;               // weight maps: 128-row boxes (CTA pairs)
+  CUtensorMap tm_a, tm_hq;                  // activations: 128-row boxes
+  CUtensorMap tm_w1, tm_w2;                 // blocked weights: one 128x128 box per load
   CUtensorMap tm_asf, tm_hsf;               // scale atoms as 2-D uint32 tensors (CTA pairs)
   CUtensorMap tm_w1sf, tm_w2sf;             // weight scale atoms, same form (CTA pairs)
   CUtensorMap tm_y;                         // FC2 output, 32x32 BF16 boxes (TMA stores)
@@ -90,6 +90,21 @@ bool encode_bf16_store_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t r
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Blocked weight store [row blocks][kblocks][128 rows][128 B] as a 3-D byte
+// tensor {128, kblocks * 128, row blocks}; box {128, 128, 1} = one contiguous
+// 16 KB block, 128-byte swizzle.
+bool encode_blocked_map(CUtensorMap* m, const void* base, uint64_t kblocks, uint64_t row_blocks) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, kblocks * 128, row_blocks};
+  cuuint64_t strides[2] = {128, kblocks * 128 * 128};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -314,10 +329,8 @@ moe_status moe_bind_weights(moe_handle* h, const uint8_t* d_w1, const float* d_w
       cudaStreamSynchronize(stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (st & MOE_DEV_BAD_SCALE) return MOE_ERR_BAD_SCALE;
-  if (!encode_u8_map(&h->tm_w1, h->wst.w1, L.H, (uint64_t)L.E * 2 * L.I, 256) ||
-      !encode_u8_map(&h->tm_w2, h->wst.w2, L.I, (uint64_t)L.E * L.H, 256) ||
-      !encode_u8_map(&h->tm_w1p, h->wst.w1, L.H, (uint64_t)L.E * 2 * L.I, 128) ||
-      !encode_u8_map(&h->tm_w2p, h->wst.w2, L.I, (uint64_t)L.E * L.H, 128))
+  if (!encode_blocked_map(&h->tm_w1, h->wst.w1, L.H / 128, (uint64_t)L.E * (2 * L.I / 128)) ||
+      !encode_blocked_map(&h->tm_w2, h->wst.w2, L.I / 128, (uint64_t)L.E * (L.H / 128)))
     return MOE_ERR_CUDA;
   h->bound = true;
   return MOE_OK;
@@ -384,7 +397,7 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   if (ev) record_event(ev[5], s);
   const bool pair = L.pair;
   const int ctas = pair ? h->pair_ctas : h->num_sms;
-  if (launch_gemm(m1, pair, &h->tm_a, pair ? &h->tm_w1p : &h->tm_w1, &h->tm_asf, &h->tm_w1sf,
+  if (launch_gemm(m1, pair, &h->tm_a, &h->tm_w1, &h->tm_asf, &h->tm_w1sf,
                   &h->tm_y, g1, ctas, s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[6], s);
@@ -407,7 +420,7 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.status = ws.status;
   g2.wait_limit_ns = g1.wait_limit_ns;
   if (ev) record_event(ev[7], s);
-  if (launch_gemm(kModeY, pair, &h->tm_hq, pair ? &h->tm_w2p : &h->tm_w2, &h->tm_hsf, &h->tm_w2sf,
+  if (launch_gemm(kModeY, pair, &h->tm_hq, &h->tm_w2, &h->tm_hsf, &h->tm_w2sf,
                   &h->tm_y, g2, ctas, s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[8], s);

@@ -162,11 +162,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = e_next;
       e_next = expert_of(u + ustride);
       const int nt = u - (u / g.NT) * g.NT;
-      // weight rows: expert e, 256-row n-tile; a pair CTA stages its half
-      const int y_b = e * g.N + nt * 256 + (int)rank * (int)C::kBRows;
-      // B scale atoms of the n-tile's two 128-row blocks (the second clamped
-      // to the first past N: those output columns are never stored)
+      // the n-tile's two 128-row weight blocks (the second clamped to the
+      // first past N: those output columns are never stored); a pair CTA
+      // stages the block of its rank
       const int nb0 = 2 * nt, nb1 = (2 * nt + 1 < g.NB) ? 2 * nt + 1 : 2 * nt;
+      const int wb0 = e * g.NB + nb0, wb1 = e * g.NB + nb1;
       const int64_t sfb0 = ((int64_t)e * g.NB + nb0) * g.KQ, sfb1 = ((int64_t)e * g.NB + nb1) * g.KQ;
       const int64_t sfa0 = (int64_t)mt * g.KQ;
       bool ok = true;
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(smem_u32(&full_bar[stage]),
                                     2 * (C::kTxBytes + (atoms ? C::kTxAtomBytes : 0u)));
             tma_load_2d_pair(sst + C::kOffA, &tmA, fb, kb * 128, mt * 128);
-            tma_load_2d_pair(sst + C::kOffB, &tmB, fb, kb * 128, y_b);
+            tma_load_3d_pair(sst + C::kOffB, &tmB, fb, 0, kb * 128, rank ? wb1 : wb0);
             if (atoms) {
               tma_load_2d_pair(sst + C::kOffSfa, &tmSfa, fb, 0, (int)(sfa0 + q));
               tma_load_2d_pair(sst + C::kOffSfb, &tmSfb, fb, 0, (int)(sfb0 + q));
@@ -207,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fb = smem_u32(&full_bar[stage]);
             mbar_arrive_expect_tx(fb, C::kTxBytes + (atoms ? C::kTxAtomBytes : 0u));
             tma_load_2d(sst + C::kOffA, &tmA, fb, kb * 128, mt * 128);
-            tma_load_2d(sst + C::kOffB, &tmB, fb, kb * 128, y_b);
+            tma_load_3d(sst + C::kOffB, &tmB, fb, 0, kb * 128, wb0);
+            tma_load_3d(sst + C::kOffB + 16384, &tmB, fb, 0, kb * 128, wb1);
             if (atoms) {
               bulk_load(sst + C::kOffSfa, g.sfa + (sfa0 + q) * kSfAtomBytes, kSfAtomBytes, fb);
               bulk_load(sst + C::kOffSfb, g.sfb + (sfb0 + q) * kSfAtomBytes, kSfAtomBytes, fb);

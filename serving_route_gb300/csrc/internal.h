@@ -33,8 +33,9 @@ struct Workspace {
 };
 
 struct WeightStore {
-  uint8_t* w1;     // [E, 2I, H]: per 256-row tile j, gate rows 128j.. then up rows 128j..
-  uint8_t* w2;     // [E, H, I]
+  uint8_t* w1;     // [E][2I/128][H/128][128][128]: 128x128 blocks, each contiguous; row blocks
+                   // in the order gate 0, up 0, gate 1, up 1, ... (one 256-row FC1 tile = gate j + up j)
+  uint8_t* w2;     // [E][H/128][I/128][128][128]
   uint8_t* w1_sf;  // [E, 2I/128, H/128] E8M0, in the interleaved row-block order of w1
   uint8_t* w2_sf;  // [E, H/128, I/128] E8M0
   uint8_t* w1_sfatoms;  // [E][2I/128][ceil(H/512)][512]: w1_sf as GEMM scale atoms
@@ -103,9 +104,10 @@ struct GemmArgs {
 };
 cudaError_t gemm_set_attributes();
 int gemm_max_pairs();
-// pair: CTA-pair kernel (tmB boxes of 128 rows, tmSfa / tmSfb = the A / B
+// tmB: the blocked weight store as a 3-D map (one 128x128 block per box).
+// pair: CTA-pair kernel (tmSfa / tmSfb = the A / B
 // scale atoms as 2-D uint32 tensors of 512-byte rows); otherwise the
-// single-CTA kernel (tmB boxes of 256 rows; scale atoms by bulk copy from
+// single-CTA kernel (scale atoms by bulk copy from
 // g.sfa / g.sfb).  tmY: the FC2 output [rows, H] BF16 with
 // 32x32 boxes and 64-byte swizzle (TMA stores of kModeY).  ctas: grid size
 // (even for pairs).

@@ -221,21 +221,34 @@ __device__ __forceinline__ uint8_t scale_to_e8m0(float s, uint32_t* status) {
   return 127;
 }
 
-// W1 rows reordered so that 256-row tile j holds gate rows [128j, 128j+128)
-// followed by up rows [128j, 128j+128): one FC1 tile then owns all 128 SwiGLU
-// columns of one 1x128 re-quantisation block.
-__global__ void bind_w1_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                               int E, int I, int H) {
-  const int64_t chunks_per_row = H / 16;
-  const int64_t total = (int64_t)E * 2 * I * chunks_per_row;
+// Bind-time weight layout: every 128-row x 128-column block of an expert's
+// matrix is stored as one contiguous 16 KB box, [E][N/128][K/128][128][128],
+// so a GEMM stage's weight box is one sequential DRAM read.  For W1 the
+// rows are first re-ordered so that 256-row tile j is gate rows
+// [128j, 128j+128) followed by up rows [128j, 128j+128) (one FC1 tile then
+// owns whole 1x128 blocks of h).  One thread per 16-byte chunk.
+__global__ void bind_blocked_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                   int E, int N, int K, int gate_up) {
+  const int NB = N / 128, KB = K / 128;
+  const int64_t total = (int64_t)E * N * (K / 16);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = i / chunks_per_row, ch = i % chunks_per_row;
-    const int64_t e = row / (2 * I), n = row % (2 * I);
-    const int64_t j = n >> 8, within = n & 255;
-    const int64_t src_n = (within < 128) ? (j * 128 + within) : (I + j * 128 + within - 128);
+    // destination index -> (e, nb, kb, r, c)
+    const int c = (int)(i & 7);
+    const int r = (int)((i >> 3) & 127);
+    const int64_t blk = i >> 10;  // (e * NB + nb) * KB + kb
+    const int kb = (int)(blk % KB);
+    const int64_t enb = blk / KB;
+    const int nb = (int)(enb % NB);
+    const int64_t e = enb / NB;
+    int64_t n = (int64_t)nb * 128 + r;  // row of the (re-ordered) matrix
+    if (gate_up) {
+      const int I = N / 2;
+      const int64_t j = n >> 8, within = n & 255;
+      n = (within < 128) ? (j * 128 + within) : (I + j * 128 + within - 128);
+    }
     reinterpret_cast<uint4*>(dst)[i] =
-        reinterpret_cast<const uint4*>(src + (e * 2 * I + src_n) * H)[ch];
+        *reinterpret_cast<const uint4*>(src + (e * N + n) * (int64_t)K + kb * 128 + c * 16);
   }
 }
 
@@ -316,10 +329,9 @@ cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const
                                   const float* w1s, const uint8_t* w2, const float* w2s,
                                   uint32_t* status, cudaStream_t s) {
   const int E = L.E, I = L.I, H = L.H;
-  const int64_t w1_chunks = (int64_t)E * 2 * I * (H / 16);
-  bind_w1_kernel<<<stream_grid(w1_chunks, 256), 256, 0, s>>>(w1, wst.w1, E, I, H);
-  cudaError_t err = cudaMemcpyAsync(wst.w2, w2, (size_t)E * H * I, cudaMemcpyDeviceToDevice, s);
-  if (err != cudaSuccess) return err;
+  const int64_t w1_chunks = (int64_t)E * 2 * I * (H / 16), w2_chunks = (int64_t)E * H * (I / 16);
+  bind_blocked_kernel<<<stream_grid(w1_chunks, 256), 256, 0, s>>>(w1, wst.w1, E, 2 * I, H, 1);
+  bind_blocked_kernel<<<stream_grid(w2_chunks, 256), 256, 0, s>>>(w2, wst.w2, E, H, I, 0);
   const int64_t n1 = (int64_t)E * 2 * (I / 128) * (H / 128);
   bind_w1_scale_kernel<<<stream_grid(n1, 256), 256, 0, s>>>(w1s, wst.w1_sf, E, I / 128, H / 128,
                                                             status);

@@ -58,6 +58,15 @@ class MegaMoELayer:
                            w2_s.data_ptr(), _stream_ptr(stream))
 
     # -- forward ------------------------------------------------------------------
+    def stage_output(self, out: torch.Tensor) -> None:
+        """Bind another BF16 [max_rows, H] output buffer (moe_stage_inputs); the
+        following forwards write there (e.g. two buffers in turn, so the
+        device-to-host copy of one forward's output overlaps the next forward)."""
+        assert out.dtype == torch.bfloat16 and out.is_cuda and out.is_contiguous()
+        assert out.shape[0] >= self.max_rows and out.shape[1] == self.H
+        B.moe_stage_inputs(self.handle, out.data_ptr())
+        self.out = out
+
     def forward(self, x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
                 num_tokens: int | None = None, stream=None) -> torch.Tensor:
         T = x.shape[0] if num_tokens is None else num_tokens
