@@ -50,6 +50,8 @@ def parse():
                    help="profiling only: the workload with this many experts (smaller weights)")
     p.add_argument("--tokens", type=int, default=0,
                    help="profiling only: the workload with this many tokens")
+    p.add_argument("--sm-budget", type=int, default=0,
+                   help="cap the SMs the layer occupies (moe_set_sm_budget; 0: every SM)")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
@@ -297,6 +299,8 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
+    if args.sm_budget:
+        layer.set_sm_budget(args.sm_budget)
     dbg = layer.debug()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
 
@@ -508,6 +512,7 @@ def main():
                    "l2": "flushed before every step (256 MiB write, untimed)",
                    "launch": "cuda graph replay" if graph is not None else "direct launches",
                    "gemm": ("cta pairs" if dbg["gemm_pair"] else "single cta") + f" x{dbg['gemm_ctas']}",
+                   "sm_budget": args.sm_budget or None,
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": aggregate_rate(world, wl.T, K, total_ms),
         "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,

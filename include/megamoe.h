@@ -221,6 +221,20 @@ MOE_API moe_status moe_debug_views(moe_handle* h, moe_debug_view* out);
 MOE_API moe_status moe_set_profile_events(moe_handle* h, void* const* events, int32_t n);
 
 /*
+ * moe_set_sm_budget -- caps the SMs the following forwards occupy, so that
+ * work on another stream (a shared expert, attention of the next layer) can
+ * run beside the layer (flashinfer PR #6398, the max_sm_count budget in a
+ * referencing commit: capping the persistent MoE kernels lets a shared-expert
+ * MLP on a side stream run at the same time).  max_sms = 0 restores the
+ * default (every SM).  Otherwise 2 <= max_sms: the persistent GEMMs launch
+ * min(max_sms, SM count) CTAs (one per SM; rounded down to an even count for
+ * CTA pairs) and the streaming kernels (quantisation, combine) at most
+ * max_sms CTAs.  Results are bit-identical for every budget.  Errors:
+ * MOE_ERR_INVALID_ARG for a NULL handle or max_sms < 0 or == 1.
+ */
+MOE_API moe_status moe_set_sm_budget(moe_handle* h, int32_t max_sms);
+
+/*
  * moe_route_noalloc -- the routing step alone, allocating nothing.  The pages
  * have no counterpart to this call; it exists for callers that cannot
  * allocate device memory and have no workspace to offer, for example a plugin

@@ -42,7 +42,8 @@ MOE_FLAG_WATCHDOG_TEST = 0x20
 # every function the header declares (checked against include/megamoe.h by a test)
 API_NAMES = ("moe_workspace_query", "moe_create", "moe_quantize_weights", "moe_bind_weights",
              "moe_stage_inputs", "moe_forward", "moe_read_status", "moe_debug_views",
-             "moe_set_profile_events", "moe_route_noalloc", "moe_destroy", "moe_status_str")
+             "moe_set_profile_events", "moe_set_sm_budget", "moe_route_noalloc", "moe_destroy",
+             "moe_status_str")
 
 
 class moe_dims(ctypes.Structure):
@@ -91,6 +92,7 @@ def lib() -> ctypes.CDLL:
         L.moe_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         L.moe_debug_views.argtypes = [vp, ctypes.POINTER(moe_debug_view)]
         L.moe_set_profile_events.argtypes = [vp, ctypes.POINTER(vp), i32]
+        L.moe_set_sm_budget.argtypes = [vp, i32]
         L.moe_route_noalloc.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.moe_destroy.argtypes = [vp]
         L.moe_destroy.restype = None
@@ -172,6 +174,10 @@ def moe_set_profile_events(h, event_handles) -> None:
     n = len(event_handles)
     arr = (ctypes.c_void_p * max(n, 1))(*event_handles)
     _check(lib().moe_set_profile_events(h, arr, n), "moe_set_profile_events")
+
+
+def moe_set_sm_budget(h, max_sms) -> None:
+    _check(lib().moe_set_sm_budget(h, max_sms), "moe_set_sm_budget")
 
 
 def moe_route_noalloc(d_idx, d_w, num_tokens, top_k, num_experts, check_routes, d_counts,

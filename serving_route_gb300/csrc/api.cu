@@ -29,6 +29,7 @@ struct moe_handle {
   CUtensorMap tm_w1sf, tm_w2sf;             // weight scale atoms, same form (CTA pairs)
   CUtensorMap tm_y;                         // FC2 output, 32x32 BF16 boxes (TMA stores)
   int pair_ctas;                            // grid of the CTA-pair GEMMs
+  int sm_budget;                            // moe_set_sm_budget (0: every SM)
   bool bound;
   uint16_t* out;
   int num_sms;
@@ -120,6 +121,18 @@ bool encode_atom_map(CUtensorMap* m, const void* base, uint64_t n_atoms) {
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// SMs a forward may occupy, and the GEMM grid that follows from it.
+int budget_sms(const moe_handle* h) {
+  return (h->sm_budget > 0 && h->sm_budget < h->num_sms) ? h->sm_budget : h->num_sms;
+}
+
+int gemm_grid(const moe_handle* h) {
+  const int sms = budget_sms(h);
+  if (!h->L.pair) return sms;
+  const int c = sms & ~1;
+  return c < h->pair_ctas ? c : h->pair_ctas;
 }
 
 }  // namespace
@@ -369,7 +382,10 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   // Kernels after the first are programmatic dependents of their predecessor
   // unless profiling events sit between them.
   const bool pdl = ev == nullptr;
-  if (launch_quant_dispatch(ws, L, d_x, num_tokens, s, pdl) != cudaSuccess) return MOE_ERR_CUDA;
+  // streaming kernels: up to 16 CTAs per SM, or one per SM of the budget
+  const int stream_ctas = h->sm_budget > 0 ? budget_sms(h) : 16 * h->num_sms;
+  if (launch_quant_dispatch(ws, L, d_x, num_tokens, s, pdl, stream_ctas) != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   GemmArgs g1;
   memset(&g1, 0, sizeof(g1));
@@ -396,12 +412,12 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   const GemmMode m1 = fused ? (emit ? kModeFusedGU : kModeFused) : kModeGU;
   if (ev) record_event(ev[5], s);
   const bool pair = L.pair;
-  const int ctas = pair ? h->pair_ctas : h->num_sms;
+  const int ctas = gemm_grid(h);
   if (launch_gemm(m1, pair, &h->tm_a, &h->tm_w1, &h->tm_asf, &h->tm_w1sf,
                   &h->tm_y, g1, ctas, s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[6], s);
-  if (!fused && launch_swiglu_quant(ws, L, h->num_sms, s, pdl) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!fused && launch_swiglu_quant(ws, L, stream_ctas, s, pdl) != cudaSuccess) return MOE_ERR_CUDA;
 
   GemmArgs g2;
   memset(&g2, 0, sizeof(g2));
@@ -424,7 +440,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
                   &h->tm_y, g2, ctas, s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[8], s);
-  if (launch_combine(ws, L, d_topk_w, h->out, num_tokens, s, pdl) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_combine(ws, L, d_topk_w, h->out, num_tokens, s, pdl, stream_ctas) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (ev) record_event(ev[9], s);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -463,7 +480,7 @@ moe_status moe_debug_views(moe_handle* h, moe_debug_view* v) {
   v->rows_alloc = h->L.rows_alloc;
   v->sf_atom_bytes = kSfAtomBytes;
   v->gemm_pair = h->L.pair ? 1 : 0;
-  v->gemm_ctas = h->L.pair ? h->pair_ctas : h->num_sms;
+  v->gemm_ctas = gemm_grid(h);
   v->pad_rows = h->L.pad_rows;
   return MOE_OK;
 }
@@ -479,6 +496,12 @@ moe_status moe_set_profile_events(moe_handle* h, void* const* events, int32_t n)
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   for (int i = 0; i < 10; ++i) h->ev[i] = reinterpret_cast<cudaEvent_t>(events[i]);
   h->n_ev = 10;
+  return MOE_OK;
+}
+
+moe_status moe_set_sm_budget(moe_handle* h, int32_t max_sms) {
+  if (!h || max_sms < 0 || max_sms == 1) return MOE_ERR_INVALID_ARG;
+  h->sm_budget = max_sms;
   return MOE_OK;
 }
 

@@ -73,10 +73,10 @@ static cudaError_t launch_k_combine(const Workspace& ws, const Layout& L, const 
 }
 
 cudaError_t launch_combine(const Workspace& ws, const Layout& L, const float* topk_w,
-                           uint16_t* out, int64_t T, cudaStream_t s, bool pdl) {
+                           uint16_t* out, int64_t T, cudaStream_t s, bool pdl, int max_ctas) {
   const int col_ctas = (L.H + kColsPerCta - 1) / kColsPerCta;
   int64_t units = T * col_ctas;
-  const int64_t cap = 152 * 16;
+  const int64_t cap = max_ctas;
   const unsigned grid = (unsigned)(units < cap ? (units < 1 ? 1 : units) : cap);
   switch (L.K) {
     case 1: return launch_k_combine<1>(ws, L, topk_w, out, T, col_ctas, grid, s, pdl);

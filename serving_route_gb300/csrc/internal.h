@@ -68,10 +68,11 @@ cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* to
                          cudaEvent_t const* ev);
 
 // quant.cu
-// pdl: launch as a programmatic dependent of the previous kernel on `s`
+// pdl: launch as a programmatic dependent of the previous kernel on `s`;
+// max_ctas: grid cap of the streaming kernels
 cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
-                                  int64_t T, cudaStream_t s, bool pdl);
-cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int num_sms, cudaStream_t s,
+                                  int64_t T, cudaStream_t s, bool pdl, int max_ctas);
+cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int max_ctas, cudaStream_t s,
                                 bool pdl);
 cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
                                     float* scale, cudaStream_t s);
@@ -117,6 +118,6 @@ cudaError_t launch_gemm(GemmMode mode, bool pair, const CUtensorMap* tmA, const 
 
 // combine.cu
 cudaError_t launch_combine(const Workspace& ws, const Layout& L, const float* topk_w,
-                           uint16_t* out, int64_t T, cudaStream_t s, bool pdl);
+                           uint16_t* out, int64_t T, cudaStream_t s, bool pdl, int max_ctas);
 
 }  // namespace mm

@@ -271,24 +271,24 @@ __global__ void scale_convert_kernel(const float* __restrict__ s, uint8_t* __res
     d[i] = scale_to_e8m0(s[i], status);
 }
 
-static int stream_grid(int64_t work, int per_block) {
+static int stream_grid(int64_t work, int per_block, int64_t cap = 152 * 16) {
   int64_t b = (work + per_block - 1) / per_block;
-  const int64_t cap = 152 * 16;
   return (int)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 
 cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
-                                  int64_t T, cudaStream_t s, bool pdl) {
+                                  int64_t T, cudaStream_t s, bool pdl, int max_ctas) {
   const int64_t warps = T * ((L.H / 128 + 3) / 4);
-  return launch_k(quant_dispatch_kernel, dim3(stream_grid(warps, 8)), dim3(256), 0, s, pdl, nullptr,
+  return launch_k(quant_dispatch_kernel, dim3(stream_grid(warps, 8, max_ctas)), dim3(256), 0, s, pdl,
+                  nullptr,
                   x, (const int32_t*)ws.inv_pad, T, L.H, L.K, ws.a, ws.a_sf);
 }
 
-cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int num_sms,
+cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int max_ctas,
                                 cudaStream_t s, bool pdl) {
-  (void)num_sms;
   const int64_t warps = (L.rows_alloc) * ((L.I / 128 + 1) / 2);
-  return launch_k(swiglu_quant_kernel, dim3(stream_grid(warps, 8)), dim3(256), 0, s, pdl, nullptr,
+  return launch_k(swiglu_quant_kernel, dim3(stream_grid(warps, 8, max_ctas)), dim3(256), 0, s, pdl,
+                  nullptr,
                   (const uint16_t*)ws.gu, (const int32_t*)ws.total_mtiles, L.I, ws.hq, ws.h_sf);
 }
 

@@ -76,6 +76,10 @@ class MegaMoELayer:
                       _stream_ptr(stream))
         return self.out[:T]
 
+    def set_sm_budget(self, max_sms: int) -> None:
+        """Cap the SMs the following forwards occupy (0: every SM)."""
+        B.moe_set_sm_budget(self.handle, max_sms)
+
     def read_status(self, stream=None):
         return B.moe_read_status(self.handle, _stream_ptr(stream))
 

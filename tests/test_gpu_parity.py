@@ -359,3 +359,29 @@ def test_token_permutation_and_pow2_weight_scaling(lib, orc):
     xt3, it3, wt3 = gh.to_device(x, idx, w * 2)
     dbl = layer.forward(xt3, it3, wt3).clone()
     assert torch.equal(dbl.float(), base.float() * 2)
+
+
+@pytest.mark.parametrize("gemm", ["single", "pair"])
+def test_sm_budget_bit_identical(lib, orc, gemm):
+    """moe_set_sm_budget changes only grid sizes: outputs are bit-identical for
+    every budget (each GEMM tile and each element is computed the same way)."""
+    import serving_route_gb300.binding as B
+    T, H, I, E, K = 513, 1024, 512, 8, 6
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=5)
+    layer, wo = layer_from_float(lib, orc, T, H, I, E, K, w1, w2, fuse=True, gemm=gemm)
+    xt, it, wt = gh.to_device(x, idx, w)
+    full = layer.forward(xt, it, wt).clone()
+    assert layer.read_status() == (0, 0)
+    for budget in (2, 3, 40, 151, 0):
+        layer.set_sm_budget(budget)
+        out = layer.forward(xt, it, wt).clone()
+        assert layer.read_status() == (0, 0), budget
+        assert torch.equal(out.view(torch.int16), full.view(torch.int16)), budget
+        ctas = layer.debug()["gemm_ctas"]
+        if budget:
+            assert ctas <= budget and (ctas % 2 == 0 or gemm == "single")
+    for bad in (-1, 1):
+        with pytest.raises(B.MoEError):
+            layer.set_sm_budget(bad)
+    ref = orc.forward(x, idx, w, *wo)
+    compare_outputs(layer.debug(), full, ref, check_routing(layer.debug(), ref, T, K))
