@@ -301,7 +301,7 @@ def main():
 
     if args.sm_budget:
         layer.set_sm_budget(args.sm_budget)
-    dbg = layer.debug()
+    dbg = layer.tactic()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
 
     def fwd():

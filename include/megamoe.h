@@ -193,10 +193,11 @@ typedef struct moe_debug_view {
   int32_t* perm;           /* [R] route id r = t*K + k at unpadded position pos */
   int32_t* inv;            /* [T*K] unpadded position of route r, or -1 */
   int32_t* inv_pad;        /* [T*K] padded GEMM row of route r, or -1 */
-  uint8_t* a;              /* [rows_alloc, H] E4M3 gathered activations (padded rows) */
+  uint8_t* a;              /* E4M3 gathered activations (padded rows), blocked: row r, column c at
+                              ((r/128)*(H/128) + c/128)*16384 + (r%128)*128 + c%128 */
   uint8_t* a_sf;           /* E8M0 scale atoms of a: [rows_alloc/128][ceil(H/512)][512] */
   uint16_t* gu;            /* [rows_alloc, 2I] BF16 gate||up (unfused or EMIT_FC1), else NULL */
-  uint8_t* hq;             /* [rows_alloc, I] E4M3 re-quantised SwiGLU output */
+  uint8_t* hq;             /* E4M3 re-quantised SwiGLU output, blocked like a (I columns) */
   uint8_t* h_sf;           /* E8M0 scale atoms of hq: [rows_alloc/128][ceil(I/512)][512] */
   uint16_t* y;             /* [rows_alloc, H] BF16 FC2 output per padded row */
   int64_t rows_alloc;      /* padded-row capacity (multiple of 128) */

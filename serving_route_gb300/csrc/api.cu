@@ -23,7 +23,7 @@ struct moe_handle {
   int64_t expected_m;
   Workspace ws;
   WeightStore wst;
-  CUtensorMap tm_a, tm_hq;                  // activations: 128-row boxes
+  CUtensorMap tm_a, tm_hq;                  // blocked activations: one 128x128 box per load
   CUtensorMap tm_w1, tm_w2;                 // blocked weights: one 128x128 box per load
   CUtensorMap tm_asf, tm_hsf;               // scale atoms as 2-D uint32 tensors (CTA pairs)
   CUtensorMap tm_w1sf, tm_w2sf;             // weight scale atoms, same form (CTA pairs)
@@ -64,20 +64,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }
   return fn;
-}
-
-// 2-D byte tensor [outer, inner], tile box [box_outer, 128], 128-byte swizzle.
-bool encode_u8_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                   uint32_t box_outer) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner};
-  cuuint32_t box[2] = {128, box_outer};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // BF16 matrix [rows, cols] for TMA stores of 32-row x 32-column boxes,
@@ -292,8 +278,8 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   h->wst.w2_sf = wb + L.o_w2_sf;
   h->wst.w1_sfatoms = wb + L.o_w1_sfatoms;
   h->wst.w2_sfatoms = wb + L.o_w2_sfatoms;
-  if (!encode_u8_map(&h->tm_a, w.a, L.H, L.rows_alloc, 128) ||
-      !encode_u8_map(&h->tm_hq, w.hq, L.I, L.rows_alloc, 128) ||
+  if (!encode_blocked_map(&h->tm_a, w.a, L.H / 128, (uint64_t)(L.rows_alloc / 128)) ||
+      !encode_blocked_map(&h->tm_hq, w.hq, L.I / 128, (uint64_t)(L.rows_alloc / 128)) ||
       !encode_atom_map(&h->tm_asf, w.a_sf, (uint64_t)(L.rows_alloc / 128) * sf_kgroups(L.H / 128)) ||
       !encode_atom_map(&h->tm_hsf, w.h_sf, (uint64_t)(L.rows_alloc / 128) * sf_kgroups(L.I / 128)) ||
       !encode_atom_map(&h->tm_w1sf, h->wst.w1_sfatoms,

@@ -42,6 +42,14 @@ __host__ __device__ __forceinline__ int64_t sf_atom_offset(int64_t row, int64_t 
          ((row & 127) >> 5) * 4 + (kblock & 3);
 }
 
+// Byte offset of (row, column) in a blocked E4M3 activation buffer: every
+// 128-row x 128-column block is one contiguous 16 KB box,
+// [rows / 128][cols / 128][128][128], so a GEMM stage's A box is one
+// sequential read.
+__host__ __device__ __forceinline__ int64_t blocked_offset(int64_t row, int64_t col, int64_t cols) {
+  return (((row >> 7) * (cols >> 7) + (col >> 7)) << 14) + ((row & 127) << 7) + (col & 127);
+}
+
 // Smallest e with amax <= 448 * 2^e, kept in [-127, 127]; amax == 0 gives 0.
 // amax = m * 2^E, m in [1, 2): e = E - 8 when m <= 1.75, else E - 7
 // (448 = 1.75 * 2^8).  Subnormal amax lies below every kept scale.

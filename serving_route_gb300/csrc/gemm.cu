@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader)
               mbar_arrive_expect_tx(smem_u32(&full_bar[stage]),
                                     2 * (C::kTxBytes + (atoms ? C::kTxAtomBytes : 0u)));
-            tma_load_2d_pair(sst + C::kOffA, &tmA, fb, kb * 128, mt * 128);
+            tma_load_3d_pair(sst + C::kOffA, &tmA, fb, 0, kb * 128, mt);
             tma_load_3d_pair(sst + C::kOffB, &tmB, fb, 0, kb * 128, rank ? wb1 : wb0);
             if (atoms) {
               tma_load_2d_pair(sst + C::kOffSfa, &tmSfa, fb, 0, (int)(sfa0 + q));
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             const uint32_t fb = smem_u32(&full_bar[stage]);
             mbar_arrive_expect_tx(fb, C::kTxBytes + (atoms ? C::kTxAtomBytes : 0u));
-            tma_load_2d(sst + C::kOffA, &tmA, fb, kb * 128, mt * 128);
+            tma_load_3d(sst + C::kOffA, &tmA, fb, 0, kb * 128, mt);
             tma_load_3d(sst + C::kOffB, &tmB, fb, 0, kb * 128, wb0);
             tma_load_3d(sst + C::kOffB + 16384, &tmB, fb, 0, kb * 128, wb1);
             if (atoms) {
@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         amax = fmaxf(amax, amax_sh[tile_par][half ^ 1][row_in_tile]);
         const int e = pow2_scale_exp(amax);
         const float inv = pow2_neg(e);
-        uint8_t* dq = g.hq + row * (int64_t)g.inter + (int64_t)nt * 128 + half * 64;
+        uint8_t* dq = g.hq + blocked_offset(row, (int64_t)nt * 128 + half * 64, g.inter);
 #pragma unroll
         for (int v = 0; v < 2; ++v) {
           uint32_t w[8];

@@ -24,10 +24,10 @@ struct Workspace {
   int32_t* perm;           // [max_rows*K]
   int32_t* inv;            // [max_rows*K]
   int32_t* inv_pad;        // [max_rows*K]
-  uint8_t* a;              // [rows_alloc, H]
+  uint8_t* a;              // blocked [rows_alloc/128][H/128][128][128]
   uint8_t* a_sf;           // atoms [rows_alloc/128][ceil(H/512)][512]
   uint16_t* gu;            // [rows_alloc, 2I] or nullptr
-  uint8_t* hq;             // [rows_alloc, I]
+  uint8_t* hq;             // blocked [rows_alloc/128][I/128][128][128]
   uint8_t* h_sf;           // atoms [rows_alloc/128][ceil(I/512)][512]
   uint16_t* y;             // [rows_alloc, H]
 };
@@ -96,7 +96,7 @@ struct GemmArgs {
   uint16_t* out;               // kModeY: y; kModeGU/kModeFusedGU: gu
   int64_t ld_out;              // elements per output row
   int inter;                   // I: column offset of the up half in gu
-  uint8_t* hq;                 // fused: [rows, I]
+  uint8_t* hq;                 // fused: blocked [rows/128][I/128][128][128]
   uint8_t* h_sf;               // fused: scale atoms [mblocks][I/128][512]
   int IB;                      // I / 128
   uint32_t* status;

@@ -85,7 +85,7 @@ __device__ __forceinline__ void quant_dispatch_unit(const uint4 (&raw)[2], bool 
   for (int k = 0; k < K; ++k) {
     const int p = __shfl_sync(0xFFFFFFFFu, p_lane, k);
     if (p >= 0 && valid) {
-      *reinterpret_cast<uint4*>(a + (int64_t)p * H + b * 128 + l8 * 16) = q;
+      *reinterpret_cast<uint4*>(a + blocked_offset(p, b * 128 + l8 * 16, H)) = q;
       if (l8 == 0) a_sf[sf_atom_offset(p, b, KB)] = (uint8_t)(e + 127);
     }
   }
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
     amax = half_warp_max(amax);
     const int e = pow2_scale_exp(amax);
     if (valid) {
-      *reinterpret_cast<uint2*>(hq + row * I + b * 128 + l16 * 8) = quant8(h, e);
+      *reinterpret_cast<uint2*>(hq + blocked_offset(row, b * 128 + l16 * 8, I)) = quant8(h, e);
       if (l16 == 0) h_sf[sf_atom_offset(row, b, IB)] = (uint8_t)(e + 127);
     }
   }

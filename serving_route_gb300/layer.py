@@ -93,8 +93,14 @@ class MegaMoELayer:
         B.moe_set_profile_events(self.handle, [e.cuda_event for e in events] if events else [])
 
     # -- introspection -------------------------------------------------------------
+    def tactic(self) -> dict:
+        """The GEMM tactic of this layer: CTA pairs or not, GEMM grid, segment padding."""
+        v = B.moe_debug_views(self.handle)
+        return dict(gemm_pair=bool(v.gemm_pair), gemm_ctas=int(v.gemm_ctas), pad_rows=int(v.pad_rows))
+
     def debug(self) -> dict:
-        """torch views of the internal buffers (slices of the workspace)."""
+        """torch views of the internal buffers (slices of the workspace); the
+        blocked E4M3 buffers a and hq come as row-major copies."""
         v = B.moe_debug_views(self.handle)
         base = self.workspace.data_ptr()
         R = v.rows_alloc
@@ -113,9 +119,9 @@ class MegaMoELayer:
             perm=view(v.perm, 4 * self.max_rows * K, torch.int32, (self.max_rows * K,)),
             inv=view(v.inv, 4 * self.max_rows * K, torch.int32, (self.max_rows * K,)),
             inv_pad=view(v.inv_pad, 4 * self.max_rows * K, torch.int32, (self.max_rows * K,)),
-            a=view(v.a, R * H, torch.uint8, (R, H)),
+            a=unblock(view(v.a, R * H, torch.uint8, (R * H,)), R, H),
             a_sf=view(v.a_sf, (R // 128) * kq(H) * 512, torch.uint8, (R // 128, kq(H), 512)),
-            hq=view(v.hq, R * I, torch.uint8, (R, I)),
+            hq=unblock(view(v.hq, R * I, torch.uint8, (R * I,)), R, I),
             h_sf=view(v.h_sf, (R // 128) * kq(I) * 512, torch.uint8, (R // 128, kq(I), 512)),
             y=view(v.y, R * H * 2, torch.bfloat16, (R, H)),
             rows_alloc=R,
@@ -137,6 +143,12 @@ class MegaMoELayer:
             self.close()
         except Exception:
             pass
+
+
+def unblock(flat: torch.Tensor, rows: int, cols: int) -> torch.Tensor:
+    """A blocked E4M3 buffer ([rows/128][cols/128][128][128], every 128x128 block
+    contiguous) as a row-major [rows, cols] copy."""
+    return flat.view(rows // 128, cols // 128, 128, 128).permute(0, 2, 1, 3).reshape(rows, cols)
 
 
 def kq(k: int) -> int:
