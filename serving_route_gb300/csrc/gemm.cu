@@ -6,10 +6,15 @@
 // GB300 design:
 //  * tcgen05.mma kind::mxf8f6f4 with block scales: both operands E4M3, one
 //    E8M0 scale per row per 32-wide K chunk.  Every scale of the layer is a
-//    power of two, so a 1x128 activation scale is four equal E8M0 bytes and a
-//    128x128 weight scale is one byte for 128 rows; the tensor core applies
-//    them exactly while it accumulates in FP32 in tensor memory.  No
-//    per-K-block promotion through registers is needed.
+//    power of two, so 1x128 activation and 128x128 weight scales are applied
+//    exactly by the tensor core while it accumulates in FP32 in tensor
+//    memory: no per-K-block promotion through registers.  A scale atom holds
+//    the bytes of four K blocks; the four MMAs of K block 4q + j select byte j
+//    (the descriptor's scale-factor ids), so one tcgen05.cp per operand
+//    serves four K blocks.
+//  * Operands come from blocked buffers (every 128x128 block one contiguous
+//    16 KB box: the weights from the bind step, A / hq from the quantisers),
+//    one 3-D TMA box per block, 128-byte swizzle.
 //  * Persistent CTAs walk a static tile list: 128 padded rows of one expert x
 //    256 output columns, expert-major, so the m-tiles sharing a weight tile
 //    run at the same time and hit it in L2.  The tile count and the m-tile ->
@@ -17,24 +22,28 @@
 //    graph-capturable.
 //  * Two variants (template PAIR):
 //    - single CTA: one CTA per SM, M128 x N256 per MMA; a 4-stage ring of
-//      48 KB stages (A 128x128 B, B 256x128 B, 128-byte swizzle).
+//      50 KB stages (A 128x128 B, B two 128x128 B blocks, scale atoms).
 //    - CTA pair (tcgen05 cta_group::2): two CTAs on the two SMs of a cluster
-//      compute M256 x N256; each stages its own 128 A rows and half of the
-//      256 B rows (32 KB per K block instead of 48 KB), so a 6-stage ring
-//      fits and more bytes are in flight per SM for the same MMA rate.  Both
-//      producers' TMA loads complete on the leader CTA's barrier, which only
-//      the leader arms (with both CTAs' bytes); the leader issues the scale
-//      copies and MMAs for the pair and multicasts its commits to both CTAs;
-//      each CTA drains its own 128 accumulator rows.  Expert segments are
-//      padded to 256 rows so a pair tile never straddles two experts.
-//  * Warp roles (320 threads): warp 0 producer (TMA only: operand tiles, the
-//    A scale atom, and the two B scale atoms taken from a 256-entry table of
-//    constant atoms indexed by the weight block's E8M0 byte), one thread of
-//    warp 1 issues the scale copies (tcgen05.cp) and MMAs, warps 2-9 the
-//    epilogue (two per TMEM lane quadrant).
-//  * Epilogues: FC2 -> BF16 y; FC1 unfused -> BF16 gate||up; FC1 fused ->
-//    BF16-rounded gate/up, SwiGLU, 1x128 re-quantisation to E4M3 + E8M0 atoms
-//    (bit-equal to the unfused path, which runs the same device functions).
+//      compute M256 x N256; each stages its own 128 A rows and one of the two
+//      128-row B blocks (32 KB per K block instead of 48 KB), so a 6-stage
+//      ring fits and more bytes are in flight per SM for the same MMA rate.
+//      Both producers' TMA loads complete on the leader CTA's barrier, which
+//      only the leader arms (with both CTAs' bytes); the leader issues the
+//      scale copies and MMAs for the pair and multicasts its commits to both
+//      CTAs; each CTA drains its own 128 accumulator rows.  Expert segments
+//      are padded to 256 rows so a pair tile never straddles two experts.
+//  * Warp roles (320 threads): warp 0 producer (TMA only: operand boxes, and
+//    every fourth K block the A scale atom and the two B scale atoms built at
+//    bind time), one thread of warp 1 issues the scale copies (tcgen05.cp)
+//    and MMAs and probes the next stage while the current one computes,
+//    warps 2-9 the epilogue (two per TMEM lane quadrant).
+//  * Epilogues: FC2 -> BF16 y (TMA stores); FC1 unfused -> BF16 gate||up;
+//    FC1 fused -> BF16-rounded gate/up, SwiGLU, 1x128 re-quantisation to E4M3
+//    + E8M0 atoms (bit-equal to the unfused path, which runs the same device
+//    functions).
+//  * Launched as a programmatic dependent: the barrier / TMEM prologue
+//    overlaps the previous kernel, the wait comes before the first global
+//    read.
 //  * Every wait is bounded (1 s); on expiry the kernel records
 //    MOE_DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include "common.cuh"

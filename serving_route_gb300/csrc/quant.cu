@@ -4,14 +4,16 @@
 //                   FP8 block scaling", flashinfer PR #4069, Limitations),
 //                   written straight into the padded, expert-sorted GEMM rows
 //                   of every active route of the token (the dispatch gather
-//                   fused into the quantiser: x is read once).
+//                   fused into the quantiser: x is read once), in the blocked
+//                   layout the GEMM loads (128x128 boxes).
 //   swiglu_quant    the unfused reference path after FC1: SwiGLU of the BF16
 //                   gate||up rows and 1x128 re-quantisation (flashinfer PR
 //                   #4069, Description: the unfused path is the maintained
 //                   reference, the fused epilogue must match it bit for bit).
-//   quantize_weights / bind_transform: setup-time weight preparation.
-// All of them are HBM-bound streaming kernels: 16-byte loads, one 128-column
-// block per half-warp, amax by shuffles, grids sized to the SM count.
+//   quantize_weights / bind_transform: setup-time weight preparation (the
+//                   blocked weight store and the GEMM scale atoms).
+// All of them are HBM-bound streaming kernels: 16-byte loads, amax by
+// shuffles, grids sized to the SM count.
 #include "common.cuh"
 #include "internal.h"
 
