@@ -90,12 +90,6 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
   return r;
 }
 
-// One CTA of 1024 threads.  The per-block histograms [nb][E] are split into
-// G = 1024 / E chunks of blocks per expert: thread (g, e) sums chunk g of
-// column e, the chunk sums give each expert's total and each chunk's prefix,
-// one block-wide scan over the experts gives the unpadded and padded
-// segment offsets, and every thread then writes the per-block bases of its
-// chunk.  The serial work per thread is ceil(nb / G) blocks instead of nb.
 __global__ void __launch_bounds__(1024) route_scan_kernel(
     const int32_t* __restrict__ block_counts, int nb, int E, int pad_rows, int64_t rows_alloc,
     int max_mtiles,
@@ -106,52 +100,27 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
   pdl_trigger();
   __shared__ int warp_sums[32];
   __shared__ int tot_u, tot_p;
-  __shared__ int part[1024];                 // [g][e] chunk sums
-  __shared__ int off_u_sh[1024], off_p_sh[1024];
-  const int t = threadIdx.x;
-  const int G = 1024 / E;                    // chunks per expert (E <= 1024)
-  const bool active = t < G * E;
-  const int e = active ? t % E : 0, g = active ? t / E : 0;
-  const int chunk = (nb + G - 1) / G;
-  const int b0 = g * chunk, b1 = min(nb, b0 + chunk);
-  int sum = 0;
-  if (active)
-    for (int b = b0; b < b1; ++b) sum += block_counts[(int64_t)b * E + e];
-  if (active) part[g * E + e] = sum;
-  __syncthreads();
-  // the expert's total (threads t < E) and this chunk's prefix
-  int c = 0, pre = 0;
-  if (active) {
-    for (int gg = 0; gg < G; ++gg) {
-      const int v = part[gg * E + e];
-      if (gg < g) pre += v;
-      c += v;
-    }
-  }
-  const bool lead = t < E;  // g == 0
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E)
+    for (int b = 0; b < nb; ++b) c += block_counts[(int64_t)b * E + e];
   const int cp = (c + pad_rows - 1) / pad_rows * pad_rows;  // GEMM segment of the expert
-  const int off_u = block_exclusive_scan(lead ? c : 0, warp_sums, &tot_u);
-  const int off_p = block_exclusive_scan(lead ? cp : 0, warp_sums, &tot_p);
-  if (lead) {
-    off_u_sh[e] = off_u;
-    off_p_sh[e] = off_p;
+  const int off_u = block_exclusive_scan(c, warp_sums, &tot_u);
+  const int off_p = block_exclusive_scan(cp, warp_sums, &tot_p);
+  if (e < E) {
     counts[e] = c;
     offsets[e] = off_u;
     pad_offsets[e] = off_p;
+    int run = 0;
+    for (int b = 0; b < nb; ++b) {
+      base_u[(int64_t)b * E + e] = off_u + run;
+      base_p[(int64_t)b * E + e] = off_p + run;
+      run += block_counts[(int64_t)b * E + e];
+    }
     const int m0 = off_p >> 7, m1 = (off_p + cp) >> 7;
     for (int m = m0; m < m1 && m < max_mtiles; ++m) mtile_expert[m] = e;
   }
-  __syncthreads();
-  if (active) {
-    const int bu = off_u_sh[e], bp = off_p_sh[e];
-    int run = pre;
-    for (int b = b0; b < b1; ++b) {
-      base_u[(int64_t)b * E + e] = bu + run;
-      base_p[(int64_t)b * E + e] = bp + run;
-      run += block_counts[(int64_t)b * E + e];
-    }
-  }
-  if (t == 0) {
+  if (e == 0) {
     offsets[E] = tot_u;
     pad_offsets[E] = tot_p;
     if ((int64_t)tot_p > rows_alloc) {
