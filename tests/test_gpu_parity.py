@@ -385,3 +385,34 @@ def test_sm_budget_bit_identical(lib, orc, gemm):
             layer.set_sm_budget(bad)
     ref = orc.forward(x, idx, w, *wo)
     compare_outputs(layer.debug(), full, ref, check_routing(layer.debug(), ref, T, K))
+
+
+def test_programmatic_launch_matches_serialised(lib, orc):
+    """Profiling events between the kernels turn the programmatic-dependent
+    launches back into plain stream order; the outputs are bit-identical."""
+    T, H, I, E, K = 300, 512, 256, 16, 4
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=9)
+    layer, wo = layer_from_float(lib, orc, T, H, I, E, K, w1, w2, fuse=True)
+    xt, it, wt = gh.to_device(x, idx, w)
+    chained = layer.forward(xt, it, wt).clone()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+    layer.set_profile_events(ev)
+    serial = layer.forward(xt, it, wt).clone()
+    layer.set_profile_events([])
+    assert layer.read_status() == (0, 0)
+    assert torch.equal(chained.view(torch.int16), serial.view(torch.int16))
+
+
+@pytest.mark.parametrize("expected_m,E,K,pair", [
+    (8192, 256, 8, True),    # 256 rows per expert: no padding either way, pairs
+    (4096, 64, 6, False),    # 384 rows: 512 with pairs against 384, one CTA per SM
+    (16384, 128, 8, True),   # 1024 rows
+    (8, 256, 8, False),      # decode: a fraction of a row
+])
+def test_automatic_tactic(lib, expected_m, E, K, pair):
+    layer = lib.MegaMoELayer(256, 256, E, K, max_rows=64, expected_m=expected_m)
+    t = layer.tactic()
+    if t["gemm_ctas"] and pair:
+        assert t["gemm_pair"] and t["pad_rows"] == 256 and t["gemm_ctas"] % 2 == 0
+    if not pair:
+        assert not t["gemm_pair"] and t["pad_rows"] == 128
