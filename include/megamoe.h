@@ -139,7 +139,9 @@ MOE_API moe_status moe_quantize_weights(const float* d_w, int64_t num_mats, int3
  * moe_bind_weights -- the layer holds its static weights in a transformed,
  * kernel-ready form that is built once, at set-up (flashinfer PR #4069,
  * "Contracts introduced by this PR": the stateful backend contract).  Copies
- * and transforms into the weight store:
+ * and transforms into the weight store (every 128x128 block of W1 and W2 one
+ * contiguous 16 KB box, W1's gate and up row blocks interleaved, and the
+ * scales as E8M0 plus the GEMM's scale atoms):
  *   d_w1        E4M3 [E, 2I, H]: rows [0, I) gate, rows [I, 2I) up.
  *   d_w1_scale  float [E, 2I/128, H/128], powers of two.
  *   d_w2        E4M3 [E, H, I].
@@ -171,7 +173,10 @@ MOE_API moe_status moe_stage_inputs(moe_handle* h, uint16_t* d_out);
  *   d_topk_w    float [num_tokens, K]; ignored (may be NaN) on masked slots.
  *   num_tokens  0..max_rows.  0 returns MOE_OK and writes nothing.
  * Writes d_out[0:num_tokens, :] of the staged output.  Route errors set the
- * device status word; the output is then undefined.
+ * device status word; the output is then undefined.  Enqueues a status reset
+ * and seven kernels; every kernel after the first is launched as a
+ * programmatic dependent of the one before (it may start while its
+ * predecessor drains and waits for it before touching the forward's data).
  */
 MOE_API moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk_idx,
                        const float* d_topk_w, int64_t num_tokens, struct CUstream_st* stream);
