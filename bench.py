@@ -499,6 +499,11 @@ def main():
     b_alg, touched = algorithmic_bytes(wl, counts)
     t_roof = max(flops / (fp8_peak * 1e12), b_alg / (hbm * 1e9))
     kern_ms = {k: v / K for k, v in per_kernel.items()}
+    route_k = layer.route_kernels(wl.T)
+    if route_k == 1:  # one cooperative routing kernel: its whole time is in the first span
+        kern_ms["route_fused"] = kern_ms.pop("route_count")
+        kern_ms.pop("route_scan")
+        kern_ms.pop("route_scatter")
     # dominant kernel: FC1 (fused epilogue), a dense FP8 contraction
     R = int(counts.sum())
     fc1_flops = 2 * R * wl.H * 2 * wl.I
@@ -526,6 +531,7 @@ def main():
                    "l2": "flushed before every step (256 MiB write, untimed)",
                    "launch": "cuda graph replay" if graph is not None else "direct launches",
                    "gemm": ("cta pairs" if dbg["gemm_pair"] else "single cta") + f" x{dbg['gemm_ctas']}",
+                   "routing": "one cooperative kernel" if route_k == 1 else "three kernels",
                    "sm_budget": args.sm_budget or None,
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": aggregate_rate(world, wl.T, K, total_ms),
@@ -538,7 +544,7 @@ def main():
         "kernel_ms_source": ("CUDA events before every kernel, a second capture of the same forward "
                              f"replayed for the same {K} steps right after the timed ones "
                              f"({prof_ms / K:.4f} ms per step with the events in place)"),
-        "gpu_launches": K * (7 if fused else 8),
+        "gpu_launches": K * (route_k + 4 + (0 if fused else 1)),
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / K,

@@ -174,9 +174,14 @@ MOE_API moe_status moe_stage_inputs(moe_handle* h, uint16_t* d_out);
  *   num_tokens  0..max_rows.  0 returns MOE_OK and writes nothing.
  * Writes d_out[0:num_tokens, :] of the staged output.  Route errors set the
  * device status word; the output is then undefined.  Enqueues a status reset
- * and seven kernels; every kernel after the first is launched as a
- * programmatic dependent of the one before (it may start while its
- * predecessor drains and waits for it before touching the forward's data).
+ * and five kernels (six with the unfused FC1 epilogue): the routing as one
+ * cooperative kernel (histogram, one grid-wide barrier, scan, stable scatter)
+ * when its ceil(num_tokens/512) blocks can all be resident and no SM budget
+ * is set, else as three kernels (histogram, scan, scatter) with the same
+ * results; then quant_dispatch, FC1, FC2 and combine.  Every kernel after the
+ * first is launched as a programmatic dependent of the one before (it may
+ * start while its predecessor drains and waits for it before touching the
+ * forward's data).
  */
 MOE_API moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk_idx,
                        const float* d_topk_w, int64_t num_tokens, struct CUstream_st* stream);
@@ -211,6 +216,9 @@ typedef struct moe_debug_view {
   int32_t gemm_pair;       /* 1: GEMMs run on CTA pairs (cta_group::2), 0: one CTA per SM */
   int32_t gemm_ctas;       /* grid size of the GEMM launches */
   int32_t pad_rows;        /* rows each expert's GEMM segment is padded to */
+  int32_t route_coop_blocks; /* forwards with ceil(num_tokens/512) <= this route in one cooperative
+                                kernel (512 tokens per block), others in three (0: always three,
+                                e.g. under an SM budget) */
 } moe_debug_view;
 
 MOE_API moe_status moe_debug_views(moe_handle* h, moe_debug_view* out);
@@ -221,8 +229,9 @@ MOE_API moe_status moe_debug_views(moe_handle* h, moe_debug_view* out);
  * caller) before its i-th kernel and events[n-1] after the last one, on the
  * forward's stream.  Kernel order: 0 status reset, 1 route_count,
  * 2 route_scan, 3 route_scatter, 4 quant_dispatch, 5 fc1, 6 swiglu_quant
- * (skipped when fused), 7 fc2, 8 combine, 9 end.  n must be 0 (profiling off)
- * or 10, with every handle non-NULL.
+ * (skipped when fused), 7 fc2, 8 combine, 9 end.  When the routing runs as
+ * one kernel, span 1 times all of it and spans 2 and 3 are empty.  n must be
+ * 0 (profiling off) or 10, with every handle non-NULL.
  */
 MOE_API moe_status moe_set_profile_events(moe_handle* h, void* const* events, int32_t n);
 

@@ -60,7 +60,7 @@ class moe_debug_view(ctypes.Structure):
                 ("hq", ctypes.c_void_p), ("h_sf", ctypes.c_void_p), ("y", ctypes.c_void_p),
                 ("rows_alloc", ctypes.c_int64), ("sf_atom_bytes", ctypes.c_int32),
                 ("gemm_pair", ctypes.c_int32), ("gemm_ctas", ctypes.c_int32),
-                ("pad_rows", ctypes.c_int32)]
+                ("pad_rows", ctypes.c_int32), ("route_coop_blocks", ctypes.c_int32)]
 
 
 class MoEError(RuntimeError):

@@ -30,6 +30,7 @@ struct moe_handle {
   CUtensorMap tm_y;                         // FC2 output, 32x32 BF16 boxes (TMA stores)
   int pair_ctas;                            // grid of the CTA-pair GEMMs
   int sm_budget;                            // moe_set_sm_budget (0: every SM)
+  int route_coop_blocks;                    // co-resident grid limit of the one-kernel routing
   bool bound;
   uint16_t* out;
   int num_sms;
@@ -178,7 +179,7 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
     o = align_up(o + bytes, kAlign);
     return at;
   };
-  L->o_status = take(1024);  // status word at +0, total_mtiles at +4
+  L->o_status = take(1024);  // status word at +0, total_mtiles at +4, routing arrival counter at +8
   L->o_counts = take(4 * E);
   L->o_offsets = take(4 * (E + 1));
   L->o_pad_offsets = take(4 * (E + 1));
@@ -249,11 +250,13 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   h->L = L;
   h->expected_m = expected_m;
   h->num_sms = sms;
+  h->route_coop_blocks = route_fused_max_blocks(L.E);
   h->device = dev;
   uint8_t* b = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(d_workspace), kAlign));
   Workspace& w = h->ws;
   w.status = reinterpret_cast<uint32_t*>(b + L.o_status);
   w.total_mtiles = reinterpret_cast<int32_t*>(b + L.o_status + 4);
+  w.grid_sync = reinterpret_cast<uint32_t*>(b + L.o_status + 8);
   w.counts = reinterpret_cast<int32_t*>(b + L.o_counts);
   w.offsets = reinterpret_cast<int32_t*>(b + L.o_offsets);
   w.pad_offsets = reinterpret_cast<int32_t*>(b + L.o_pad_offsets);
@@ -360,9 +363,13 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   const bool check = (h->dims.flags & MOE_FLAG_CHECK_ROUTES) != 0;
 
   if (ev) record_event(ev[0], s);
-  cudaMemsetAsync(ws.status, 0, 4, s);
-  if (launch_route(ws, L, d_topk_idx, d_topk_w, num_tokens, check, s, ev ? ev + 1 : nullptr) !=
-      cudaSuccess)
+  // status word, total_mtiles and the routing kernel's arrival counter
+  cudaMemsetAsync(ws.status, 0, 12, s);
+  // Under an SM budget the routing keeps to its three small kernels: a
+  // cooperative grid would have to be resident beside the side-stream work.
+  const int coop = h->sm_budget > 0 ? 0 : h->route_coop_blocks;
+  if (launch_route(ws, L, d_topk_idx, d_topk_w, num_tokens, check, s, ev ? ev + 1 : nullptr,
+                   coop) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[4], s);
   // Kernels after the first are programmatic dependents of their predecessor
@@ -468,6 +475,7 @@ moe_status moe_debug_views(moe_handle* h, moe_debug_view* v) {
   v->gemm_pair = h->L.pair ? 1 : 0;
   v->gemm_ctas = gemm_grid(h);
   v->pad_rows = h->L.pad_rows;
+  v->route_coop_blocks = h->sm_budget > 0 ? 0 : h->route_coop_blocks;
   return MOE_OK;
 }
 

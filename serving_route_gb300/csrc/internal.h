@@ -14,6 +14,7 @@ namespace mm {
 struct Workspace {
   uint32_t* status;        // device status word (MOE_DEV_* bits)
   int32_t* total_mtiles;   // number of 128-row GEMM tiles of this forward
+  uint32_t* grid_sync;     // arrival counter of the one-kernel routing (zeroed before each forward)
   int32_t* counts;         // [E]
   int32_t* offsets;        // [E+1]
   int32_t* pad_offsets;    // [E+1]
@@ -63,9 +64,16 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
                           float capacity_factor, Layout* L);
 
 // route.cu
+// One cooperative kernel (count, grid barrier, scan, scatter) when its
+// ceil(T/512) blocks can all be resident (coop_max_blocks: the device's limit
+// for the fused kernel, 0 = never) and ws.grid_sync is zero; otherwise the
+// three kernels route_count / route_scan / route_scatter.  Same outputs.
 cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* topk_idx,
                          const float* topk_w, int64_t T, bool check, cudaStream_t s,
-                         cudaEvent_t const* ev);
+                         cudaEvent_t const* ev, int coop_max_blocks);
+// Largest grid of the one-kernel routing that is co-resident on the current
+// device for E experts (0 if cooperative launch is unavailable).
+int route_fused_max_blocks(int E);
 
 // quant.cu
 // pdl: launch as a programmatic dependent of the previous kernel on `s`;

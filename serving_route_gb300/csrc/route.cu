@@ -196,19 +196,275 @@ __global__ void __launch_bounds__(kRouteTokens) route_scatter_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// One-kernel routing: the three steps above in one cooperative launch, with a
+// grid-wide barrier where the kernel boundaries were.  The outputs are the
+// same bit for bit: the same per-warp counting, scans and rank rule.
+//   phase 1  validate this block's tokens and count their routes per warp
+//            and expert; publish the block's histogram row
+//   barrier  every block arrives on a counter zeroed before the forward; the
+//            launch is cooperative (all blocks resident), and the wait is
+//            bounded all the same
+//   phase 2  every block reads the whole [nb][E] histogram: expert totals,
+//            its own prefix over earlier blocks, the unpadded and padded
+//            exclusive scans; the expert-level outputs (counts, offsets,
+//            m-tile table) are spread over the blocks
+//   phase 3  the stable scatter of route_scatter, bases from shared memory
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// 512 tokens per block (a warp per 32 tokens, as in route_scatter): four
+// times fewer histogram rows than the 128-token blocks of the three-kernel
+// form, and four times the threads to read them after the barrier.
+constexpr int kFusedTokens = 512;
+constexpr int kRouteWarps = kFusedTokens / 32;
+
+inline size_t route_fused_smem(int E) { return sizeof(int32_t) * (size_t)(kRouteWarps + 2) * E; }
+
+__global__ void __launch_bounds__(kFusedTokens) route_fused_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ w, int T, int K, int E, int check,
+    int pad_rows, int64_t rows_alloc, int max_mtiles, int32_t* __restrict__ block_counts,
+    uint32_t* __restrict__ grid_sync, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ pad_offsets, int32_t* __restrict__ mtile_expert,
+    int32_t* __restrict__ total_mtiles, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+    int32_t* __restrict__ inv_pad, uint32_t* __restrict__ status, uint64_t wait_limit_ns) {
+  extern __shared__ int32_t sm[];
+  int32_t* wh = sm;                   // [warps][E]: per-warp counts, then running bases
+  int32_t* bu = sm + kRouteWarps * E;  // [E]: expert totals, then this block's unpadded bases
+  int32_t* bp = bu + E;               // [E]: this block's prefix, then its padded bases
+  __shared__ int warp_sums[32];
+  __shared__ int tot_u, tot_p, passed;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb = (int)gridDim.x, b = (int)blockIdx.x;
+  for (int i = tid; i < kRouteWarps * E; i += blockDim.x) wh[i] = 0;
+  __syncthreads();
+
+  // ---- phase 1
+  const int t = b * kFusedTokens + tid;
+  uint32_t err = 0;
+  if (t < T) {
+    int ids[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ids[k] = (k < K) ? idx[(int64_t)t * K + k] : -1;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k >= K) break;
+      const int id = ids[k];
+      if (id == -1) continue;
+      if (id < 0 || id >= E) {
+        err |= MOE_DEV_ROUTE_RANGE;
+        continue;
+      }
+      atomicAdd(&wh[warp * E + id], 1);
+      if (check) {
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2)
+          if (k2 < k && ids[k2] == id) err |= MOE_DEV_ROUTE_DUP;
+        const float wv = w[(int64_t)t * K + k];
+        if (!isfinite(wv)) err |= MOE_DEV_ROUTE_NONFINITE;
+      }
+    }
+  }
+  if (err) record_status(status, err);
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int v = 0; v < kRouteWarps; ++v) c += wh[v * E + e];
+    block_counts[(int64_t)b * E + e] = c;
+  }
+
+  // ---- grid barrier
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();  // this block's histogram row before its arrival
+    atomicAdd(grid_sync, 1u);
+    bool ok = true;
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(grid_sync) < (uint32_t)nb) {
+      if (globaltimer_ns() - t0 > wait_limit_ns) {
+        ok = false;
+        break;
+      }
+    }
+    if (!ok) record_status(status, MOE_DEV_TIMEOUT);
+    __threadfence();
+    passed = ok ? 1 : 0;
+  }
+  __syncthreads();
+  pdl_trigger();  // quant_dispatch may launch; it waits for this grid to complete
+  if (!passed) {
+    // No routing this forward (the status says why): this block's routes are
+    // marked unrouted, so every later kernel skips them; total_mtiles keeps
+    // the 0 written before the forward unless block 0 got through.
+    const int64_t r0 = (int64_t)b * kFusedTokens * K;
+    const int64_t r1 = min((int64_t)T, (int64_t)(b + 1) * kFusedTokens) * K;
+    for (int64_t r = r0 + tid; r < r1; r += blockDim.x) {
+      inv[r] = -1;
+      inv_pad[r] = -1;
+    }
+    return;
+  }
+
+  // ---- phase 2
+  // expert totals and this block's prefix over the earlier blocks: the
+  // (block, expert) entries spread over the threads, eight loads in flight
+  // per thread, summed with shared-memory atomics
+  for (int e = tid; e < E; e += blockDim.x) {
+    bu[e] = 0;
+    bp[e] = 0;
+  }
+  __syncthreads();
+  const int n_ent = nb * E;
+  for (int p0 = tid; p0 < n_ent; p0 += 8 * kFusedTokens) {
+    int c[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int p = p0 + j * kFusedTokens;
+      c[j] = p < n_ent ? __ldcg(block_counts + p) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int p = p0 + j * kFusedTokens;
+      if (c[j] != 0) {
+        const int v = p / E, e = p - v * E;
+        atomicAdd(&bu[e], c[j]);
+        if (v < b) atomicAdd(&bp[e], c[j]);
+      }
+    }
+  }
+  __syncthreads();
+  // thread tid scans the run of experts [e0, e1)
+  const int per = (E + kFusedTokens - 1) / kFusedTokens;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int su = 0, sp = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int c = bu[e];
+    su += c;
+    sp += (c + pad_rows - 1) / pad_rows * pad_rows;
+  }
+  int run_u = block_exclusive_scan(su, warp_sums, &tot_u);
+  int run_p = block_exclusive_scan(sp, warp_sums, &tot_p);
+  for (int e = e0; e < e1; ++e) {
+    const int c = bu[e], cp = (c + pad_rows - 1) / pad_rows * pad_rows, pre = bp[e];
+    if (e % nb == b) {
+      counts[e] = c;
+      offsets[e] = run_u;
+      pad_offsets[e] = run_p;
+      const int m0 = run_p >> 7, m1 = (run_p + cp) >> 7;
+      for (int m = m0; m < m1 && m < max_mtiles; ++m) mtile_expert[m] = e;
+    }
+    bu[e] = run_u + pre;
+    bp[e] = run_p + pre;
+    run_u += c;
+    run_p += cp;
+  }
+  if (b == 0 && tid == 0) {
+    offsets[E] = tot_u;
+    pad_offsets[E] = tot_p;
+    if ((int64_t)tot_p > rows_alloc) {
+      record_status(status, MOE_DEV_CAPACITY);
+      *total_mtiles = 0;
+    } else {
+      *total_mtiles = tot_p >> 7;
+    }
+  }
+  // per-warp exclusive prefix of this block's counts, per expert
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = 0;
+#pragma unroll
+    for (int v = 0; v < kRouteWarps; ++v) {
+      const int c = wh[v * E + e];
+      wh[v * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 3 (as route_scatter)
+  int32_t* my = wh + warp * E;
+  const int64_t t0 = (int64_t)b * kFusedTokens + warp * 32;
+  const int64_t r0 = t0 * K;
+  const int64_t r1 = min((int64_t)T, t0 + 32) * K;
+  for (int64_t rb = r0; rb < r1; rb += 32) {
+    const int64_t r = rb + lane;
+    const bool in = r < r1;
+    const int id = in ? idx[r] : -1;
+    const bool act = in && id >= 0 && id < E;
+    const unsigned amask = __ballot_sync(0xFFFFFFFFu, act);
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, act ? id : -1) & amask;
+    int rank = 0, base = 0;
+    if (act) {
+      rank = __popc(peers & ((1u << lane) - 1u));
+      base = my[id];
+    }
+    __syncwarp();
+    if (act) {
+      const int local = base + rank;
+      const int pos = bu[id] + local;
+      const int64_t ppos = (int64_t)bp[id] + local;
+      perm[pos] = (int32_t)r;
+      inv[r] = pos;
+      inv_pad[r] = (ppos < rows_alloc) ? (int32_t)ppos : -1;
+      if ((peers >> lane) == 1u) my[id] = base + __popc(peers);
+    } else if (in) {
+      inv[r] = -1;
+      inv_pad[r] = -1;
+    }
+    __syncwarp();
+  }
+}
+
+int route_fused_max_blocks(int E) {
+  int dev = 0, coop = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop)
+    return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  // up to 72 KB of dynamic shared memory (E = 1024)
+  if (cudaFuncSetAttribute(route_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)route_fused_smem(1024)) != cudaSuccess)
+    return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_fused_kernel, kFusedTokens,
+                                                    route_fused_smem(E)) != cudaSuccess)
+    return 0;
+  return per_sm * sms;
+}
+
 cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* topk_idx,
                          const float* topk_w, int64_t T, bool check, cudaStream_t s,
-                         cudaEvent_t const* ev) {
+                         cudaEvent_t const* ev, int coop_max_blocks) {
   const int nb = (int)((T + kRouteTokens - 1) / kRouteTokens);
   const int E = L.E;
   const int max_mtiles = (int)(L.rows_alloc / 128);
+  const int pad_rows = L.pad_rows > 0 ? L.pad_rows : 128;
+  const int nb_fused = (int)((T + kFusedTokens - 1) / kFusedTokens);
+  if (ws.grid_sync && coop_max_blocks > 0 && nb_fused <= coop_max_blocks) {
+    if (ev) record_event(ev[0], s);
+    cudaLaunchAttribute coop;
+    coop.id = cudaLaunchAttributeCooperative;
+    coop.val.cooperative = 1;
+    const cudaError_t err = launch_k(
+        route_fused_kernel, dim3(nb_fused), dim3(kFusedTokens), route_fused_smem(E), s, false, &coop,
+        topk_idx, topk_w, (int)T, L.K, E, check ? 1 : 0, pad_rows, L.rows_alloc, max_mtiles,
+        ws.block_counts, ws.grid_sync, ws.counts, ws.offsets, ws.pad_offsets, ws.mtile_expert,
+        ws.total_mtiles, ws.perm, ws.inv, ws.inv_pad, ws.status, (uint64_t)kWaitLimitNs);
+    if (ev) {  // the scan and scatter are inside the one kernel: zero-length spans
+      record_event(ev[1], s);
+      record_event(ev[2], s);
+    }
+    return err;
+  }
   if (ev) record_event(ev[0], s);
   cudaError_t err = launch_k(route_count_kernel, dim3(nb), dim3(kRouteTokens), sizeof(int32_t) * E, s,
                              false, nullptr, topk_idx, topk_w, (int)T, L.K, E, check ? 1 : 0,
                              ws.block_counts, ws.status);
   if (err != cudaSuccess) return err;
   if (ev) record_event(ev[1], s);
-  const int pad_rows = L.pad_rows > 0 ? L.pad_rows : 128;
   err = launch_k(route_scan_kernel, dim3(1), dim3(1024), 0, s, ev == nullptr, nullptr,
                  (const int32_t*)ws.block_counts, nb, E, pad_rows, L.rows_alloc, max_mtiles, ws.counts,
                  ws.offsets, ws.pad_offsets, ws.base_u, ws.base_p, ws.mtile_expert, ws.total_mtiles,

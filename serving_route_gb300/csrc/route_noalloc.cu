@@ -111,8 +111,10 @@ extern "C" moe_status moe_route_noalloc(const int32_t* d_topk_idx, const float* 
   // written earlier in the same call.  The caller's status word is cleared
   // here because the kernels OR error bits into it.
   if (cudaMemsetAsync(d_status, 0, sizeof(uint32_t), stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_route(ws, L, d_topk_idx, d_topk_w, num_tokens, check_routes != 0, stream, nullptr) !=
-      cudaSuccess)
+  // the three-kernel routing: the cooperative one-kernel form would need a
+  // zeroed arrival counter in the scratch
+  if (launch_route(ws, L, d_topk_idx, d_topk_w, num_tokens, check_routes != 0, stream, nullptr,
+                   0) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -94,9 +94,16 @@ class MegaMoELayer:
 
     # -- introspection -------------------------------------------------------------
     def tactic(self) -> dict:
-        """The GEMM tactic of this layer: CTA pairs or not, GEMM grid, segment padding."""
+        """The tactic of this layer: CTA pairs or not, GEMM grid, segment padding,
+        and the largest ceil(T/512) routed by one cooperative kernel (0: never)."""
         v = B.moe_debug_views(self.handle)
-        return dict(gemm_pair=bool(v.gemm_pair), gemm_ctas=int(v.gemm_ctas), pad_rows=int(v.pad_rows))
+        return dict(gemm_pair=bool(v.gemm_pair), gemm_ctas=int(v.gemm_ctas), pad_rows=int(v.pad_rows),
+                    route_coop_blocks=int(v.route_coop_blocks))
+
+    def route_kernels(self, num_tokens: int) -> int:
+        """Kernels the routing step launches for a forward of num_tokens tokens (1 or 3)."""
+        lim = self.tactic()["route_coop_blocks"]
+        return 1 if 0 < (num_tokens + 511) // 512 <= lim else 3
 
     def debug(self) -> dict:
         """torch views of the internal buffers (slices of the workspace); the

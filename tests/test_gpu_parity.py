@@ -260,12 +260,17 @@ def test_route_errors_set_status(lib, orc):
     bad = idx.copy(); bad[4, 0] = -7; cases.append((bad, w, B.MOE_DEV_ROUTE_RANGE))
     bad = idx.copy(); bad[5, 1] = bad[5, 0]; cases.append((bad, w, B.MOE_DEV_ROUTE_DUP))
     wb = w.copy(); wb[6, 1] = np.inf; cases.append((idx, wb, B.MOE_DEV_ROUTE_NONFINITE))
-    for bi, bw, bit in cases:
-        xt, it, wt = gh.to_device(x, bi, bw)
-        layer.forward(xt, it, wt)
-        st, bits = layer.read_status()
-        assert st == B.MOE_ERR_BAD_ROUTE and bits == bit, (st, bits, bit)
-        assert orc.route(bi, bw, E)["err"] == bit
+    # one routing kernel, then the three-kernel form (under an SM budget)
+    for budget in (0, 4):
+        layer.set_sm_budget(budget)
+        assert layer.route_kernels(T) == (3 if budget else 1)
+        for bi, bw, bit in cases:
+            xt, it, wt = gh.to_device(x, bi, bw)
+            layer.forward(xt, it, wt)
+            st, bits = layer.read_status()
+            assert st == B.MOE_ERR_BAD_ROUTE and bits == bit, (budget, st, bits, bit)
+            assert orc.route(bi, bw, E)["err"] == bit
+    layer.set_sm_budget(0)
     # a clean forward clears the word again
     xt, it, wt = gh.to_device(x, idx, w)
     layer.forward(xt, it, wt)
@@ -385,6 +390,44 @@ def test_sm_budget_bit_identical(lib, orc, gemm):
             layer.set_sm_budget(bad)
     ref = orc.forward(x, idx, w, *wo)
     compare_outputs(layer.debug(), full, ref, check_routing(layer.debug(), ref, T, K))
+
+
+@pytest.mark.parametrize("T,H,E,K,mask", [
+    (1, 256, 4, 2, 0.0),         # one token: a grid of one block
+    (700, 256, 64, 6, 0.1),      # two 512-token blocks, ragged tail, masked slots
+    (4096, 256, 64, 6, 0.0),     # the dsv2lite routing: 8 blocks (32 in the three-kernel form)
+    (80000, 128, 256, 8, 0.05),  # 157 blocks, more than the SMs
+    (3000, 128, 1024, 8, 0.0),   # E at its limit: 72 KB of shared memory per block
+])
+def test_one_kernel_routing_matches_three_kernels(lib, orc, T, H, E, K, mask):
+    """The cooperative one-kernel routing (the default) and the three-kernel
+    routing (taken under an SM budget) give the same tables bit for bit, equal
+    to the oracle's, and the same layer output."""
+    I = 128
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=21, mask=mask)
+    layer, _ = layer_from_float(lib, orc, T, H, I, E, K, w1, w2)
+    assert layer.route_kernels(T) == 1
+    xt, it, wt = gh.to_device(x, idx, w)
+    keys = ("counts", "offsets", "pad_offsets", "perm", "inv", "inv_pad")
+    one = layer.forward(xt, it, wt).clone()
+    assert layer.read_status() == (0, 0)
+    d1 = {k: layer.debug()[k].clone() for k in keys}
+    layer.set_sm_budget(64)
+    assert layer.route_kernels(T) == 3
+    three = layer.forward(xt, it, wt).clone()
+    assert layer.read_status() == (0, 0)
+    d3 = layer.debug()
+    R = int(d1["offsets"][-1])
+    n = {"perm": R, "inv": T * K, "inv_pad": T * K}
+    for k in keys:
+        a, b = d1[k][:n.get(k, d1[k].numel())], d3[k][:n.get(k, d3[k].numel())]
+        assert torch.equal(a, b), k
+    assert torch.equal(one.view(torch.int16), three.view(torch.int16))
+    ref = orc.route(idx, w, E)
+    assert np.array_equal(d1["counts"].cpu().numpy(), ref["counts"])
+    assert np.array_equal(d1["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(d1["perm"][:R].cpu().numpy(), ref["perm"])
+    assert np.array_equal(d1["inv"][:T * K].cpu().numpy(), ref["inv"])
 
 
 def test_programmatic_launch_matches_serialised(lib, orc):
