@@ -53,6 +53,8 @@ def parse():
                    help="profiling only: the workload with this many experts (smaller weights)")
     p.add_argument("--tokens", type=int, default=0,
                    help="profiling only: the workload with this many tokens")
+    p.add_argument("--gemms", default="auto", choices=["auto", "one_launch", "split"],
+                   help="FC1 -> FC2 as one persistent launch, two launches, or chosen per forward")
     p.add_argument("--sm-budget", type=int, default=0,
                    help="cap the SMs the layer occupies (moe_set_sm_budget; 0: every SM)")
     p.add_argument("--no-graph", action="store_true")
@@ -266,7 +268,8 @@ def main():
     fused = not args.unfused
 
     layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, expected_m=wl.T,
-                           fuse_fc1=fused, check_routes=True, gemm=args.gemm)
+                           fuse_fc1=fused, check_routes=True, gemm=args.gemm,
+                           gemms=args.gemms)
     # weights: generated and quantised on the GPU, bound once
     w1q = torch.empty((wl.E, 2 * wl.I, wl.H), dtype=torch.uint8, device=dev)
     w1s = torch.empty((wl.E, 2 * wl.I // 128, wl.H // 128), dtype=torch.float32, device=dev)
@@ -499,7 +502,9 @@ def main():
     b_alg, touched = algorithmic_bytes(wl, counts)
     t_roof = max(flops / (fp8_peak * 1e12), b_alg / (hbm * 1e9))
     kern_ms = {k: v / K for k, v in per_kernel.items()}
-    route_k = layer.route_kernels(wl.T)
+    plan = layer.plan(wl.T)
+    route_k = plan["route_kernels"]
+    mega = plan["gemm_launches"] == 1
     if route_k == 1:  # one cooperative routing kernel: its whole time is in the first span
         kern_ms["route_fused"] = kern_ms.pop("route_count")
         kern_ms.pop("route_scan")
@@ -532,6 +537,7 @@ def main():
                    "launch": "cuda graph replay" if graph is not None else "direct launches",
                    "gemm": ("cta pairs" if dbg["gemm_pair"] else "single cta") + f" x{dbg['gemm_ctas']}",
                    "routing": "one cooperative kernel" if route_k == 1 else "three kernels",
+                   "gemms": ("FC1 + FC2 in one persistent launch" if mega else "two launches"),
                    "sm_budget": args.sm_budget or None,
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": aggregate_rate(world, wl.T, K, total_ms),
@@ -543,8 +549,9 @@ def main():
         "kernel_ms": kern_ms,
         "kernel_ms_source": ("CUDA events before every kernel, a second capture of the same forward "
                              f"replayed for the same {K} steps right after the timed ones "
-                             f"({prof_ms / K:.4f} ms per step with the events in place)"),
-        "gpu_launches": K * (route_k + 4 + (0 if fused else 1)),
+                             f"({prof_ms / K:.4f} ms per step with the events in place; FC1 and FC2 "
+                             "run there as two launches of the same GEMM code)"),
+        "gpu_launches": K * plan["kernels"],
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / K,

@@ -82,6 +82,20 @@ typedef enum moe_status {
  * the kernel winds down (drains its copies, frees tensor memory) and the
  * context stays usable.  Single-CTA GEMM tactic only. */
 #define MOE_FLAG_WATCHDOG_TEST 0x20u
+/* FC1 -> FC2 in one launch.  With the fused FC1 epilogue both GEMMs can run
+ * as one persistent launch (the megakernel): every FC1 tile, then every FC2
+ * tile, an FC2 tile loading its hq rows once all FC1 tiles of its 128-row
+ * m-tile have published them (a per-m-tile counter with a bounded wait;
+ * flashinfer PR #4069, the fused FC1 -> FC2 kernel with fc1_done flags), so
+ * FC2 tiles fill FC1's last wave and FC2 needs no ramp of its own.  That
+ * gains about one tile round per forward and costs ~1% on long forwards, so
+ * by default a forward uses one launch when its estimated tile rounds (FC1 +
+ * FC2 tiles over the GEMM grid, from num_tokens, E, top_k and the tactic) are
+ * at most 48, else two.  MOE_FLAG_GEMMS_ONE_LAUNCH / MOE_FLAG_SPLIT_GEMMS
+ * force one or the other (not both).  Results are bit-identical either way.
+ * Forwards with profiling events (moe_set_profile_events) always use two. */
+#define MOE_FLAG_SPLIT_GEMMS 0x40u
+#define MOE_FLAG_GEMMS_ONE_LAUNCH 0x80u
 
 typedef struct moe_dims {
   int32_t hidden;      /* H: multiple of 128, 128..16384 */
@@ -118,6 +132,13 @@ MOE_API moe_status moe_workspace_query(const moe_dims* dims, int64_t expected_m,
  * moe_create -- binds dims and caller-owned device regions; creates no CUDA
  * stream and allocates no device memory.  Sets kernel attributes, so call it
  * before any stream capture.  *out receives a host handle.
+ * Workspace pooling: a forward leaves nothing in the workspace that a later
+ * forward reads, so several handles (the layers of a model, with equal or
+ * different dims) may share one workspace of the largest size any of them
+ * queried, as long as their forwards never overlap on the GPU (one stream, or
+ * ordered by events).  The status word then belongs to the latest forward of
+ * any of them: read it (moe_read_status) before another handle's forward.
+ * The weight store and the staged output stay per handle.
  */
 MOE_API moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows,
                       float capacity_factor, void* d_workspace, size_t workspace_bytes,
@@ -174,14 +195,15 @@ MOE_API moe_status moe_stage_inputs(moe_handle* h, uint16_t* d_out);
  *   num_tokens  0..max_rows.  0 returns MOE_OK and writes nothing.
  * Writes d_out[0:num_tokens, :] of the staged output.  Route errors set the
  * device status word; the output is then undefined.  Enqueues a status reset
- * and five kernels (six with the unfused FC1 epilogue): the routing as one
+ * and four to eight kernels (moe_forward_plan says which): the routing as one
  * cooperative kernel (histogram, one grid-wide barrier, scan, stable scatter)
  * when its ceil(num_tokens/512) blocks can all be resident and no SM budget
  * is set, else as three kernels (histogram, scan, scatter) with the same
- * results; then quant_dispatch, FC1, FC2 and combine.  Every kernel after the
- * first is launched as a programmatic dependent of the one before (it may
- * start while its predecessor drains and waits for it before touching the
- * forward's data).
+ * results; quant_dispatch; FC1 and FC2 as one persistent launch or two (see
+ * MOE_FLAG_GEMMS_ONE_LAUNCH), with swiglu_quant between them on the unfused
+ * path; combine.  Every kernel after the first is launched as a programmatic
+ * dependent of the one before (it may start while its predecessor drains and
+ * waits for it before touching the forward's data).
  */
 MOE_API moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk_idx,
                        const float* d_topk_w, int64_t num_tokens, struct CUstream_st* stream);
@@ -248,6 +270,23 @@ MOE_API moe_status moe_set_profile_events(moe_handle* h, void* const* events, in
  * MOE_ERR_INVALID_ARG for a NULL handle or max_sms < 0 or == 1.
  */
 MOE_API moe_status moe_set_sm_budget(moe_handle* h, int32_t max_sms);
+
+/*
+ * moe_forward_plan -- the kernels moe_forward enqueues for num_tokens tokens
+ * with the handle's current flags and SM budget, without profiling events
+ * (the routing form, one or two GEMM launches: see MOE_FLAG_GEMMS_ONE_LAUNCH).
+ * Pure host arithmetic, no CUDA call; the same function the forward uses.
+ * num_tokens 0 gives all zeros.  MOE_ERR_INVALID_ARG for a NULL argument or
+ * num_tokens < 0.
+ */
+typedef struct moe_plan {
+  int32_t route_kernels;  /* 1 (one cooperative kernel) or 3 */
+  int32_t gemm_launches;  /* 1 (FC1 -> FC2 in one persistent launch) or 2 */
+  int32_t swiglu_kernels; /* 1 on the unfused path, else 0 */
+  int32_t kernels;        /* all of them: + quant_dispatch + combine */
+} moe_plan;
+
+MOE_API moe_status moe_forward_plan(moe_handle* h, int64_t num_tokens, moe_plan* out);
 
 /*
  * moe_route_noalloc -- the routing step alone, allocating nothing.  The pages

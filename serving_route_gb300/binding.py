@@ -38,12 +38,14 @@ MOE_FLAG_EMIT_FC1 = 0x4
 MOE_FLAG_GEMM_SINGLE_CTA = 0x8
 MOE_FLAG_GEMM_CTA_PAIR = 0x10
 MOE_FLAG_WATCHDOG_TEST = 0x20
+MOE_FLAG_SPLIT_GEMMS = 0x40
+MOE_FLAG_GEMMS_ONE_LAUNCH = 0x80
 
 # every function the header declares (checked against include/megamoe.h by a test)
 API_NAMES = ("moe_workspace_query", "moe_create", "moe_quantize_weights", "moe_bind_weights",
              "moe_stage_inputs", "moe_forward", "moe_read_status", "moe_debug_views",
-             "moe_set_profile_events", "moe_set_sm_budget", "moe_route_noalloc", "moe_destroy",
-             "moe_status_str")
+             "moe_set_profile_events", "moe_set_sm_budget", "moe_forward_plan", "moe_route_noalloc",
+             "moe_destroy", "moe_status_str")
 
 
 class moe_dims(ctypes.Structure):
@@ -61,6 +63,11 @@ class moe_debug_view(ctypes.Structure):
                 ("rows_alloc", ctypes.c_int64), ("sf_atom_bytes", ctypes.c_int32),
                 ("gemm_pair", ctypes.c_int32), ("gemm_ctas", ctypes.c_int32),
                 ("pad_rows", ctypes.c_int32), ("route_coop_blocks", ctypes.c_int32)]
+
+
+class moe_plan(ctypes.Structure):
+    _fields_ = [("route_kernels", ctypes.c_int32), ("gemm_launches", ctypes.c_int32),
+                ("swiglu_kernels", ctypes.c_int32), ("kernels", ctypes.c_int32)]
 
 
 class MoEError(RuntimeError):
@@ -93,6 +100,7 @@ def lib() -> ctypes.CDLL:
         L.moe_debug_views.argtypes = [vp, ctypes.POINTER(moe_debug_view)]
         L.moe_set_profile_events.argtypes = [vp, ctypes.POINTER(vp), i32]
         L.moe_set_sm_budget.argtypes = [vp, i32]
+        L.moe_forward_plan.argtypes = [vp, i64, ctypes.POINTER(moe_plan)]
         L.moe_route_noalloc.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.moe_destroy.argtypes = [vp]
         L.moe_destroy.restype = None
@@ -178,6 +186,12 @@ def moe_set_profile_events(h, event_handles) -> None:
 
 def moe_set_sm_budget(h, max_sms) -> None:
     _check(lib().moe_set_sm_budget(h, max_sms), "moe_set_sm_budget")
+
+
+def moe_forward_plan(h, num_tokens) -> moe_plan:
+    p = moe_plan()
+    _check(lib().moe_forward_plan(h, num_tokens, ctypes.byref(p)), "moe_forward_plan")
+    return p
 
 
 def moe_route_noalloc(d_idx, d_w, num_tokens, top_k, num_experts, check_routes, d_counts,

@@ -115,11 +115,47 @@ int budget_sms(const moe_handle* h) {
   return (h->sm_budget > 0 && h->sm_budget < h->num_sms) ? h->sm_budget : h->num_sms;
 }
 
+// Tile rounds of a forward of T tokens, estimated on the host (the real
+// counts stay on the device): routed rows per touched expert, padded to the
+// tactic's segment, in 128-row m-tiles, times the FC1 + FC2 n-tiles, over the
+// GEMM grid (in pairs for CTA pairs).
+double gemm_rounds_estimate(const moe_handle* h, int grid, int64_t T) {
+  const Layout& L = h->L;
+  const double routes = (double)T * L.K;
+  const double touched = routes < L.E ? routes : (double)L.E;
+  const double per = routes / touched;
+  const double seg = std::ceil(per / L.pad_rows) * L.pad_rows;
+  const double mtiles = touched * seg / 128.0;
+  const double units = (L.pair ? mtiles / 2 : mtiles) * (L.I / 128 + (L.H + 255) / 256);
+  const double slots = L.pair ? grid / 2 : grid;
+  return units / (slots > 0 ? slots : 1);
+}
+
 int gemm_grid(const moe_handle* h) {
   const int sms = budget_sms(h);
   if (!h->L.pair) return sms;
   const int c = sms & ~1;
   return c < h->pair_ctas ? c : h->pair_ctas;
+}
+
+// What a forward of T tokens launches (without profiling events): one
+// cooperative routing kernel when its blocks can all be resident and no SM
+// budget is set; FC1 -> FC2 as one launch when the fused epilogue is on and
+// the forward is short (or forced).
+moe_plan forward_plan(const moe_handle* h, int64_t T) {
+  moe_plan p = {0, 0, 0, 0};
+  if (T <= 0) return p;
+  const uint32_t f = h->dims.flags;
+  const bool fused = (f & MOE_FLAG_FUSE_FC1_EPILOGUE) != 0;
+  const int64_t fused_blocks = (T + 511) / 512;
+  const int coop = h->sm_budget > 0 ? 0 : h->route_coop_blocks;
+  p.route_kernels = (coop > 0 && fused_blocks <= coop) ? 1 : 3;
+  const bool one = fused && !(f & MOE_FLAG_SPLIT_GEMMS) &&
+                   ((f & MOE_FLAG_GEMMS_ONE_LAUNCH) || gemm_rounds_estimate(h, gemm_grid(h), T) <= 48.0);
+  p.gemm_launches = one ? 1 : 2;
+  p.swiglu_kernels = fused ? 0 : 1;
+  p.kernels = p.route_kernels + 1 + p.gemm_launches + p.swiglu_kernels + 1;
+  return p;
 }
 
 }  // namespace
@@ -129,6 +165,8 @@ namespace mm {
 moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_rows, float cf,
                           Layout* L) {
   if (!valid_dims(d)) return MOE_ERR_UNSUPPORTED;
+  if ((d->flags & MOE_FLAG_SPLIT_GEMMS) && (d->flags & MOE_FLAG_GEMMS_ONE_LAUNCH))
+    return MOE_ERR_INVALID_ARG;
   if ((d->flags & MOE_FLAG_GEMM_SINGLE_CTA) && (d->flags & MOE_FLAG_GEMM_CTA_PAIR))
     return MOE_ERR_INVALID_ARG;
   if (max_rows < 1 || max_rows > (int64_t)1 << 24) return MOE_ERR_INVALID_ARG;
@@ -179,7 +217,11 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
     o = align_up(o + bytes, kAlign);
     return at;
   };
-  L->o_status = take(1024);  // status word at +0, total_mtiles at +4, routing arrival counter at +8
+  // status word at +0, total_mtiles at +4, routing arrival counter at +8;
+  // the megakernel's per-m-tile counters follow at +1024, so one memset
+  // clears both
+  L->o_status = take(1024 + 4 * MB);
+  L->o_fc1_done = L->o_status + 1024;
   L->o_counts = take(4 * E);
   L->o_offsets = take(4 * (E + 1));
   L->o_pad_offsets = take(4 * (E + 1));
@@ -257,6 +299,7 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   w.status = reinterpret_cast<uint32_t*>(b + L.o_status);
   w.total_mtiles = reinterpret_cast<int32_t*>(b + L.o_status + 4);
   w.grid_sync = reinterpret_cast<uint32_t*>(b + L.o_status + 8);
+  w.fc1_done = reinterpret_cast<int32_t*>(b + L.o_fc1_done);
   w.counts = reinterpret_cast<int32_t*>(b + L.o_counts);
   w.offsets = reinterpret_cast<int32_t*>(b + L.o_offsets);
   w.pad_offsets = reinterpret_cast<int32_t*>(b + L.o_pad_offsets);
@@ -363,11 +406,16 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   const bool check = (h->dims.flags & MOE_FLAG_CHECK_ROUTES) != 0;
 
   if (ev) record_event(ev[0], s);
-  // status word, total_mtiles and the routing kernel's arrival counter
-  cudaMemsetAsync(ws.status, 0, 12, s);
+  // Both GEMMs in one launch unless asked otherwise or profiled per kernel
+  // (events between kernels need two launches to time FC1 and FC2).
+  const moe_plan plan = forward_plan(h, num_tokens);
+  const bool mega = ev == nullptr && plan.gemm_launches == 1;
+  // status word, total_mtiles, the routing kernel's arrival counter and (for
+  // the megakernel) the per-m-tile FC1 counters
+  cudaMemsetAsync(ws.status, 0, mega ? 1024 + 4 * (size_t)(L.rows_alloc / 128) : 12, s);
   // Under an SM budget the routing keeps to its three small kernels: a
   // cooperative grid would have to be resident beside the side-stream work.
-  const int coop = h->sm_budget > 0 ? 0 : h->route_coop_blocks;
+  const int coop = plan.route_kernels == 1 ? h->route_coop_blocks : 0;
   if (launch_route(ws, L, d_topk_idx, d_topk_w, num_tokens, check, s, ev ? ev + 1 : nullptr,
                    coop) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -406,8 +454,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   if (ev) record_event(ev[5], s);
   const bool pair = L.pair;
   const int ctas = gemm_grid(h);
-  if (launch_gemm(m1, pair, &h->tm_a, &h->tm_w1, &h->tm_asf, &h->tm_w1sf,
-                  &h->tm_y, g1, ctas, s, pdl) != cudaSuccess)
+  if (!mega && launch_gemm(m1, pair, &h->tm_a, &h->tm_w1, &h->tm_asf, &h->tm_w1sf, &h->tm_y, g1,
+                           ctas, s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[6], s);
   if (!fused && launch_swiglu_quant(ws, L, stream_ctas, s, pdl) != cudaSuccess) return MOE_ERR_CUDA;
@@ -429,9 +477,19 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.status = ws.status;
   g2.wait_limit_ns = g1.wait_limit_ns;
   if (ev) record_event(ev[7], s);
-  if (launch_gemm(kModeY, pair, &h->tm_hq, &h->tm_w2, &h->tm_hsf, &h->tm_w2sf,
-                  &h->tm_y, g2, ctas, s, pdl) != cudaSuccess)
+  if (mega) {
+    // the FC1 epilogue publishes, per m-tile, how many of its NT tiles are stored
+    g2.fc1_done = ws.fc1_done;
+    g2.fc1_ntiles = g1.NT;
+    g1.fc1_done = ws.fc1_done;
+    g1.fc1_ntiles = g1.NT;
+    if (launch_gemm_mega(pair, &h->tm_a, &h->tm_w1, &h->tm_asf, &h->tm_w1sf, &h->tm_hq, &h->tm_w2,
+                         &h->tm_hsf, &h->tm_w2sf, &h->tm_y, g1, g2, ctas, s, pdl) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else if (launch_gemm(kModeY, pair, &h->tm_hq, &h->tm_w2, &h->tm_hsf, &h->tm_w2sf, &h->tm_y, g2,
+                         ctas, s, pdl) != cudaSuccess) {
     return MOE_ERR_CUDA;
+  }
   if (ev) record_event(ev[8], s);
   if (launch_combine(ws, L, d_topk_w, h->out, num_tokens, s, pdl, stream_ctas) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -490,6 +548,12 @@ moe_status moe_set_profile_events(moe_handle* h, void* const* events, int32_t n)
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   for (int i = 0; i < 10; ++i) h->ev[i] = reinterpret_cast<cudaEvent_t>(events[i]);
   h->n_ev = 10;
+  return MOE_OK;
+}
+
+moe_status moe_forward_plan(moe_handle* h, int64_t num_tokens, moe_plan* out) {
+  if (!h || !out || num_tokens < 0) return MOE_ERR_INVALID_ARG;
+  *out = forward_plan(h, num_tokens);
   return MOE_OK;
 }
 

@@ -79,20 +79,51 @@ struct StageCfg {
   static constexpr size_t kDynSmem = (size_t)kStages * kStageBytes + kYStageBytes + 1024;
 };
 
+// Bounded wait until *count >= target (acquire at GPU scope), then a proxy
+// fence so that the TMA loads this thread issues next observe what the
+// threads that published the count wrote.
+__device__ __noinline__ bool wait_count_geq(const int32_t* count, int target, volatile int* abort,
+                                            uint32_t* status, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu_s32(count) < target) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      record_status(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
+// One launch runs the tiles of one GEMM (phase 0), or with MODE == kModeMega
+// the FC1 tiles (phase 0: tmA/tmB/tmSfa/tmSfb, g) and then the FC2 tiles
+// (phase 1: tmA2/tmB2/tmSfa2/tmSfb2, g2, tmY).  Units are numbered phase 0
+// first; each CTA (pair) takes every ustride-th unit in order, so a CTA has
+// issued all of its FC1 tiles before any FC2 tile, and FC2 tiles -- which
+// wait for their m-tile's fc1_done count -- never hold up an FC1 tile:
+// with every CTA resident the waits always end.
 template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmSfa,
                             const __grid_constant__ CUtensorMap tmSfb,
-                            const __grid_constant__ CUtensorMap tmY, const GemmArgs g) {
+                            const __grid_constant__ CUtensorMap tmY, const GemmArgs g,
+                            const __grid_constant__ CUtensorMap tmA2,
+                            const __grid_constant__ CUtensorMap tmB2,
+                            const __grid_constant__ CUtensorMap tmSfa2,
+                            const __grid_constant__ CUtensorMap tmSfb2, const GemmArgs g2) {
   using C = StageCfg<PAIR>;
   constexpr int kStages = C::kStages;
+  constexpr bool kMega = MODE == kModeMega;
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ __align__(8) uint64_t accf_bar, acce_bar, drain_bar;
   __shared__ __align__(8) uint64_t amax_bar[4];  // per quadrant: both column halves posted
+  __shared__ __align__(8) uint64_t fc1_bar[2];   // kModeMega: the epilogue warps' FC1 stores, by tile parity
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ float amax_sh[2][2][128];  // [tile parity][column half][row] (fused epilogue)
@@ -105,11 +136,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool leader = rank == 0;
   const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int ustride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  // this CTA's 128-row m-tile of work unit u
-  auto own_mtile = [&](int u) {
-    const int m = u / g.NT;
-    return PAIR ? 2 * m + (int)rank : m;
-  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -120,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&acce_bar), kEpiWarps * (PAIR ? 2 : 1));
     mbar_init(smem_u32(&drain_bar), 1);
     for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&amax_bar[i]), 2);
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&fc1_bar[i]), kEpiWarps);
     abort_sh = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmA);
@@ -127,6 +154,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (PAIR) {
       prefetch_tensormap(&tmSfa);
       prefetch_tensormap(&tmSfb);
+    }
+    if (kMega) {
+      prefetch_tensormap(&tmA2);
+      prefetch_tensormap(&tmB2);
+      if (PAIR) {
+        prefetch_tensormap(&tmSfa2);
+        prefetch_tensormap(&tmSfb2);
+      }
     }
   }
   if (warp == 1) {
@@ -150,7 +185,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   int mtiles = *g.total_mtiles;
   if (mtiles > g.max_mtiles) mtiles = g.max_mtiles;
   // work units: single CTA -> (m-tile, n-tile); pair -> (m-tile pair, n-tile)
-  const int total = (PAIR ? mtiles / 2 : mtiles) * g.NT;
+  const int units_m = PAIR ? mtiles / 2 : mtiles;
+  const int total0 = units_m * g.NT;
+  const int total = total0 + (kMega ? units_m * g2.NT : 0);
+  // unit u -> phase, m index (pair index for pairs), n-tile
+  auto phase_of = [&](int u) { return (kMega && u >= total0) ? 1 : 0; };
+  auto m_of = [&](int u, int ph) { return ph ? (u - total0) / g2.NT : u / g.NT; };
+  auto nt_of = [&](int u, int ph, int m) { return ph ? (u - total0) - m * g2.NT : u - m * g.NT; };
+  auto own_mtile = [&](int m) { return PAIR ? 2 * m + (int)rank : m; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -158,28 +200,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     // fetched one unit ahead so no dependent global load stalls the producer
     // at a tile boundary.  Every fourth K block the stage also carries the
     // scale atoms of the next four K blocks (A: this m-tile; B: the two
-    // 128-row halves of the n-tile).
+    // 128-row halves of the n-tile).  An FC2 tile of the megakernel first
+    // waits until every FC1 tile of its m-tile has published its hq rows.
     auto expert_of = [&](int u) -> int {
-      return u < total ? g.mtile_expert[(PAIR ? 2 : 1) * (u / g.NT)] : 0;
+      return u < total ? g.mtile_expert[(PAIR ? 2 : 1) * m_of(u, phase_of(u))] : 0;
     };
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued at least once, parity of last issue
+    // the m-tile count an FC2 unit waits for, read (relaxed) one unit ahead
+    auto count_of = [&](int u) -> int {
+      return (kMega && u < total && phase_of(u))
+                 ? ld_relaxed_gpu_s32(g2.fc1_done + own_mtile(m_of(u, 1)))
+                 : 0;
+    };
     int e_next = expert_of(unit0);
+    int count_next = count_of(unit0);
     for (int u = unit0; u < total && !*abort; u += ustride) {
-      const int mt = own_mtile(u);
+      const int ph = phase_of(u);
+      const int m = m_of(u, ph);
+      const int nt = nt_of(u, ph, m);
+      const int mt = own_mtile(m);
       const int e = e_next;
       e_next = expert_of(u + ustride);
-      const int nt = u - (u / g.NT) * g.NT;
+      const int count_seen = count_next;
+      count_next = count_of(u + ustride);
+      const int KB = ph ? g2.KB : g.KB, NB = ph ? g2.NB : g.NB, KQ = ph ? g2.KQ : g.KQ;
+      const CUtensorMap* mA = ph ? &tmA2 : &tmA;
+      const CUtensorMap* mB = ph ? &tmB2 : &tmB;
+      const CUtensorMap* mSfa = ph ? &tmSfa2 : &tmSfa;
+      const CUtensorMap* mSfb = ph ? &tmSfb2 : &tmSfb;
+      const uint8_t* gsfa = ph ? g2.sfa : g.sfa;
+      const uint8_t* gsfb = ph ? g2.sfb : g.sfb;
+      if (kMega && ph == 1) {
+        // usually complete by now (read a unit ago): the fence makes that
+        // read an acquire; otherwise the bounded acquire-polling wait
+        int ok = 1;
+        if (lane == 0) {
+          if (count_seen >= g2.fc1_ntiles) {
+            fence_acq_rel_gpu();
+            fence_proxy_async_global();
+          } else {
+            ok = wait_count_geq(g2.fc1_done + mt, g2.fc1_ntiles, abort, g.status, g.wait_limit_ns);
+          }
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+      }
       // the n-tile's two 128-row weight blocks (the second clamped to the
       // first past N: those output columns are never stored); a pair CTA
       // stages the block of its rank
-      const int nb0 = 2 * nt, nb1 = (2 * nt + 1 < g.NB) ? 2 * nt + 1 : 2 * nt;
-      const int wb0 = e * g.NB + nb0, wb1 = e * g.NB + nb1;
-      const int64_t sfb0 = ((int64_t)e * g.NB + nb0) * g.KQ, sfb1 = ((int64_t)e * g.NB + nb1) * g.KQ;
-      const int64_t sfa0 = (int64_t)mt * g.KQ;
+      const int nb0 = 2 * nt, nb1 = (2 * nt + 1 < NB) ? 2 * nt + 1 : 2 * nt;
+      const int wb0 = e * NB + nb0, wb1 = e * NB + nb1;
+      const int64_t sfb0 = ((int64_t)e * NB + nb0) * KQ, sfb1 = ((int64_t)e * NB + nb1) * KQ;
+      const int64_t sfa0 = (int64_t)mt * KQ;
       bool ok = true;
-      for (int kb = 0; kb < g.KB; ++kb) {
+      for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort, g.status, g.wait_limit_ns)) {
           ok = false;
           break;
@@ -205,23 +280,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader)
               mbar_arrive_expect_tx(smem_u32(&full_bar[stage]),
                                     2 * (C::kTxBytes + (atoms ? C::kTxAtomBytes : 0u)));
-            tma_load_3d_pair(sst + C::kOffA, &tmA, fb, 0, kb * 128, mt);
-            tma_load_3d_pair(sst + C::kOffB, &tmB, fb, 0, kb * 128, rank ? wb1 : wb0);
+            tma_load_3d_pair(sst + C::kOffA, mA, fb, 0, kb * 128, mt);
+            tma_load_3d_pair(sst + C::kOffB, mB, fb, 0, kb * 128, rank ? wb1 : wb0);
             if (atoms) {
-              tma_load_2d_pair(sst + C::kOffSfa, &tmSfa, fb, 0, (int)(sfa0 + q));
-              tma_load_2d_pair(sst + C::kOffSfb, &tmSfb, fb, 0, (int)(sfb0 + q));
-              tma_load_2d_pair(sst + C::kOffSfb + 512, &tmSfb, fb, 0, (int)(sfb1 + q));
+              tma_load_2d_pair(sst + C::kOffSfa, mSfa, fb, 0, (int)(sfa0 + q));
+              tma_load_2d_pair(sst + C::kOffSfb, mSfb, fb, 0, (int)(sfb0 + q));
+              tma_load_2d_pair(sst + C::kOffSfb + 512, mSfb, fb, 0, (int)(sfb1 + q));
             }
           } else {
             const uint32_t fb = smem_u32(&full_bar[stage]);
             mbar_arrive_expect_tx(fb, C::kTxBytes + (atoms ? C::kTxAtomBytes : 0u));
-            tma_load_3d(sst + C::kOffA, &tmA, fb, 0, kb * 128, mt);
-            tma_load_3d(sst + C::kOffB, &tmB, fb, 0, kb * 128, wb0);
-            tma_load_3d(sst + C::kOffB + 16384, &tmB, fb, 0, kb * 128, wb1);
+            tma_load_3d(sst + C::kOffA, mA, fb, 0, kb * 128, mt);
+            tma_load_3d(sst + C::kOffB, mB, fb, 0, kb * 128, wb0);
+            tma_load_3d(sst + C::kOffB + 16384, mB, fb, 0, kb * 128, wb1);
             if (atoms) {
-              bulk_load(sst + C::kOffSfa, g.sfa + (sfa0 + q) * kSfAtomBytes, kSfAtomBytes, fb);
-              bulk_load(sst + C::kOffSfb, g.sfb + (sfb0 + q) * kSfAtomBytes, kSfAtomBytes, fb);
-              bulk_load(sst + C::kOffSfb + 512, g.sfb + (sfb1 + q) * kSfAtomBytes, kSfAtomBytes, fb);
+              bulk_load(sst + C::kOffSfa, gsfa + (sfa0 + q) * kSfAtomBytes, kSfAtomBytes, fb);
+              bulk_load(sst + C::kOffSfb, gsfb + (sfb0 + q) * kSfAtomBytes, kSfAtomBytes, fb);
+              bulk_load(sst + C::kOffSfb + 512, gsfb + (sfb1 + q) * kSfAtomBytes, kSfAtomBytes, fb);
             }
           }
         }
@@ -278,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait<PAIR>(smem_u32(&acce_bar), acc_phase ^ 1u, abort, g.status, g.wait_limit_ns)) break;
         tc_fence_after();
         bool ok = true;
-        for (int kb = 0; kb < g.KB; ++kb) {
+        const int KB = phase_of(u) ? g2.KB : g.KB;
+        for (int kb = 0; kb < KB; ++kb) {
           if (!ready &&
               !mbar_wait_slow<PAIR>(smem_u32(&full_bar[stage]), phase, abort, g.status, g.wait_limit_ns)) {
             ok = false;
@@ -358,18 +434,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the accumulator-empty barrier lives in the leader CTA
     const uint32_t acce_addr = PAIR ? mapa_shared(smem_u32(&acce_bar), 0) : smem_u32(&acce_bar);
     uint32_t acc_phase = 0;
+    uint32_t fc1_tiles = 0;  // kModeMega: FC1 tiles this CTA has published
     for (int u = unit0; u < total; u += ustride) {
-      const int mt = own_mtile(u);
-      const int nt = u - (u / g.NT) * g.NT;
+      const int ph = phase_of(u);
+      const int m = m_of(u, ph);
+      const int nt = nt_of(u, ph, m);
+      const int mt = own_mtile(m);
+      // the epilogue of this unit: the launch's mode, or per phase in the
+      // megakernel (FC1 fused, with gate||up kept when its output is bound)
+      const int em = kMega ? (ph ? kModeY : (g.out ? kModeFusedGU : kModeFused)) : MODE;
+      const bool em_y = em == kModeY;
+      const bool em_gu = em == kModeGU || em == kModeFusedGU;
+      const bool em_fused = em == kModeFused || em == kModeFusedGU;
       if (!mbar_wait(smem_u32(&accf_bar), acc_phase, abort, g.status, g.wait_limit_ns)) break;
       tc_fence_after();
       const int64_t row = (int64_t)mt * 128 + row_in_tile;
       // FC2: the second column half of a tile past H holds no output
-      const bool active = !(MODE == kModeY && half == 1 && nt * 256 + 128 >= g.N);
+      const bool active = !(em_y && half == 1 && nt * 256 + 128 >= (ph ? g2.N : g.N));
       uint32_t pk[64];  // BF16 pairs of this warp's 128 accumulator columns
       if (active) {
         uint32_t r[4][32];
-        if constexpr (MODE == kModeY) {
+        if (em_y) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld32(tlane + half * 128 + c * 32, r[c]);
         } else {
@@ -404,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Stores are 32 bytes per thread per instruction (whole sectors): every
       // destination below is 32-byte aligned (row pitches and tile offsets are
       // multiples of 64 bytes, buffers 1024-byte aligned).
-      if constexpr (MODE == kModeY && C::kTmaStoreY) {
+      if (em_y && C::kTmaStoreY) {
         // TMA stores: the warp's 32 rows x 128 columns leave in four 32x32
         // boxes through its 2 KB staging buffer; row r's 16-byte chunk j sits
         // at r*64 + ((j ^ ((r >> 1) & 3)) * 16) (the 64-byte swizzle).
@@ -430,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      } else if constexpr (MODE == kModeY) {
+      } else if (em_y) {
         if (active) {
           uint16_t* dst = g.out + row * g.ld_out + (int64_t)nt * 256 + half * 128;
 #pragma unroll
@@ -439,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          pk[8 * v + 4], pk[8 * v + 5], pk[8 * v + 6], pk[8 * v + 7]);
         }
       }
-      if constexpr (MODE == kModeGU || MODE == kModeFusedGU) {
+      if (em_gu) {
         uint16_t* dg = g.out + row * g.ld_out + (int64_t)nt * 128 + half * 64;
         uint16_t* du = dg + g.inter;
 #pragma unroll
@@ -451,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        pk[32 + 8 * v + 6], pk[32 + 8 * v + 7]);
         }
       }
-      if constexpr (MODE == kModeFused || MODE == kModeFusedGU) {
+      if (em_fused) {
         // gate pairs pk[0..31], up pairs pk[32..63] -> h[0..63]
         float h[64];
         float amax = 0.f;
@@ -484,10 +569,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (half == 0) g.h_sf[sf_atom_offset(row, nt, g.IB)] = (uint8_t)(e + 127);
       }
+      if (kMega && ph == 0) {
+        // Publish this FC1 tile: every epilogue warp's hq / scale stores are
+        // ordered before its arrival (proxy fence: FC2 reads them by TMA);
+        // one thread waits for all eight arrivals, then adds to the m-tile's
+        // count with release semantics.  Two barriers alternate by tile, so a
+        // warp already on the next FC1 tile cannot arrive on this phase.
+        fence_proxy_async_global();
+        __syncwarp();
+        const uint32_t fb = smem_u32(&fc1_bar[fc1_tiles & 1u]);
+        if (lane == 0) mbar_arrive(fb);
+        if (warp == 2) {
+          int ok = 1;
+          if (lane == 0) {
+            ok = mbar_wait(fb, (fc1_tiles >> 1) & 1u, abort, g.status, g.wait_limit_ns) ? 1 : 0;
+            if (ok) {
+              __threadfence();
+              red_release_gpu_add(g.fc1_done + mt, 1);
+            }
+          }
+          if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;  // the whole warp leaves together
+        }
+        ++fc1_tiles;
+      }
     }
   }
 
-  if constexpr (MODE == kModeY && StageCfg<PAIR>::kTmaStoreY) {
+  if constexpr ((MODE == kModeY || MODE == kModeMega) && StageCfg<PAIR>::kTmaStoreY) {
     if (warp >= 2 && lane == 0) bulk_wait_group0();  // this warp's output boxes are written
   }
   tc_fence_before();
@@ -519,7 +627,9 @@ cudaError_t gemm_set_attributes() {
   if ((e = set_attr<kModeY, true>()) != cudaSuccess) return e;
   if ((e = set_attr<kModeGU, true>()) != cudaSuccess) return e;
   if ((e = set_attr<kModeFused, true>()) != cudaSuccess) return e;
-  return set_attr<kModeFusedGU, true>();
+  if ((e = set_attr<kModeFusedGU, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<kModeMega, false>()) != cudaSuccess) return e;
+  return set_attr<kModeMega, true>();
 }
 
 static cudaLaunchAttribute pair_cluster_attr() {
@@ -547,30 +657,51 @@ int gemm_max_pairs() {
   return n;
 }
 
+// Single-phase launches pass the phase-0 maps and args again as phase 1
+// (unused).  The single-CTA kernel reads scale atoms by bulk copy, so its
+// atom maps are placeholders too.
 template <int MODE>
 static cudaError_t launch_mode(bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
                                const CUtensorMap* tmSfa, const CUtensorMap* tmSfb,
-                               const CUtensorMap* tmY, const GemmArgs& g, int ctas,
-                               cudaStream_t s, bool pdl) {
+                               const CUtensorMap* tmA2, const CUtensorMap* tmB2,
+                               const CUtensorMap* tmSfa2, const CUtensorMap* tmSfb2,
+                               const CUtensorMap* tmY, const GemmArgs& g, const GemmArgs& g2,
+                               int ctas, cudaStream_t s, bool pdl) {
   if (!pair)
     return launch_k(fp8_grouped_gemm_kernel<MODE, false>, dim3(ctas), dim3(kThreads),
-                    StageCfg<false>::kDynSmem, s, pdl, nullptr, *tmA, *tmB, *tmA, *tmA, *tmY, g);
+                    StageCfg<false>::kDynSmem, s, pdl, nullptr, *tmA, *tmB, *tmA, *tmA, *tmY, g,
+                    *tmA2, *tmB2, *tmA2, *tmA2, g2);
   const cudaLaunchAttribute cluster = pair_cluster_attr();
   return launch_k(fp8_grouped_gemm_kernel<MODE, true>, dim3(ctas), dim3(kThreads),
-                  StageCfg<true>::kDynSmem, s, pdl, &cluster, *tmA, *tmB, *tmSfa, *tmSfb, *tmY, g);
+                  StageCfg<true>::kDynSmem, s, pdl, &cluster, *tmA, *tmB, *tmSfa, *tmSfb, *tmY, g,
+                  *tmA2, *tmB2, *tmSfa2, *tmSfb2, g2);
 }
 
 cudaError_t launch_gemm(GemmMode mode, bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         const CUtensorMap* tmSfa, const CUtensorMap* tmSfb, const CUtensorMap* tmY,
                         const GemmArgs& g, int ctas, cudaStream_t s, bool pdl) {
+#define MM_ONE_PHASE(M) \
+  launch_mode<M>(pair, tmA, tmB, tmSfa, tmSfb, tmA, tmB, tmSfa, tmSfb, tmY, g, g, ctas, s, pdl)
   switch (mode) {
-    case kModeY: return launch_mode<kModeY>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s, pdl);
-    case kModeGU: return launch_mode<kModeGU>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s, pdl);
-    case kModeFused: return launch_mode<kModeFused>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s, pdl);
-    case kModeFusedGU:
-      return launch_mode<kModeFusedGU>(pair, tmA, tmB, tmSfa, tmSfb, tmY, g, ctas, s, pdl);
+    case kModeY: return MM_ONE_PHASE(kModeY);
+    case kModeGU: return MM_ONE_PHASE(kModeGU);
+    case kModeFused: return MM_ONE_PHASE(kModeFused);
+    case kModeFusedGU: return MM_ONE_PHASE(kModeFusedGU);
+    case kModeMega: break;  // two phases: launch_gemm_mega
   }
+#undef MM_ONE_PHASE
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_mega(bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                             const CUtensorMap* tmSfa, const CUtensorMap* tmSfb,
+                             const CUtensorMap* tmA2, const CUtensorMap* tmB2,
+                             const CUtensorMap* tmSfa2, const CUtensorMap* tmSfb2,
+                             const CUtensorMap* tmY, const GemmArgs& g, const GemmArgs& g2, int ctas,
+                             cudaStream_t s, bool pdl) {
+  if (!g2.fc1_done || g2.fc1_ntiles != g.NT) return cudaErrorInvalidValue;
+  return launch_mode<kModeMega>(pair, tmA, tmB, tmSfa, tmSfb, tmA2, tmB2, tmSfa2, tmSfb2, tmY, g,
+                                g2, ctas, s, pdl);
 }
 
 }  // namespace mm

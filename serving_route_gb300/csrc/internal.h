@@ -15,6 +15,7 @@ struct Workspace {
   uint32_t* status;        // device status word (MOE_DEV_* bits)
   int32_t* total_mtiles;   // number of 128-row GEMM tiles of this forward
   uint32_t* grid_sync;     // arrival counter of the one-kernel routing (zeroed before each forward)
+  int32_t* fc1_done;       // [max_mtiles] FC1 tiles published per m-tile (zeroed before each forward)
   int32_t* counts;         // [E]
   int32_t* offsets;        // [E+1]
   int32_t* pad_offsets;    // [E+1]
@@ -54,6 +55,7 @@ struct Layout {
   bool keep_gu;
   size_t ws_bytes, w_bytes;
   // byte offsets inside the workspace / weight store
+  size_t o_fc1_done;   // [max_mtiles] int32 counters of the megakernel, right after the status
   size_t o_status, o_counts, o_offsets, o_pad_offsets, o_mtile_expert, o_block_counts, o_base_u,
       o_base_p, o_perm, o_inv, o_inv_pad, o_a, o_a_sf, o_gu, o_hq, o_h_sf, o_y;
   size_t o_w1, o_w2, o_w1_sf, o_w2_sf, o_w1_sfatoms, o_w2_sfatoms;
@@ -89,7 +91,10 @@ cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const
                                   uint32_t* status, cudaStream_t s);
 
 // gemm.cu
-enum GemmMode { kModeY = 0, kModeGU = 1, kModeFused = 2, kModeFusedGU = 3 };
+// kModeMega: one persistent launch of both GEMMs -- every FC1 tile (fused
+// epilogue; gate||up also stored when that phase's `out` is set), then every
+// FC2 tile, each FC2 tile's loads waiting for its m-tile's fc1_done count.
+enum GemmMode { kModeY = 0, kModeGU = 1, kModeFused = 2, kModeFusedGU = 3, kModeMega = 4 };
 struct GemmArgs {
   const uint8_t* sfa;          // scale atoms of A: [mblocks][KQ][512]
   const uint8_t* sfb;          // scale atoms of B: [E][NB][KQ][512]
@@ -110,6 +115,11 @@ struct GemmArgs {
   uint32_t* status;
   uint64_t wait_limit_ns;      // bound of every mbarrier wait (1 s; 20 ms in the watchdog test)
   int watchdog_test;           // 1: CTA 0 withholds one stage so its MMA wait expires
+  // kModeMega: per 128-row m-tile, the FC1 tiles whose fused-epilogue stores
+  // are complete and visible (zeroed before each forward); FC2 tiles of an
+  // m-tile start loading when it reaches fc1_ntiles
+  int32_t* fc1_done;
+  int fc1_ntiles;
 };
 cudaError_t gemm_set_attributes();
 int gemm_max_pairs();
@@ -123,6 +133,15 @@ int gemm_max_pairs();
 cudaError_t launch_gemm(GemmMode mode, bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         const CUtensorMap* tmSfa, const CUtensorMap* tmSfb, const CUtensorMap* tmY,
                         const GemmArgs& g, int ctas, cudaStream_t s, bool pdl);
+// Both GEMMs in one launch (kModeMega): phase 0 = FC1 with tmA/tmB/tmSfa/tmSfb
+// and g (fused epilogue), phase 1 = FC2 with tmA2/tmB2/tmSfa2/tmSfb2, tmY and
+// g2 (g2.fc1_done / fc1_ntiles set).
+cudaError_t launch_gemm_mega(bool pair, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                             const CUtensorMap* tmSfa, const CUtensorMap* tmSfb,
+                             const CUtensorMap* tmA2, const CUtensorMap* tmB2,
+                             const CUtensorMap* tmSfa2, const CUtensorMap* tmSfb2,
+                             const CUtensorMap* tmY, const GemmArgs& g, const GemmArgs& g2, int ctas,
+                             cudaStream_t s, bool pdl);
 
 // combine.cu
 cudaError_t launch_combine(const Workspace& ws, const Layout& L, const float* topk_w,

@@ -211,12 +211,6 @@ __global__ void __launch_bounds__(kRouteTokens) route_scatter_kernel(
 //            m-tile table) are spread over the blocks
 //   phase 3  the stable scatter of route_scatter, bases from shared memory
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // 512 tokens per block (a warp per 32 tokens, as in route_scatter): four
 // times fewer histogram rows than the 128-token blocks of the three-kernel
 // form, and four times the threads to read them after the barrier.
@@ -285,7 +279,7 @@ __global__ void __launch_bounds__(kFusedTokens) route_fused_kernel(
     atomicAdd(grid_sync, 1u);
     bool ok = true;
     const uint64_t t0 = globaltimer_ns();
-    while (ld_acquire_gpu(grid_sync) < (uint32_t)nb) {
+    while (ld_acquire_gpu_u32(grid_sync) < (uint32_t)nb) {
       if (globaltimer_ns() - t0 > wait_limit_ns) {
         ok = false;
         break;

@@ -16,9 +16,16 @@ class MegaMoELayer:
     def __init__(self, hidden: int, inter: int, num_experts: int, top_k: int, *, max_rows: int,
                  expected_m: int | None = None, capacity_factor: float = 1.0,
                  fuse_fc1: bool = False, check_routes: bool = True, emit_fc1: bool = False,
-                 gemm: str = "auto", watchdog_test: bool = False, device="cuda"):
+                 gemm: str = "auto", watchdog_test: bool = False, device="cuda",
+                 workspace: torch.Tensor | None = None, gemms: str = "auto"):
         """gemm: "auto" (tactic from expected_m), "single" (one CTA per SM) or
-        "pair" (CTA pairs, tcgen05 cta_group::2)."""
+        "pair" (CTA pairs, tcgen05 cta_group::2).  gemms (fused epilogue only):
+        "auto" (FC1 -> FC2 in one persistent launch for short forwards, two
+        launches for long ones), "one_launch" or "split"; same results.
+        workspace: a uint8 device
+        tensor shared with other layers whose forwards never overlap with this
+        one's (at least workspace_bytes() of every layer that shares it); by
+        default the layer allocates its own."""
         self.H, self.I, self.E, self.K = hidden, inter, num_experts, top_k
         self.max_rows = max_rows
         self.flags = ((B.MOE_FLAG_FUSE_FC1_EPILOGUE if fuse_fc1 else 0)
@@ -26,17 +33,36 @@ class MegaMoELayer:
                       | (B.MOE_FLAG_EMIT_FC1 if emit_fc1 else 0)
                       | {"auto": 0, "single": B.MOE_FLAG_GEMM_SINGLE_CTA,
                          "pair": B.MOE_FLAG_GEMM_CTA_PAIR}[gemm]
-                      | (B.MOE_FLAG_WATCHDOG_TEST if watchdog_test else 0))
+                      | (B.MOE_FLAG_WATCHDOG_TEST if watchdog_test else 0)
+                      | {"auto": 0, "one_launch": B.MOE_FLAG_GEMMS_ONE_LAUNCH,
+                         "split": B.MOE_FLAG_SPLIT_GEMMS}[gemms])
         em = expected_m if expected_m is not None else max_rows
         ws, wb = B.moe_workspace_query(hidden, inter, num_experts, top_k, self.flags, em, max_rows,
                                        capacity_factor)
-        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
+        if workspace is None:
+            workspace = torch.empty(ws, dtype=torch.uint8, device=device)
+        assert workspace.dtype == torch.uint8 and workspace.is_cuda and workspace.is_contiguous()
+        assert workspace.numel() >= ws, (workspace.numel(), ws)
+        self.workspace = workspace
         self.weight_store = torch.empty(wb, dtype=torch.uint8, device=device)
         self.handle = B.moe_create(hidden, inter, num_experts, top_k, self.flags, em, max_rows,
-                                   capacity_factor, self.workspace.data_ptr(), ws,
+                                   capacity_factor, self.workspace.data_ptr(), self.workspace.numel(),
                                    self.weight_store.data_ptr(), wb)
         self.out = torch.empty(max_rows, hidden, dtype=torch.bfloat16, device=device)
         B.moe_stage_inputs(self.handle, self.out.data_ptr())
+
+    @staticmethod
+    def workspace_bytes(hidden: int, inter: int, num_experts: int, top_k: int, *, max_rows: int,
+                        expected_m: int | None = None, capacity_factor: float = 1.0,
+                        fuse_fc1: bool = False, emit_fc1: bool = False, gemm: str = "auto") -> int:
+        """Workspace size a layer of these dims needs (for a shared workspace)."""
+        flags = ((B.MOE_FLAG_FUSE_FC1_EPILOGUE if fuse_fc1 else 0)
+                 | (B.MOE_FLAG_EMIT_FC1 if emit_fc1 else 0)
+                 | {"auto": 0, "single": B.MOE_FLAG_GEMM_SINGLE_CTA,
+                    "pair": B.MOE_FLAG_GEMM_CTA_PAIR}[gemm])
+        em = expected_m if expected_m is not None else max_rows
+        return B.moe_workspace_query(hidden, inter, num_experts, top_k, flags, em, max_rows,
+                                     capacity_factor)[0]
 
     # -- weights ----------------------------------------------------------------
     @staticmethod
@@ -100,10 +126,15 @@ class MegaMoELayer:
         return dict(gemm_pair=bool(v.gemm_pair), gemm_ctas=int(v.gemm_ctas), pad_rows=int(v.pad_rows),
                     route_coop_blocks=int(v.route_coop_blocks))
 
+    def plan(self, num_tokens: int) -> dict:
+        """The kernels a forward of num_tokens tokens enqueues (moe_forward_plan)."""
+        p = B.moe_forward_plan(self.handle, num_tokens)
+        return dict(route_kernels=p.route_kernels, gemm_launches=p.gemm_launches,
+                    swiglu_kernels=p.swiglu_kernels, kernels=p.kernels)
+
     def route_kernels(self, num_tokens: int) -> int:
         """Kernels the routing step launches for a forward of num_tokens tokens (1 or 3)."""
-        lim = self.tactic()["route_coop_blocks"]
-        return 1 if 0 < (num_tokens + 511) // 512 <= lim else 3
+        return self.plan(num_tokens)["route_kernels"]
 
     def debug(self) -> dict:
         """torch views of the internal buffers (slices of the workspace); the

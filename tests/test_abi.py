@@ -62,6 +62,14 @@ def test_workspace_query_capacity_and_tactic(B):
     for bad in ((0, 128, 1.0), (1, 0, 1.0), (1, 128, 0.0), (1, 128, -1.0), (1, 128, 100.0)):
         with pytest.raises(B.MoEError):
             B.moe_workspace_query(512, 256, 8, 2, 0, *bad)
+    # one or two GEMM launches: the forcing flags exclude each other, and
+    # neither changes a buffer size
+    f = B.MOE_FLAG_FUSE_FC1_EPILOGUE
+    assert B.moe_workspace_query(7168, 2048, 256, 8, f | B.MOE_FLAG_SPLIT_GEMMS, 1, 8192) == fused
+    assert B.moe_workspace_query(7168, 2048, 256, 8, f | B.MOE_FLAG_GEMMS_ONE_LAUNCH, 1, 8192) == fused
+    with pytest.raises(B.MoEError):
+        B.moe_workspace_query(512, 256, 8, 2, f | B.MOE_FLAG_SPLIT_GEMMS | B.MOE_FLAG_GEMMS_ONE_LAUNCH,
+                              1, 128)
 
 
 def test_null_arguments_rejected_without_cuda(B):
@@ -70,3 +78,4 @@ def test_null_arguments_rejected_without_cuda(B):
     assert L.moe_stage_inputs(None, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_forward(None, None, None, None, 1, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_debug_views(None, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_forward_plan(None, 1, None) == B.MOE_ERR_INVALID_ARG

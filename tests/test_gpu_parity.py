@@ -430,6 +430,102 @@ def test_one_kernel_routing_matches_three_kernels(lib, orc, T, H, E, K, mask):
     assert np.array_equal(d1["inv"][:T * K].cpu().numpy(), ref["inv"])
 
 
+def test_shared_workspace_between_layers(lib, orc):
+    """Two layers of different dims share one workspace (workspace pooling) and
+    run in turn on one stream: every output is bit-identical to the same layer
+    with a workspace of its own, and matches the oracle."""
+    S = lib
+    dims = [(300, 512, 256, 8, 2), (517, 256, 384, 6, 4)]
+    probs = [small_problem(orc, T, H, I, E, K, seed=31 + j) for j, (T, H, I, E, K) in enumerate(dims)]
+    need = max(S.MegaMoELayer.workspace_bytes(H, I, E, K, max_rows=T, fuse_fc1=True)
+               for T, H, I, E, K in dims)
+    shared = torch.empty(need, dtype=torch.uint8, device="cuda")
+    pooled, private, refs, inputs = [], [], [], []
+    for (T, H, I, E, K), (x, idx, w, w1, w2) in zip(dims, probs):
+        q1, s1 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w1).cuda())
+        q2, s2 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w2).cuda())
+        for lst, ws in ((pooled, shared), (private, None)):
+            layer = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, workspace=ws)
+            layer.bind_weights(q1, s1, q2, s2)
+            lst.append(layer)
+        refs.append(orc.forward(x, idx, w, *(orc.quant_weights(w1) + orc.quant_weights(w2))))
+        inputs.append(gh.to_device(x, idx, w))
+    assert pooled[0].workspace.data_ptr() == pooled[1].workspace.data_ptr()
+    expect = []
+    for layer, (xt, it, wt) in zip(private, inputs):
+        expect.append(layer.forward(xt, it, wt).clone())
+        assert layer.read_status() == (0, 0)
+    for rnd in range(3):  # alternate: each forward overwrites what the other left
+        for j, (layer, (xt, it, wt)) in enumerate(zip(pooled, inputs)):
+            out = layer.forward(xt, it, wt)
+            assert layer.read_status() == (0, 0)
+            assert torch.equal(out.view(torch.int16), expect[j].view(torch.int16)), (rnd, j)
+    for j, (T, H, I, E, K) in enumerate(dims):
+        o = gh.bf16_np(expect[j])
+        r = gh.bits_to_f64(refs[j]["out"])
+        assert gh.rel_l2(o, r) <= OUT_TOL
+
+
+@pytest.mark.parametrize("T,H,I,E,K,gemm,emit,empty", [
+    (77, 256, 384, 6, 2, "single", True, ()),      # ragged T, 3 FC1 n-tiles, gate||up kept
+    (513, 1024, 512, 8, 6, "pair", False, ()),     # CTA pairs
+    (300, 512, 256, 16, 4, "single", False, (3, 7, 11)),  # empty experts
+    (8, 512, 256, 64, 8, "auto", False, ()),       # decode-like: one row per touched expert
+    (2048, 768, 640, 32, 8, "pair", True, (0,)),   # pairs, odd FC2 n-tile count, an empty expert
+])
+def test_megakernel_matches_two_launches(lib, orc, T, H, I, E, K, gemm, emit, empty):
+    """The one-launch FC1 -> FC2 kernel (per-m-tile fc1_done counts) and the two
+    launches compute every tile the same way: output, hq, its scales and
+    gate||up are bit-identical; the output also matches the oracle."""
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=41, empty=empty)
+    xt, it, wt = gh.to_device(x, idx, w)
+    res = []
+    for split in (False, True):
+        q1, s1 = lib.MegaMoELayer.quantize_weights(torch.from_numpy(w1).cuda())
+        q2, s2 = lib.MegaMoELayer.quantize_weights(torch.from_numpy(w2).cuda())
+        layer = lib.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, emit_fc1=emit, gemm=gemm,
+                                 gemms="split" if split else "one_launch")
+        layer.bind_weights(q1, s1, q2, s2)
+        out = layer.forward(xt, it, wt).clone()
+        assert layer.read_status() == (0, 0), split
+        d = layer.debug()
+        off = d["offsets"].cpu().numpy()
+        rows = torch.from_numpy(gh.padded_rows(off, d["pad_offsets"].cpu().numpy(), int(off[-1]))).cuda()
+        sf = lib.sf_atom_rows(d["h_sf"], d["rows_alloc"], I // 128)[rows]
+        r = [out.view(torch.int16), d["hq"][rows], sf, d["y"][rows].view(torch.int16)]
+        if emit:
+            r.append(d["gu"][rows].view(torch.int16))
+        res.append(r)
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+    ref = orc.forward(x, idx, w, *(orc.quant_weights(w1) + orc.quant_weights(w2)))
+    o = gh.bf16_np(res[0][0].view(torch.bfloat16))
+    assert gh.rel_l2(o, gh.bits_to_f64(ref["out"])) <= OUT_TOL
+
+
+def test_forward_plan(lib):
+    """moe_forward_plan: one GEMM launch for short fused forwards, two for long
+    ones and for the unfused path; the flags force either; an SM budget keeps
+    the routing in three kernels."""
+    S = lib
+    dv2 = (2048, 1408, 64, 6)
+    short = S.MegaMoELayer(*dv2, max_rows=4096, fuse_fc1=True)
+    assert short.plan(4096) == dict(route_kernels=1, gemm_launches=1, swiglu_kernels=0, kernels=4)
+    assert short.plan(0)["kernels"] == 0
+    dv3 = (7168, 2048, 256, 8)
+    long_ = S.MegaMoELayer(*dv3, max_rows=1024, fuse_fc1=True, gemm="single")
+    assert long_.plan(8)["gemm_launches"] == 1          # decode, few tile rounds
+    assert long_.plan(1024)["gemm_launches"] == 2       # every expert touched
+    forced = S.MegaMoELayer(*dv3, max_rows=1024, fuse_fc1=True, gemm="single", gemms="one_launch")
+    assert forced.plan(1024)["gemm_launches"] == 1
+    split = S.MegaMoELayer(*dv2, max_rows=4096, fuse_fc1=True, gemms="split")
+    assert split.plan(4096)["gemm_launches"] == 2
+    unfused = S.MegaMoELayer(*dv2, max_rows=4096, fuse_fc1=False)
+    assert unfused.plan(4096) == dict(route_kernels=1, gemm_launches=2, swiglu_kernels=1, kernels=6)
+    short.set_sm_budget(64)
+    assert short.plan(4096)["route_kernels"] == 3
+
+
 def test_programmatic_launch_matches_serialised(lib, orc):
     """Profiling events between the kernels turn the programmatic-dependent
     launches back into plain stream order; the outputs are bit-identical."""

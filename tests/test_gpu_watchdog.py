@@ -17,7 +17,11 @@ from tests.test_gpu_parity import compare_outputs, small_problem
 pytestmark = pytest.mark.gpu
 
 
-def test_watchdog_expires_with_status_and_context_survives(orc):
+@pytest.mark.parametrize("split", [False, True])
+def test_watchdog_expires_with_status_and_context_survives(orc, split):
+    """split=False: the one-launch FC1 -> FC2 kernel, where the FC2 tiles of
+    the other CTAs also wait in vain for the m-tile counts that CTA 0 never
+    publishes, and expire on their own bound."""
     import __graft_entry__ as ge
     ge.build()
     import serving_route_gb300 as S
@@ -29,7 +33,8 @@ def test_watchdog_expires_with_status_and_context_survives(orc):
     q2, s2 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w2).cuda())
     xt, it, wt = gh.to_device(x, idx, w)
 
-    bad = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm="single", watchdog_test=True)
+    bad = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm="single", watchdog_test=True,
+                         gemms="split" if split else "one_launch")
     bad.bind_weights(q1, s1, q2, s2)
     bad.forward(xt, it, wt)
     st, bits = bad.read_status()
