@@ -55,6 +55,9 @@ def parse():
                    help="profiling only: the workload with this many tokens")
     p.add_argument("--gemms", default="auto", choices=["auto", "one_launch", "split"],
                    help="FC1 -> FC2 as one persistent launch, two launches, or chosen per forward")
+    p.add_argument("--side-mlp", type=int, default=0,
+                   help="measure the layer beside a shared-expert MLP of this intermediate size on "
+                        "another stream, per SM budget (prints that sweep instead of the bench line)")
     p.add_argument("--sm-budget", type=int, default=0,
                    help="cap the SMs the layer occupies (moe_set_sm_budget; 0: every SM)")
     p.add_argument("--no-graph", action="store_true")
@@ -233,6 +236,86 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def side_stream_sweep(args, torch, layer, x, idx, wts, wl, dev, flush):
+    """The layer on one stream and a shared-expert MLP on another, per SM budget
+    of the layer (moe_set_sm_budget), against the two run one after the other.
+    The MLP is the caller's other work, not part of the library: a dense BF16
+    SwiGLU FFN of intermediate size args.side_mlp over the same tokens, as
+    torch matmuls.  Direct launches, L2 flushed before every repetition,
+    median of the repetitions."""
+    n = args.side_mlp
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    wgu = (torch.randn(wl.H, 2 * n, device=dev, generator=gen) * wl.H ** -0.5).to(torch.bfloat16)
+    wd = (torch.randn(n, wl.H, device=dev, generator=gen) * n ** -0.5).to(torch.bfloat16)
+    main_s, side_s = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def mlp():
+        gu = x @ wgu
+        return (torch.nn.functional.silu(gu[:, :n]) * gu[:, n:]) @ wd
+
+    def layer_fwd():
+        layer.forward(x, idx, wts, stream=main_s)
+
+    def serial():
+        layer_fwd()
+        with torch.cuda.stream(main_s):
+            mlp()
+
+    def concurrent():
+        fork = torch.cuda.Event()
+        fork.record(main_s)
+        side_s.wait_event(fork)
+        with torch.cuda.stream(side_s):
+            mlp()
+        join = torch.cuda.Event()
+        join.record(side_s)
+        layer_fwd()
+        main_s.wait_event(join)
+
+    def timed(fn, reps=max(args.steps, 20), warm=max(args.warmup, 3)):
+        ts = []
+        for i in range(warm + reps):
+            flush.zero_()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(main_s)
+            fn()
+            b.record(main_s)
+            torch.cuda.synchronize()
+            if i >= warm:
+                ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def mlp_alone():
+        with torch.cuda.stream(main_s):
+            mlp()
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    layer_ms, mlp_ms, serial_ms = timed(layer_fwd), timed(mlp_alone), timed(serial)
+    points = []
+    for budget in [0] + [sms - d for d in (4, 8, 16, 24, 32, 48)]:
+        layer.set_sm_budget(budget)
+        points.append({"sm_budget": budget or sms, "ms": timed(concurrent),
+                       "layer_alone_ms": timed(layer_fwd)})
+    layer.set_sm_budget(0)
+    st, bits = layer.read_status(main_s)
+    if st != 0:
+        raise RuntimeError(f"forward reported device status {bits:#x}")
+    best = min(points, key=lambda p: p["ms"])
+    print(json.dumps({
+        "metric": "layer + side-stream shared-expert MLP, ms per step (lower is better)",
+        "unit": "ms", "higher_is_better": False, "n_gpus": 1, "data": "synthetic",
+        "config": {"workload": wl.name, "side_mlp_inter": n, "side_mlp": "BF16 SwiGLU FFN, torch matmuls",
+                   "launch": "direct launches", "l2": "flushed before every repetition",
+                   "gemm": ("cta pairs" if layer.tactic()["gemm_pair"] else "single cta")},
+        "layer_ms": layer_ms, "mlp_ms": mlp_ms, "serial_ms": serial_ms,
+        "concurrent": points, "best": best,
+        "best_vs_serial": best["ms"] / serial_ms,
+        "all_sms_vs_serial": points[0]["ms"] / serial_ms}))
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -307,6 +390,9 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
+    if args.side_mlp:
+        side_stream_sweep(args, torch, layer, x, idx, wts, wl, dev, flush)
+        return
     if args.sm_budget:
         layer.set_sm_budget(args.sm_budget)
     dbg = layer.tactic()

@@ -265,9 +265,12 @@ MOE_API moe_status moe_set_profile_events(moe_handle* h, void* const* events, in
  * MLP on a side stream run at the same time).  max_sms = 0 restores the
  * default (every SM).  Otherwise 2 <= max_sms: the persistent GEMMs launch
  * min(max_sms, SM count) CTAs (one per SM; rounded down to an even count for
- * CTA pairs) and the streaming kernels (quantisation, combine) at most
- * max_sms CTAs.  Results are bit-identical for every budget.  Errors:
- * MOE_ERR_INVALID_ARG for a NULL handle or max_sms < 0 or == 1.
+ * CTA pairs) and the routing keeps to its three small kernels (no
+ * cooperative grid).  The short streaming kernels (quantisation, combine)
+ * keep their full grids: their CTAs cannot be pinned to a subset of SMs, and
+ * a grid of one CTA per budgeted SM made them several times slower.  Results
+ * are bit-identical for every budget.  Errors: MOE_ERR_INVALID_ARG for a NULL
+ * handle or max_sms < 0 or == 1.
  */
 MOE_API moe_status moe_set_sm_budget(moe_handle* h, int32_t max_sms);
 

@@ -424,7 +424,10 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   // unless profiling events sit between them.
   const bool pdl = ev == nullptr;
   // streaming kernels: up to 16 CTAs per SM, or one per SM of the budget
-  const int stream_ctas = h->sm_budget > 0 ? budget_sms(h) : 16 * h->num_sms;
+  // Streaming kernels keep their full grids under an SM budget: their CTAs
+  // cannot be confined to a subset of SMs, and one CTA per budgeted SM
+  // starves them of memory parallelism.  The budget caps the persistent GEMM.
+  const int stream_ctas = 16 * h->num_sms;
   if (launch_quant_dispatch(ws, L, d_x, num_tokens, s, pdl, stream_ctas) != cudaSuccess)
     return MOE_ERR_CUDA;
 
