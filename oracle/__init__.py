@@ -9,9 +9,14 @@ The arithmetic lives in ``oracle.c`` (plain C, float64; see its header for
 the definition followed, step by step, with citations).  This module only
 marshals numpy arrays through ctypes.
 
+Formats: ``fmt=0`` is the DeepSeek layout (1x128 activation, 128x128 weight
+scales); ``fmt=1`` is MXFP8 (one scale per 32 elements along K, for
+activations and for every weight row).
+
 Parity status per function (pins live in ``tests/test_oracle_*.py``):
-  e4m3 encode/decode, bf16 rounding, pow2 scale rule, 1x128 / 128x128
-  quantisation, routing, FC1/FC2 block-scaled products, combine: pinned.
+  e4m3 encode/decode, bf16 rounding, pow2 scale rule, 1x128 / 128x128 and
+  MXFP8 1x32 quantisation, routing, FC1/FC2 block-scaled products in both
+  formats, combine: pinned.
   SwiGLU's exp: parity unpinned at the ulp level (host ``exp`` versus the
   GPU's ``expf``); covered by tolerance only.
   Combine summation order: parity unpinned at the ulp level (float64 here,
@@ -56,14 +61,20 @@ def lib():
         L.or_swiglu.argtypes = [ctypes.c_uint16, ctypes.c_uint16]
         L.or_swiglu.restype = ctypes.c_float
         L.or_quant_rows.argtypes = [vp, i64, i64, vp, vp]
+        L.or_quant_rows_bw.argtypes = [vp, i64, i64, i32, vp, vp]
         L.or_quant_rows_bf16.argtypes = [vp, i64, i64, vp, vp]
+        L.or_quant_rows_bf16_bw.argtypes = [vp, i64, i64, i32, vp, vp]
         L.or_quant_weights.argtypes = [vp, i64, i64, i64, vp, vp]
+        L.or_quant_weights_mx.argtypes = [vp, i64, i64, i64, vp, vp]
         L.or_route.argtypes = [i64, i32, i32, vp, vp, i32, vp, vp, vp, vp]
         L.or_route.restype = ctypes.c_uint32
         L.or_expert_ffn.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.or_expert_ffn_fmt.argtypes = [i32] + L.or_expert_ffn.argtypes
         L.or_combine.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp]
         L.or_forward.argtypes = [i64, i32, i32, i32, i32, i32] + [vp] * 7 + [vp] * 13
         L.or_forward.restype = ctypes.c_uint32
+        L.or_forward_fmt.argtypes = [i32] + L.or_forward.argtypes
+        L.or_forward_fmt.restype = ctypes.c_uint32
         _lib = L
     return _lib
 
@@ -102,22 +113,23 @@ def swiglu(g_bits: int, u_bits: int) -> float:
 # --------------------------------------------------------------------------
 # quantisation
 # --------------------------------------------------------------------------
-def quant_rows(v: np.ndarray):
-    """1x128 quantisation of float64 rows -> (q uint8, s float32 [rows, cols/128])."""
+def quant_rows(v: np.ndarray, block: int = 128):
+    """1 x block quantisation of float64 rows (block 128, or 32 for MXFP8)
+    -> (q uint8, s float32 [rows, cols/block])."""
     v = np.ascontiguousarray(v, dtype=np.float64)
     rows, cols = v.shape
     q = np.empty((rows, cols), np.uint8)
-    s = np.empty((rows, cols // 128), np.float32)
-    lib().or_quant_rows(_p(v), rows, cols, _p(q), _p(s))
+    s = np.empty((rows, cols // block), np.float32)
+    lib().or_quant_rows_bw(_p(v), rows, cols, block, _p(q), _p(s))
     return q, s
 
 
-def quant_rows_bf16(x_bits: np.ndarray):
+def quant_rows_bf16(x_bits: np.ndarray, block: int = 128):
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     rows, cols = x.shape
     q = np.empty((rows, cols), np.uint8)
-    s = np.empty((rows, cols // 128), np.float32)
-    lib().or_quant_rows_bf16(_p(x), rows, cols, _p(q), _p(s))
+    s = np.empty((rows, cols // block), np.float32)
+    lib().or_quant_rows_bf16_bw(_p(x), rows, cols, block, _p(q), _p(s))
     return q, s
 
 
@@ -128,6 +140,17 @@ def quant_weights(w: np.ndarray):
     q = np.empty(w.shape, np.uint8)
     s = np.empty((nmat, rows // 128, cols // 128), np.float32)
     lib().or_quant_weights(_p(w), nmat, rows, cols, _p(q), _p(s))
+    return q, s
+
+
+def quant_weights_mx(w: np.ndarray):
+    """MXFP8 quantisation of float32 [nmat, rows, cols]: every row 1x32 along
+    the columns -> (q uint8, s float32 [nmat, rows, cols/32])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    nmat, rows, cols = w.shape
+    q = np.empty(w.shape, np.uint8)
+    s = np.empty((nmat, rows, cols // 32), np.float32)
+    lib().or_quant_weights_mx(_p(w), nmat, rows, cols, _p(q), _p(s))
     return q, s
 
 
@@ -148,16 +171,18 @@ def route(idx: np.ndarray, w: np.ndarray, E: int, check: bool = True):
     return dict(err=int(err), counts=counts, offsets=offsets, perm=perm[:R], inv=inv[:T * K])
 
 
-def expert_ffn(H, I, E, offsets, A, As, W1, W1s, W2, W2s, sel=None):
+def expert_ffn(H, I, E, offsets, A, As, W1, W1s, W2, W2s, sel=None, fmt=0):
     R = int(offsets[E])
     n = max(R, 1)
+    bw = 32 if fmt == 1 else 128
     gu = np.zeros((n, 2 * I), np.uint16)
     hq = np.zeros((n, I), np.uint8)
-    hs = np.zeros((n, I // 128), np.float32)
+    hs = np.zeros((n, I // bw), np.float32)
     y = np.zeros((n, H), np.uint16)
     args = [np.ascontiguousarray(a) for a in (offsets, A, As, W1, W1s, W2, W2s)]
     sel_a = None if sel is None else np.ascontiguousarray(sel, dtype=np.uint8)
-    lib().or_expert_ffn(H, I, E, *[_p(a) for a in args], _p(sel_a), _p(gu), _p(hq), _p(hs), _p(y))
+    lib().or_expert_ffn_fmt(fmt, H, I, E, *[_p(a) for a in args], _p(sel_a), _p(gu), _p(hq), _p(hs),
+                            _p(y))
     return gu[:R], hq[:R], hs[:R], y[:R]
 
 
@@ -171,9 +196,10 @@ def combine(inv, w, y, T, K, H, tok_sel=None):
     return out
 
 
-def forward(x_bits, idx, w, W1, W1s, W2, W2s, check=True, tok_sel=None):
+def forward(x_bits, idx, w, W1, W1s, W2, W2s, check=True, tok_sel=None, fmt=0):
     """Whole layer.  Returns a dict with every intermediate (sorted-position
-    arrays cover the R active routes) and ``out`` (bf16 bits [T, H])."""
+    arrays cover the R active routes) and ``out`` (bf16 bits [T, H]).
+    fmt=1: MXFP8 (W1s [E, 2I, H/32], W2s [E, H, I/32]; 1x32 activations)."""
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     w = np.ascontiguousarray(w, dtype=np.float32)
@@ -186,18 +212,20 @@ def forward(x_bits, idx, w, W1, W1s, W2, W2s, check=True, tok_sel=None):
     offsets = np.empty(E + 1, np.int32)
     perm = np.full(RK, -1, np.int32)
     inv = np.empty(RK, np.int32)
+    bw = 32 if fmt == 1 else 128
     xq = np.empty((T, H), np.uint8)
-    xs = np.empty((T, H // 128), np.float32)
+    xs = np.empty((T, H // bw), np.float32)
     A = np.zeros((RK, H), np.uint8)
-    As = np.zeros((RK, H // 128), np.float32)
+    As = np.zeros((RK, H // bw), np.float32)
     gu = np.zeros((RK, 2 * I), np.uint16)
     hq = np.zeros((RK, I), np.uint8)
-    hs = np.zeros((RK, I // 128), np.float32)
+    hs = np.zeros((RK, I // bw), np.float32)
     y = np.zeros((RK, H), np.uint16)
     out = np.zeros((T, H), np.uint16)
     ins = [np.ascontiguousarray(a) for a in (W1, W1s, W2, W2s)]
     ts = None if tok_sel is None else np.ascontiguousarray(tok_sel, dtype=np.uint8)
-    err = lib().or_forward(T, H, I, E, K, int(check), _p(x), _p(idx), _p(w), *[_p(a) for a in ins],
+    err = lib().or_forward_fmt(fmt, T, H, I, E, K, int(check), _p(x), _p(idx), _p(w),
+                               *[_p(a) for a in ins],
                            _p(ts), _p(counts), _p(offsets), _p(perm), _p(inv), _p(xq), _p(xs),
                            _p(A), _p(As), _p(gu), _p(hq), _p(hs), _p(y), _p(out))
     R = int(offsets[E]) if err == 0 else 0

@@ -37,6 +37,13 @@
  * one BF16 rounding.  Because block sums are exact, the compiler may evaluate
  * them in any order (the simd pragma); no result changes.
  *
+ * Format 1 (MXFP8, "32e4m3xe8m0" on flashinfer PR #4688 and the SM100 MXFP8
+ * megakernels of PR #4069's kernel drops): E4M3 values with one power-of-two
+ * scale per 32 consecutive elements along K -- activations 1x32 (steps 2 and
+ * 6), each weight row 1x32 -- with the same scale rule per 32-block.  Steps
+ * 4 and 7 then sum 32-wide exact block sums, each times its activation and
+ * weight-row scales.  Format 0 is the DeepSeek 1x128 / 128x128 layout above.
+ *
  * Readings where the pages are silent (listed with their reasons in the
  * design notes): E4M3 is the OCP E4M3FN variant (max 448, NaN 0x7F/0xFF, no
  * infinity); scales are powers of two; gate/up are rounded to BF16 before
@@ -151,28 +158,38 @@ int or_pow2_scale_exp(double amax) {
  * 1x128 quantisation of rows, and 128x128 quantisation of weight matrices.
  * ------------------------------------------------------------------------- */
 
-/* v [rows, cols] (cols % 128 == 0) -> q [rows, cols], s [rows, cols/128] */
-void or_quant_rows(const double* v, int64_t rows, int64_t cols, uint8_t* q, float* s) {
-  int64_t nb = cols / 128;
+/* v [rows, cols] (cols % bw == 0) -> q [rows, cols], s [rows, cols/bw]: one
+ * scale per row and bw-wide block (bw = 128: 1x128; bw = 32: MXFP8 1x32) */
+void or_quant_rows_bw(const double* v, int64_t rows, int64_t cols, int bw, uint8_t* q, float* s) {
+  int64_t nb = cols / bw;
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r) {
     for (int64_t b = 0; b < nb; ++b) {
-      const double* src = v + r * cols + b * 128;
+      const double* src = v + r * cols + b * bw;
       double amax = 0.0;
-      for (int j = 0; j < 128; ++j) amax = fmax(amax, fabs(src[j]));
+      for (int j = 0; j < bw; ++j) amax = fmax(amax, fabs(src[j]));
       int e = or_pow2_scale_exp(amax);
-      for (int j = 0; j < 128; ++j) q[r * cols + b * 128 + j] = or_e4m3_encode(ldexp(src[j], -e));
+      for (int j = 0; j < bw; ++j) q[r * cols + b * bw + j] = or_e4m3_encode(ldexp(src[j], -e));
       s[r * nb + b] = (float)ldexp(1.0, e);
     }
   }
 }
 
-/* bf16 rows -> 1x128 quantisation */
-void or_quant_rows_bf16(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* q, float* s) {
+void or_quant_rows(const double* v, int64_t rows, int64_t cols, uint8_t* q, float* s) {
+  or_quant_rows_bw(v, rows, cols, 128, q, s);
+}
+
+/* bf16 rows -> 1 x bw quantisation */
+void or_quant_rows_bf16_bw(const uint16_t* x, int64_t rows, int64_t cols, int bw, uint8_t* q,
+                           float* s) {
   double* v = (double*)malloc(sizeof(double) * (size_t)(rows * cols));
   for (int64_t i = 0; i < rows * cols; ++i) v[i] = or_bf16_decode(x[i]);
-  or_quant_rows(v, rows, cols, q, s);
+  or_quant_rows_bw(v, rows, cols, bw, q, s);
   free(v);
+}
+
+void or_quant_rows_bf16(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* q, float* s) {
+  or_quant_rows_bf16_bw(x, rows, cols, 128, q, s);
 }
 
 /* w [nmat, rows, cols] float -> q (same shape), s [nmat, rows/128, cols/128] */
@@ -197,6 +214,18 @@ void or_quant_weights(const float* w, int64_t nmat, int64_t rows, int64_t cols, 
       }
     }
   }
+}
+
+/* MXFP8 weights: w [nmat, rows, cols] float -> q, s [nmat, rows, cols/32]:
+ * every row quantised 1x32 along K */
+void or_quant_weights_mx(const float* w, int64_t nmat, int64_t rows, int64_t cols, uint8_t* q,
+                         float* s) {
+  double* v = (double*)malloc(sizeof(double) * (size_t)(rows * cols));
+  for (int64_t m = 0; m < nmat; ++m) {
+    for (int64_t i = 0; i < rows * cols; ++i) v[i] = (double)w[m * rows * cols + i];
+    or_quant_rows_bw(v, rows, cols, 32, q + m * rows * cols, s + m * rows * (cols / 32));
+  }
+  free(v);
 }
 
 /* ---------------------------------------------------------------------------
@@ -244,22 +273,27 @@ uint32_t or_route(int64_t T, int K, int E, const int32_t* idx, const float* w, i
 }
 
 /* ---------------------------------------------------------------------------
- * One FP8 block-scaled row-times-matrix product: for row a (len K, scales
- * as[K/128]) and matrix W [N, K] with block scales ws [N/128, K/128],
- * out[n] = BF16( sum_kb blocksum(kb) * as[kb] * ws[n/128, kb] ).
+ * One FP8 block-scaled row-times-matrix product.
+ * Format 0: row a (len K, scales as[K/128]), matrix W [N, K] with block
+ *   scales ws [N/128, K/128]:
+ *   out[n] = BF16( sum_kb blocksum_128(kb) * as[kb] * ws[n/128, kb] ).
+ * Format 1 (MXFP8): scales as[K/32] and ws [N, K/32]:
+ *   out[n] = BF16( sum_b blocksum_32(b) * as[b] * ws[n, b] ).
  * ------------------------------------------------------------------------- */
-static void fp8_row_matmul(const double* a, const float* as, const double* Wd, const float* ws,
-                           int64_t N, int64_t Kd, uint16_t* out) {
-  int64_t kbn = Kd / 128;
+static void fp8_row_matmul(int fmt, const double* a, const float* as, const double* Wd,
+                           const float* ws, int64_t N, int64_t Kd, uint16_t* out) {
+  const int bw = fmt == 1 ? 32 : 128;
+  const int64_t nb = Kd / bw;
   for (int64_t n = 0; n < N; ++n) {
     double acc = 0.0;
-    for (int64_t kb = 0; kb < kbn; ++kb) {
-      const double* ar = a + kb * 128;
-      const double* wr = Wd + n * Kd + kb * 128;
+    for (int64_t b = 0; b < nb; ++b) {
+      const double* ar = a + b * bw;
+      const double* wr = Wd + n * Kd + b * bw;
       double bs = 0.0;
 #pragma omp simd reduction(+ : bs)
-      for (int j = 0; j < 128; ++j) bs += ar[j] * wr[j];
-      acc += bs * (double)as[kb] * (double)ws[(n / 128) * kbn + kb];
+      for (int j = 0; j < bw; ++j) bs += ar[j] * wr[j];
+      const double wsc = fmt == 1 ? (double)ws[n * nb + b] : (double)ws[(n / 128) * nb + b];
+      acc += bs * (double)as[b] * wsc;
     }
     out[n] = or_bf16_round(acc);
   }
@@ -282,10 +316,15 @@ float or_swiglu(uint16_t g_bits, uint16_t u_bits) {
  * Positions are processed expert by expert so each expert's weights are
  * decoded once.  `sel` (nullable) marks which positions to compute.
  * ------------------------------------------------------------------------- */
-void or_expert_ffn(int H, int I, int E, const int32_t* offsets, const uint8_t* A, const float* As,
-                   const uint8_t* W1, const float* W1s, const uint8_t* W2, const float* W2s,
-                   const uint8_t* sel, uint16_t* gu, uint8_t* hq, float* hs, uint16_t* y) {
-  const int64_t HB = H / 128, IB = I / 128;
+void or_expert_ffn_fmt(int fmt, int H, int I, int E, const int32_t* offsets, const uint8_t* A,
+                       const float* As, const uint8_t* W1, const float* W1s, const uint8_t* W2,
+                       const float* W2s, const uint8_t* sel, uint16_t* gu, uint8_t* hq, float* hs,
+                       uint16_t* y) {
+  const int bw = fmt == 1 ? 32 : 128;
+  const int64_t HB = H / bw, IB = I / bw;  /* activation scales per row */
+  /* weight scales per expert: [2I/128][H/128] and [H/128][I/128], or per row [2I][H/32], [H][I/32] */
+  const int64_t w1s_per_e = fmt == 1 ? (int64_t)2 * I * HB : (int64_t)(2 * I / 128) * HB;
+  const int64_t w2s_per_e = fmt == 1 ? (int64_t)H * IB : (int64_t)(H / 128) * IB;
   double* w1d = (double*)malloc(sizeof(double) * (size_t)(2 * I) * (size_t)H);
   double* w2d = (double*)malloc(sizeof(double) * (size_t)H * (size_t)I);
   for (int e = 0; e < E; ++e) {
@@ -296,8 +335,8 @@ void or_expert_ffn(int H, int I, int E, const int32_t* offsets, const uint8_t* A
     if (!any) continue;
     decode_e4m3_array(W1 + (int64_t)e * 2 * I * H, (int64_t)2 * I * H, w1d);
     decode_e4m3_array(W2 + (int64_t)e * H * I, (int64_t)H * I, w2d);
-    const float* w1s = W1s + (int64_t)e * (2 * I / 128) * HB;
-    const float* w2s = W2s + (int64_t)e * (H / 128) * IB;
+    const float* w1s = W1s + (int64_t)e * w1s_per_e;
+    const float* w2s = W2s + (int64_t)e * w2s_per_e;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t p = p0; p < p1; ++p) {
       if (sel && !sel[p]) continue;
@@ -306,11 +345,11 @@ void or_expert_ffn(int H, int I, int E, const int32_t* offsets, const uint8_t* A
       double* hd = (double*)malloc(sizeof(double) * (size_t)I);
       uint16_t* gup = gu + p * 2 * I;
       decode_e4m3_array(A + p * H, H, a);
-      fp8_row_matmul(a, As + p * HB, w1d, w1s, 2 * I, H, gup);
+      fp8_row_matmul(fmt, a, As + p * HB, w1d, w1s, 2 * I, H, gup);
       for (int n = 0; n < I; ++n) h[n] = (double)or_swiglu(gup[n], gup[I + n]);
-      or_quant_rows(h, 1, I, hq + p * I, hs + p * IB);
+      or_quant_rows_bw(h, 1, I, bw, hq + p * I, hs + p * IB);
       decode_e4m3_array(hq + p * I, I, hd);
-      fp8_row_matmul(hd, hs + p * IB, w2d, w2s, H, I, y + p * H);
+      fp8_row_matmul(fmt, hd, hs + p * IB, w2d, w2s, H, I, y + p * H);
       free(a);
       free(h);
       free(hd);
@@ -318,6 +357,12 @@ void or_expert_ffn(int H, int I, int E, const int32_t* offsets, const uint8_t* A
   }
   free(w1d);
   free(w2d);
+}
+
+void or_expert_ffn(int H, int I, int E, const int32_t* offsets, const uint8_t* A, const float* As,
+                   const uint8_t* W1, const float* W1s, const uint8_t* W2, const float* W2s,
+                   const uint8_t* sel, uint16_t* gu, uint8_t* hq, float* hs, uint16_t* y) {
+  or_expert_ffn_fmt(0, H, I, E, offsets, A, As, W1, W1s, W2, W2s, sel, gu, hq, hs, y);
 }
 
 /* combine: out[t, c] = BF16( sum_k active  w[t,k] * y[inv[t*K+k], c] ) */
@@ -344,16 +389,17 @@ void or_combine(int64_t T, int K, int H, const int32_t* inv, const float* w, con
  * combine to the selected tokens (routing always covers every token).
  * Returns the route error bits; on error nothing past routing is computed.
  * ------------------------------------------------------------------------- */
-uint32_t or_forward(int64_t T, int H, int I, int E, int K, int check, const uint16_t* x,
-                    const int32_t* idx, const float* w, const uint8_t* W1, const float* W1s,
-                    const uint8_t* W2, const float* W2s, const uint8_t* tok_sel,
-                    int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
-                    uint8_t* xq, float* xs, uint8_t* A, float* As, uint16_t* gu, uint8_t* hq,
-                    float* hs, uint16_t* y, uint16_t* out) {
+uint32_t or_forward_fmt(int fmt, int64_t T, int H, int I, int E, int K, int check,
+                        const uint16_t* x, const int32_t* idx, const float* w, const uint8_t* W1,
+                        const float* W1s, const uint8_t* W2, const float* W2s,
+                        const uint8_t* tok_sel, int32_t* counts, int32_t* offsets, int32_t* perm,
+                        int32_t* inv, uint8_t* xq, float* xs, uint8_t* A, float* As, uint16_t* gu,
+                        uint8_t* hq, float* hs, uint16_t* y, uint16_t* out) {
   uint32_t err = or_route(T, K, E, idx, w, check, counts, offsets, perm, inv);
   if (err) return err;
-  const int64_t R = offsets[E], HB = H / 128;
-  or_quant_rows_bf16(x, T, H, xq, xs);
+  const int bw = fmt == 1 ? 32 : 128;
+  const int64_t R = offsets[E], HB = H / bw;
+  or_quant_rows_bf16_bw(x, T, H, bw, xq, xs);
   uint8_t* sel = NULL;
   if (tok_sel) {
     sel = (uint8_t*)calloc((size_t)(R > 0 ? R : 1), 1);
@@ -364,8 +410,18 @@ uint32_t or_forward(int64_t T, int H, int I, int E, int K, int check, const uint
     memcpy(A + p * H, xq + t * H, (size_t)H);
     memcpy(As + p * HB, xs + t * HB, sizeof(float) * (size_t)HB);
   }
-  or_expert_ffn(H, I, E, offsets, A, As, W1, W1s, W2, W2s, sel, gu, hq, hs, y);
+  or_expert_ffn_fmt(fmt, H, I, E, offsets, A, As, W1, W1s, W2, W2s, sel, gu, hq, hs, y);
   or_combine(T, K, H, inv, w, y, tok_sel, out);
   free(sel);
   return 0;
+}
+
+uint32_t or_forward(int64_t T, int H, int I, int E, int K, int check, const uint16_t* x,
+                    const int32_t* idx, const float* w, const uint8_t* W1, const float* W1s,
+                    const uint8_t* W2, const float* W2s, const uint8_t* tok_sel,
+                    int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                    uint8_t* xq, float* xs, uint8_t* A, float* As, uint16_t* gu, uint8_t* hq,
+                    float* hs, uint16_t* y, uint16_t* out) {
+  return or_forward_fmt(0, T, H, I, E, K, check, x, idx, w, W1, W1s, W2, W2s, tok_sel, counts,
+                        offsets, perm, inv, xq, xs, A, As, gu, hq, hs, y, out);
 }
