@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--unfused", action="store_true", help="time the unfused reference path")
     p.add_argument("--gemm", default="auto", choices=["auto", "single", "pair"])
+    p.add_argument("--format", default="deepseek", choices=["deepseek", "mxfp8"],
+                   help="block scales: DeepSeek 1x128 / 128x128, or MXFP8 1x32 along K")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling only: the workload with this many experts (smaller weights)")
     p.add_argument("--tokens", type=int, default=0,
@@ -352,12 +354,15 @@ def main():
 
     layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, expected_m=wl.T,
                            fuse_fc1=fused, check_routes=True, gemm=args.gemm,
-                           gemms=args.gemms)
+                           gemms=args.gemms, fmt=args.format)
     # weights: generated and quantised on the GPU, bound once
+    mx = args.format == "mxfp8"
     w1q = torch.empty((wl.E, 2 * wl.I, wl.H), dtype=torch.uint8, device=dev)
-    w1s = torch.empty((wl.E, 2 * wl.I // 128, wl.H // 128), dtype=torch.float32, device=dev)
+    w1s = torch.empty((wl.E, 2 * wl.I, wl.H // 32) if mx else (wl.E, 2 * wl.I // 128, wl.H // 128),
+                      dtype=torch.float32, device=dev)
     w2q = torch.empty((wl.E, wl.H, wl.I), dtype=torch.uint8, device=dev)
-    w2s = torch.empty((wl.E, wl.H // 128, wl.I // 128), dtype=torch.float32, device=dev)
+    w2s = torch.empty((wl.E, wl.H, wl.I // 32) if mx else (wl.E, wl.H // 128, wl.I // 128),
+                      dtype=torch.float32, device=dev)
     chunk = 16
     with torch.cuda.stream(stream):
         for e0 in range(0, wl.E, chunk):
@@ -365,13 +370,13 @@ def main():
             f = torch.empty((ne, 2 * wl.I, wl.H), dtype=torch.float32, device=dev)
             g.dev_normal_f32(wl.seed, g.STREAM_W1, e0 * 2 * wl.I * wl.H, f.numel(),
                              g.weight_sigma(wl.H), f.data_ptr(), sp)
-            q, s = layer.quantize_weights(f, stream)
+            q, s = layer.quantize_weights(f, stream, fmt=args.format)
             w1q[e0:e0 + ne].copy_(q)
             w1s[e0:e0 + ne].copy_(s)
             f = torch.empty((ne, wl.H, wl.I), dtype=torch.float32, device=dev)
             g.dev_normal_f32(wl.seed, g.STREAM_W2, e0 * wl.H * wl.I, f.numel(),
                              g.weight_sigma(wl.I), f.data_ptr(), sp)
-            q, s = layer.quantize_weights(f, stream)
+            q, s = layer.quantize_weights(f, stream, fmt=args.format)
             w2q[e0:e0 + ne].copy_(q)
             w2s[e0:e0 + ne].copy_(s)
             del f, q, s
@@ -619,6 +624,8 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "K": wl.K,
                    "fc1_epilogue": "fused" if fused else "unfused",
+                   "format": ("MXFP8: E4M3, E8M0 scale per 32 along K" if args.format == "mxfp8"
+                              else "E4M3, 1x128 activation / 128x128 weight scales"),
                    "l2": "flushed before every step (256 MiB write, untimed)",
                    "launch": "cuda graph replay" if graph is not None else "direct launches",
                    "gemm": ("cta pairs" if dbg["gemm_pair"] else "single cta") + f" x{dbg['gemm_ctas']}",

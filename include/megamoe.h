@@ -96,6 +96,14 @@ typedef enum moe_status {
  * Forwards with profiling events (moe_set_profile_events) always use two. */
 #define MOE_FLAG_SPLIT_GEMMS 0x40u
 #define MOE_FLAG_GEMMS_ONE_LAUNCH 0x80u
+/* MXFP8 instead of the DeepSeek 1x128 / 128x128 scales: E4M3 values with one
+ * power-of-two (E8M0) scale per 32 consecutive elements along K -- for the
+ * activations (x and the re-quantised SwiGLU output, 1x32) and for every
+ * weight row (moe_quantize_weights_mx) -- same scale rule per 32-block
+ * ("32e4m3xe8m0" on flashinfer PR #4688; the SM100 MXFP8 megakernels of PR
+ * #4069).  The tensor core applies every scale (one per 32-wide MMA K step),
+ * so the GEMMs copy one scale atom per K block instead of one per four. */
+#define MOE_FLAG_MXFP8 0x100u
 
 typedef struct moe_dims {
   int32_t hidden;      /* H: multiple of 128, 128..16384 */
@@ -157,6 +165,22 @@ MOE_API moe_status moe_quantize_weights(const float* d_w, int64_t num_mats, int3
                                 uint8_t* d_q, float* d_scale, struct CUstream_st* stream);
 
 /*
+ * moe_quantize_weights_mx -- FP32 expert weights to the MXFP8 form that
+ * moe_bind_weights takes under MOE_FLAG_MXFP8: every row quantised in 1x32
+ * blocks along the columns (the K dimension of both GEMMs), scale = the
+ * smallest power of two >= amax/448 (1 for an all-zero block), codes = E4M3
+ * round-to-nearest-even of w/scale.
+ *   d_w     float [num_mats, rows, cols]; rows and cols multiples of 128.
+ *   d_q     uint8 [num_mats, rows, cols] (output).
+ *   d_scale float [num_mats, rows, cols/32] (output).
+ * Asynchronous on `stream`.  MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED as
+ * moe_quantize_weights.
+ */
+MOE_API moe_status moe_quantize_weights_mx(const float* d_w, int64_t num_mats, int32_t rows,
+                                           int32_t cols, uint8_t* d_q, float* d_scale,
+                                           struct CUstream_st* stream);
+
+/*
  * moe_bind_weights -- the layer holds its static weights in a transformed,
  * kernel-ready form that is built once, at set-up (flashinfer PR #4069,
  * "Contracts introduced by this PR": the stateful backend contract).  Copies
@@ -164,9 +188,10 @@ MOE_API moe_status moe_quantize_weights(const float* d_w, int64_t num_mats, int3
  * contiguous 16 KB box, W1's gate and up row blocks interleaved, and the
  * scales as E8M0 plus the GEMM's scale atoms):
  *   d_w1        E4M3 [E, 2I, H]: rows [0, I) gate, rows [I, 2I) up.
- *   d_w1_scale  float [E, 2I/128, H/128], powers of two.
+ *   d_w1_scale  float [E, 2I/128, H/128], powers of two
+ *               (MOE_FLAG_MXFP8: [E, 2I, H/32], one per row and 32 columns).
  *   d_w2        E4M3 [E, H, I].
- *   d_w2_scale  float [E, H/128, I/128], powers of two.
+ *   d_w2_scale  float [E, H/128, I/128], powers of two (MXFP8: [E, H, I/32]).
  * Enqueued on `stream`, then waits for that stream: the caller may free the
  * inputs when this returns.  Returns MOE_ERR_BAD_SCALE if any scale is not a
  * power of two within the E8M0 range.
@@ -227,14 +252,17 @@ typedef struct moe_debug_view {
   int32_t* inv_pad;        /* [T*K] padded GEMM row of route r, or -1 */
   uint8_t* a;              /* E4M3 gathered activations (padded rows), blocked: row r, column c at
                               ((r/128)*(H/128) + c/128)*16384 + (r%128)*128 + c%128 */
-  uint8_t* a_sf;           /* E8M0 scale atoms of a: [rows_alloc/128][ceil(H/512)][512] */
+  uint8_t* a_sf;           /* E8M0 scale atoms of a: [rows_alloc/128][ceil(H/512)][512]
+                              (MXFP8: [rows_alloc/128][H/128][512]) */
   uint16_t* gu;            /* [rows_alloc, 2I] BF16 gate||up (unfused or EMIT_FC1), else NULL */
   uint8_t* hq;             /* E4M3 re-quantised SwiGLU output, blocked like a (I columns) */
-  uint8_t* h_sf;           /* E8M0 scale atoms of hq: [rows_alloc/128][ceil(I/512)][512] */
+  uint8_t* h_sf;           /* E8M0 scale atoms of hq: [rows_alloc/128][ceil(I/512)][512]
+                              (MXFP8: [rows_alloc/128][I/128][512]) */
   uint16_t* y;             /* [rows_alloc, H] BF16 FC2 output per padded row */
   int64_t rows_alloc;      /* padded-row capacity (multiple of 128) */
-  int32_t sf_atom_bytes;   /* 512: 128 rows x 4 K blocks; the scale of row r, K block
-                              4q + j is byte (r%32)*16 + (r/32)*4 + j of atom q */
+  int32_t sf_atom_bytes;   /* 512: 128 rows x 4 scale units; the scale of row r, unit
+                              4q + j is byte (r%32)*16 + (r/32)*4 + j of atom q.  A unit
+                              is a 128-wide K block, or a 32-wide chunk under MXFP8 */
   int32_t gemm_pair;       /* 1: GEMMs run on CTA pairs (cta_group::2), 0: one CTA per SM */
   int32_t gemm_ctas;       /* grid size of the GEMM launches */
   int32_t pad_rows;        /* rows each expert's GEMM segment is padded to */

@@ -210,6 +210,7 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
   if (L->rows_alloc > ((int64_t)1 << 31) - 256) return MOE_ERR_INVALID_ARG;
   L->nb_max = (max_rows + 127) / 128;
   L->keep_gu = !(d->flags & MOE_FLAG_FUSE_FC1_EPILOGUE) || (d->flags & MOE_FLAG_EMIT_FC1);
+  L->mx = (d->flags & MOE_FLAG_MXFP8) != 0;
   const size_t H = L->H, I = L->I, E = L->E, R = L->rows_alloc, MB = R / 128;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -233,10 +234,10 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
   L->o_inv = take(4 * (size_t)rk);
   L->o_inv_pad = take(4 * (size_t)rk);
   L->o_a = take(R * H);
-  L->o_a_sf = take(MB * sf_kgroups(H / 128) * kSfAtomBytes);
+  L->o_a_sf = take(MB * atoms_along_k(H / 128, L->mx) * kSfAtomBytes);
   L->o_gu = L->keep_gu ? take(R * 2 * I * 2) : 0;
   L->o_hq = take(R * I);
-  L->o_h_sf = take(MB * sf_kgroups(I / 128) * kSfAtomBytes);
+  L->o_h_sf = take(MB * atoms_along_k(I / 128, L->mx) * kSfAtomBytes);
   L->o_y = take(R * H * 2);
   L->ws_bytes = o + kAlign;  // slack to align the caller's base
   o = 0;
@@ -244,8 +245,8 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
   L->o_w2 = take(E * H * I);
   L->o_w1_sf = take(E * (2 * I / 128) * (H / 128));
   L->o_w2_sf = take(E * (H / 128) * (I / 128));
-  L->o_w1_sfatoms = take(E * (2 * I / 128) * sf_kgroups(H / 128) * kSfAtomBytes);
-  L->o_w2_sfatoms = take(E * (H / 128) * sf_kgroups(I / 128) * kSfAtomBytes);
+  L->o_w1_sfatoms = take(E * (2 * I / 128) * atoms_along_k(H / 128, L->mx) * kSfAtomBytes);
+  L->o_w2_sfatoms = take(E * (H / 128) * atoms_along_k(I / 128, L->mx) * kSfAtomBytes);
   L->w_bytes = o + kAlign;
   return MOE_OK;
 }
@@ -326,12 +327,12 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   h->wst.w2_sfatoms = wb + L.o_w2_sfatoms;
   if (!encode_blocked_map(&h->tm_a, w.a, L.H / 128, (uint64_t)(L.rows_alloc / 128)) ||
       !encode_blocked_map(&h->tm_hq, w.hq, L.I / 128, (uint64_t)(L.rows_alloc / 128)) ||
-      !encode_atom_map(&h->tm_asf, w.a_sf, (uint64_t)(L.rows_alloc / 128) * sf_kgroups(L.H / 128)) ||
-      !encode_atom_map(&h->tm_hsf, w.h_sf, (uint64_t)(L.rows_alloc / 128) * sf_kgroups(L.I / 128)) ||
+      !encode_atom_map(&h->tm_asf, w.a_sf, (uint64_t)(L.rows_alloc / 128) * atoms_along_k(L.H / 128, L.mx)) ||
+      !encode_atom_map(&h->tm_hsf, w.h_sf, (uint64_t)(L.rows_alloc / 128) * atoms_along_k(L.I / 128, L.mx)) ||
       !encode_atom_map(&h->tm_w1sf, h->wst.w1_sfatoms,
-                       (uint64_t)L.E * (2 * L.I / 128) * sf_kgroups(L.H / 128)) ||
+                       (uint64_t)L.E * (2 * L.I / 128) * atoms_along_k(L.H / 128, L.mx)) ||
       !encode_atom_map(&h->tm_w2sf, h->wst.w2_sfatoms,
-                       (uint64_t)L.E * (L.H / 128) * sf_kgroups(L.I / 128)) ||
+                       (uint64_t)L.E * (L.H / 128) * atoms_along_k(L.I / 128, L.mx)) ||
       !encode_bf16_store_map(&h->tm_y, w.y, L.H, L.rows_alloc)) {
     delete h;
     return MOE_ERR_CUDA;
@@ -354,6 +355,17 @@ moe_status moe_quantize_weights(const float* d_w, int64_t num_mats, int32_t rows
   if (reinterpret_cast<uintptr_t>(d_w) % 16 || reinterpret_cast<uintptr_t>(d_q) % 16)
     return MOE_ERR_INVALID_ARG;
   if (launch_quantize_weights(d_w, num_mats, rows, cols, d_q, d_scale, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_quantize_weights_mx(const float* d_w, int64_t num_mats, int32_t rows, int32_t cols,
+                                   uint8_t* d_q, float* d_scale, struct CUstream_st* stream) {
+  if (!d_w || !d_q || !d_scale || num_mats < 0 || rows <= 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+  if (rows % 128 || cols % 128) return MOE_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(d_w) % 16 || reinterpret_cast<uintptr_t>(d_q) % 16)
+    return MOE_ERR_INVALID_ARG;
+  if (launch_quantize_weights_mx(d_w, num_mats, rows, cols, d_q, d_scale, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -438,7 +450,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g1.mtile_expert = ws.mtile_expert;
   g1.total_mtiles = ws.total_mtiles;
   g1.KB = L.H / 128;
-  g1.KQ = (int)sf_kgroups(g1.KB);
+  g1.KQ = (int)atoms_along_k(g1.KB, L.mx);
+  g1.mx = L.mx ? 1 : 0;
   g1.NT = L.I / 128;  // 256-wide tiles over 2I
   g1.N = 2 * L.I;
   g1.NB = 2 * L.I / 128;
@@ -470,7 +483,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.mtile_expert = ws.mtile_expert;
   g2.total_mtiles = ws.total_mtiles;
   g2.KB = L.I / 128;
-  g2.KQ = (int)sf_kgroups(g2.KB);
+  g2.KQ = (int)atoms_along_k(g2.KB, L.mx);
+  g2.mx = L.mx ? 1 : 0;
   g2.NT = (L.H + 255) / 256;
   g2.N = L.H;
   g2.NB = L.H / 128;

@@ -270,8 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) {
           const uint32_t sst = sbase + stage * C::kStageBytes;
-          const bool atoms = (kb & 3) == 0;
-          const int q = kb >> 2;
+          // scale atoms: every fourth K block, or every K block under MXFP8
+          const bool atoms = g.mx || (kb & 3) == 0;
+          const int q = g.mx ? kb : kb >> 2;
           if constexpr (PAIR) {
             // Both CTAs' bytes complete on the leader's full barrier; only the
             // leader arrives (expecting both shares), so the peer's copies
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t st = sbase + stage * C::kStageBytes;
           const uint32_t j = (uint32_t)kb & 3u;
-          if (j == 0) {
+          if (g.mx || j == 0) {
             sf = tmem + kColSf + (group & 3u) * kSfSlotCols;
             ++group;
             if constexpr (PAIR) {
@@ -376,12 +377,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_cp_sf_atom(sf + 12, sdesc_sf_atom(st + C::kOffSfb + 512));
             }
           }
-          const uint32_t idesc = idesc0 | (j << 4) | (j << 29);  // scale byte j of each word
           const uint64_t ad = sdesc_k_sw128(st + C::kOffA);
           const uint64_t bd = sdesc_k_sw128(st + C::kOffB);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+            // scale byte of each TMEM scale word: K block j of the group, or
+            // under MXFP8 the 32-wide chunk k of this K block
+            const uint32_t sb = g.mx ? (uint32_t)k : j;
+            const uint32_t idesc = idesc0 | (sb << 4) | (sb << 29);
             // +32 bytes along K inside the 128-byte swizzle atom = +2 in the address field
             if constexpr (PAIR)
               tc_mma_mxf8_pair(tmem, ad + 2 * k, bd + 2 * k, idesc, sf, sf + 8, acc);
@@ -536,7 +540,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                        pk[32 + 8 * v + 6], pk[32 + 8 * v + 7]);
         }
       }
-      if (em_fused) {
+      if (em_fused && g.mx) {
+        // MXFP8: this thread's 64 h columns are two whole 32-wide chunks of
+        // its row, so each gets its scale without any exchange
+        float h[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          h[2 * i] = swiglu(bf16_bits_to_float(pk[i] & 0xFFFFu),
+                            bf16_bits_to_float(pk[32 + i] & 0xFFFFu));
+          h[2 * i + 1] = swiglu(bf16_bits_to_float(pk[i] >> 16), bf16_bits_to_float(pk[32 + i] >> 16));
+        }
+        uint8_t* dq = g.hq + blocked_offset(row, (int64_t)nt * 128 + half * 64, g.inter);
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[32 * v + i]));
+          const int e = pow2_scale_exp(amax);
+          const float inv = pow2_neg(e);
+          uint32_t w[8];
+#pragma unroll
+          for (int uu = 0; uu < 8; ++uu) {
+            const int jx = 32 * v + 4 * uu;
+            w[uu] = e4m3x4(h[jx] * inv, h[jx + 1] * inv, h[jx + 2] * inv, h[jx + 3] * inv);
+          }
+          st_global_v8(dq + 32 * v, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+          g.h_sf[sf_atom_offset(row, 4 * nt + 2 * half + v, 4 * g.IB)] = (uint8_t)(e + 127);
+        }
+      } else if (em_fused) {
         // gate pairs pk[0..31], up pairs pk[32..63] -> h[0..63]
         float h[64];
         float amax = 0.f;

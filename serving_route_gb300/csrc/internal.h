@@ -46,6 +46,7 @@ struct WeightStore {
 
 struct Layout {
   int H, I, E, K;
+  bool mx;             // MXFP8: one scale per 32-wide K chunk (else 1x128 / 128x128)
   int pad_rows;        // expert segments padded to this many rows (128, or 256 for CTA pairs)
   bool pair;           // GEMMs run on CTA pairs (tcgen05 cta_group::2)
   int64_t max_rows;
@@ -60,6 +61,10 @@ struct Layout {
       o_base_p, o_perm, o_inv, o_inv_pad, o_a, o_a_sf, o_gu, o_hq, o_h_sf, o_y;
   size_t o_w1, o_w2, o_w1_sf, o_w2_sf, o_w1_sfatoms, o_w2_sfatoms;
 };
+
+// Scale atoms along K: one per four 128-wide K blocks (one byte per block),
+// or under MXFP8 one per K block (one byte per 32-wide chunk).
+inline int64_t atoms_along_k(int64_t kblocks, bool mx) { return mx ? kblocks : (kblocks + 3) >> 2; }
 
 // layout.cpp-style pure host arithmetic (api.cu)
 moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_rows,
@@ -86,6 +91,8 @@ cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int max_ct
                                 bool pdl);
 cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
                                     float* scale, cudaStream_t s);
+cudaError_t launch_quantize_weights_mx(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
+                                       float* scale, cudaStream_t s);
 cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const uint8_t* w1,
                                   const float* w1s, const uint8_t* w2, const float* w2s,
                                   uint32_t* status, cudaStream_t s);
@@ -101,7 +108,8 @@ struct GemmArgs {
   const int32_t* mtile_expert;
   const int32_t* total_mtiles;
   int KB;                      // K / 128
-  int KQ;                      // groups of four K blocks (one scale atom each)
+  int KQ;                      // scale atoms along K (atoms_along_k)
+  int mx;                      // MXFP8: an atom per K block, MMA k uses byte k
   int NT;                      // 256-wide N tiles per expert
   int N;                       // B rows per expert
   int NB;                      // N / 128

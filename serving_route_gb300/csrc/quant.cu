@@ -54,6 +54,8 @@ __device__ __forceinline__ float group8_max(float v) {
   return v;
 }
 
+// MX: MXFP8, one scale per 32 columns (a lane pair) instead of per 128.
+template <bool MX>
 __device__ __forceinline__ void quant_dispatch_unit(const uint4 (&raw)[2], bool valid, int p_lane,
                                                     int b, int H, int K, int l8,
                                                     uint8_t* __restrict__ a,
@@ -75,7 +77,7 @@ __device__ __forceinline__ void quant_dispatch_unit(const uint4 (&raw)[2], bool 
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  amax = group8_max(amax);
+  amax = MX ? fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1)) : group8_max(amax);
   const int e = pow2_scale_exp(amax);
   const float inv = pow2_neg(e);
   uint4 q;
@@ -88,11 +90,17 @@ __device__ __forceinline__ void quant_dispatch_unit(const uint4 (&raw)[2], bool 
     const int p = __shfl_sync(0xFFFFFFFFu, p_lane, k);
     if (p >= 0 && valid) {
       *reinterpret_cast<uint4*>(a + blocked_offset(p, b * 128 + l8 * 16, H)) = q;
-      if (l8 == 0) a_sf[sf_atom_offset(p, b, KB)] = (uint8_t)(e + 127);
+      if (MX) {
+        // scale unit = 32-wide chunk 4b + l8/2 of the row
+        if ((l8 & 1) == 0) a_sf[sf_atom_offset(p, 4 * b + (l8 >> 1), 4 * KB)] = (uint8_t)(e + 127);
+      } else if (l8 == 0) {
+        a_sf[sf_atom_offset(p, b, KB)] = (uint8_t)(e + 127);
+      }
     }
   }
 }
 
+template <bool MX>
 __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pad, int64_t T, int H, int K,
     uint8_t* __restrict__ a, uint8_t* __restrict__ a_sf) {
@@ -121,13 +129,15 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     }
     const int p0 = (lane < K) ? inv_pad[t0 * K + lane] : -1;
     const int p1 = (lane < K && has1) ? inv_pad[t1 * K + lane] : -1;
-    quant_dispatch_unit(r0, v0, p0, b0, H, K, l8, a, a_sf);
-    quant_dispatch_unit(r1, v1, p1, b1, H, K, l8, a, a_sf);
+    quant_dispatch_unit<MX>(r0, v0, p0, b0, H, K, l8, a, a_sf);
+    quant_dispatch_unit<MX>(r1, v1, p1, b1, H, K, l8, a, a_sf);
   }
   pdl_trigger();
 }
 
-// Unfused SwiGLU + re-quantisation over the padded GEMM rows of this forward.
+// Unfused SwiGLU + re-quantisation over the padded GEMM rows of this forward
+// (MX: one scale per 32 columns, four lanes, instead of per 128).
+template <bool MX>
 __global__ void __launch_bounds__(256) swiglu_quant_kernel(
     const uint16_t* __restrict__ gu, const int32_t* __restrict__ total_mtiles, int I,
     uint8_t* __restrict__ hq, uint8_t* __restrict__ h_sf) {
@@ -157,11 +167,20 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
       h[i] = swiglu(g[i], up[i]);
       amax = fmaxf(amax, fabsf(h[i]));
     }
-    amax = half_warp_max(amax);
+    if (MX) {
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    } else {
+      amax = half_warp_max(amax);
+    }
     const int e = pow2_scale_exp(amax);
     if (valid) {
       *reinterpret_cast<uint2*>(hq + blocked_offset(row, b * 128 + l16 * 8, I)) = quant8(h, e);
-      if (l16 == 0) h_sf[sf_atom_offset(row, b, IB)] = (uint8_t)(e + 127);
+      if (MX) {
+        if ((l16 & 3) == 0) h_sf[sf_atom_offset(row, 4 * b + (l16 >> 2), 4 * IB)] = (uint8_t)(e + 127);
+      } else if (l16 == 0) {
+        h_sf[sf_atom_offset(row, b, IB)] = (uint8_t)(e + 127);
+      }
     }
   }
   pdl_trigger();
@@ -211,6 +230,42 @@ __global__ void __launch_bounds__(256) quantize_weights_kernel(const float* __re
     *reinterpret_cast<uint4*>(q + base + 16 * i) = o;
   }
   if (threadIdx.x == 0) scale[(m * rb + bi) * cb + bj] = pow2_neg(-e);
+}
+
+// MXFP8 weights: every row quantised in 1x32 blocks along its columns; one
+// thread per 32-float chunk (chunks are contiguous, so the scale index is the
+// chunk index: [nmat, rows, cols/32]).
+__global__ void __launch_bounds__(256) quantize_weights_mx_kernel(const float* __restrict__ w,
+                                                                  int64_t chunks,
+                                                                  uint8_t* __restrict__ q,
+                                                                  float* __restrict__ scale) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float4 f = *reinterpret_cast<const float4*>(w + i * 32 + 4 * k);
+      v[4 * k] = f.x;
+      v[4 * k + 1] = f.y;
+      v[4 * k + 2] = f.z;
+      v[4 * k + 3] = f.w;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(v[k]));
+    const int e = pow2_scale_exp(amax);
+    const float inv = pow2_neg(e);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint4 o;
+      o.x = e4m3x4(v[16 * h + 0] * inv, v[16 * h + 1] * inv, v[16 * h + 2] * inv, v[16 * h + 3] * inv);
+      o.y = e4m3x4(v[16 * h + 4] * inv, v[16 * h + 5] * inv, v[16 * h + 6] * inv, v[16 * h + 7] * inv);
+      o.z = e4m3x4(v[16 * h + 8] * inv, v[16 * h + 9] * inv, v[16 * h + 10] * inv, v[16 * h + 11] * inv);
+      o.w = e4m3x4(v[16 * h + 12] * inv, v[16 * h + 13] * inv, v[16 * h + 14] * inv, v[16 * h + 15] * inv);
+      *reinterpret_cast<uint4*>(q + i * 32 + 16 * h) = o;
+    }
+    scale[i] = pow2_neg(-e);
+  }
 }
 
 // float power-of-two scale -> E8M0 byte; anything else flags MOE_DEV_BAD_SCALE.
@@ -281,16 +336,16 @@ static int stream_grid(int64_t work, int per_block, int64_t cap = 152 * 16) {
 cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
                                   int64_t T, cudaStream_t s, bool pdl, int max_ctas) {
   const int64_t warps = T * ((L.H / 128 + 3) / 4);
-  return launch_k(quant_dispatch_kernel, dim3(stream_grid(warps, 8, max_ctas)), dim3(256), 0, s, pdl,
-                  nullptr,
+  return launch_k(L.mx ? quant_dispatch_kernel<true> : quant_dispatch_kernel<false>,
+                  dim3(stream_grid(warps, 8, max_ctas)), dim3(256), 0, s, pdl, nullptr,
                   x, (const int32_t*)ws.inv_pad, T, L.H, L.K, ws.a, ws.a_sf);
 }
 
 cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int max_ctas,
                                 cudaStream_t s, bool pdl) {
   const int64_t warps = (L.rows_alloc) * ((L.I / 128 + 1) / 2);
-  return launch_k(swiglu_quant_kernel, dim3(stream_grid(warps, 8, max_ctas)), dim3(256), 0, s, pdl,
-                  nullptr,
+  return launch_k(L.mx ? swiglu_quant_kernel<true> : swiglu_quant_kernel<false>,
+                  dim3(stream_grid(warps, 8, max_ctas)), dim3(256), 0, s, pdl, nullptr,
                   (const uint16_t*)ws.gu, (const int32_t*)ws.total_mtiles, L.I, ws.hq, ws.h_sf);
 }
 
@@ -301,6 +356,45 @@ cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int 
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   quantize_weights_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, rows, cols, q, scale);
   return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weights_mx(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
+                                       float* scale, cudaStream_t s) {
+  const int64_t chunks = nmat * rows * (int64_t)(cols / 32);
+  if (chunks == 0) return cudaSuccess;
+  quantize_weights_mx_kernel<<<stream_grid(chunks, 256), 256, 0, s>>>(w, chunks, q, scale);
+  return cudaGetLastError();
+}
+
+// MXFP8 weight-scale atoms: for every expert, 128-row block nb (W1 in the
+// interleaved gate/up order of the weight store) and K block kb, one
+// 512-byte atom; row r's word holds the E8M0 scales of its 32-wide chunks
+// 4kb .. 4kb+3 (byte (r%32)*16 + (r/32)*4 + j).  One thread per word.
+__global__ void sfb_atoms_mx_kernel(const float* __restrict__ sc, int E, int N, int KB, int gate_up,
+                                    uint32_t* __restrict__ atoms, uint32_t* status) {
+  const int NB = N / 128;
+  const int64_t words = (int64_t)E * NB * KB * 128;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int wd = (int)(i & 127);
+    const int64_t atom = i >> 7;
+    const int kb = (int)(atom % KB);
+    const int64_t enb = atom / KB;
+    const int nb = (int)(enb % NB);
+    const int64_t e = enb / NB;
+    const int r = (wd & 3) * 32 + (wd >> 2);
+    int64_t n = (int64_t)nb * 128 + r;  // row of the (re-ordered) matrix
+    if (gate_up) {
+      const int I = N / 2;
+      const int64_t j = n >> 8, within = n & 255;
+      n = (within < 128) ? (j * 128 + within) : (I + j * 128 + within - 128);
+    }
+    const float* src = sc + (e * N + n) * (int64_t)(4 * KB) + 4 * kb;
+    uint32_t v = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v |= (uint32_t)scale_to_e8m0(src[j], status) << (8 * j);
+    atoms[i] = v;
+  }
 }
 
 // Weight-scale atoms for the GEMM B operand: for every expert, 128-row block
@@ -334,6 +428,15 @@ cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const
   const int64_t w1_chunks = (int64_t)E * 2 * I * (H / 16), w2_chunks = (int64_t)E * H * (I / 16);
   bind_blocked_kernel<<<stream_grid(w1_chunks, 256), 256, 0, s>>>(w1, wst.w1, E, 2 * I, H, 1);
   bind_blocked_kernel<<<stream_grid(w2_chunks, 256), 256, 0, s>>>(w2, wst.w2, E, H, I, 0);
+  if (L.mx) {
+    const int64_t words1 = (int64_t)E * (2 * I / 128) * (H / 128) * 128;
+    const int64_t words2 = (int64_t)E * (H / 128) * (I / 128) * 128;
+    sfb_atoms_mx_kernel<<<stream_grid(words1, 256), 256, 0, s>>>(
+        w1s, E, 2 * I, H / 128, 1, reinterpret_cast<uint32_t*>(wst.w1_sfatoms), status);
+    sfb_atoms_mx_kernel<<<stream_grid(words2, 256), 256, 0, s>>>(
+        w2s, E, H, I / 128, 0, reinterpret_cast<uint32_t*>(wst.w2_sfatoms), status);
+    return cudaGetLastError();
+  }
   const int64_t n1 = (int64_t)E * 2 * (I / 128) * (H / 128);
   bind_w1_scale_kernel<<<stream_grid(n1, 256), 256, 0, s>>>(w1s, wst.w1_sf, E, I / 128, H / 128,
                                                             status);

@@ -17,16 +17,22 @@ class MegaMoELayer:
                  expected_m: int | None = None, capacity_factor: float = 1.0,
                  fuse_fc1: bool = False, check_routes: bool = True, emit_fc1: bool = False,
                  gemm: str = "auto", watchdog_test: bool = False, device="cuda",
-                 workspace: torch.Tensor | None = None, gemms: str = "auto"):
+                 workspace: torch.Tensor | None = None, gemms: str = "auto",
+                 fmt: str = "deepseek"):
         """gemm: "auto" (tactic from expected_m), "single" (one CTA per SM) or
         "pair" (CTA pairs, tcgen05 cta_group::2).  gemms (fused epilogue only):
         "auto" (FC1 -> FC2 in one persistent launch for short forwards, two
         launches for long ones), "one_launch" or "split"; same results.
+        fmt: "deepseek" (1x128 activation / 128x128 weight scales) or
+        "mxfp8" (one scale per 32 elements along K for both; weights from
+        quantize_weights(..., fmt="mxfp8")).
         workspace: a uint8 device
         tensor shared with other layers whose forwards never overlap with this
         one's (at least workspace_bytes() of every layer that shares it); by
         default the layer allocates its own."""
         self.H, self.I, self.E, self.K = hidden, inter, num_experts, top_k
+        assert fmt in ("deepseek", "mxfp8")
+        self.fmt = fmt
         self.max_rows = max_rows
         self.flags = ((B.MOE_FLAG_FUSE_FC1_EPILOGUE if fuse_fc1 else 0)
                       | (B.MOE_FLAG_CHECK_ROUTES if check_routes else 0)
@@ -35,7 +41,8 @@ class MegaMoELayer:
                          "pair": B.MOE_FLAG_GEMM_CTA_PAIR}[gemm]
                       | (B.MOE_FLAG_WATCHDOG_TEST if watchdog_test else 0)
                       | {"auto": 0, "one_launch": B.MOE_FLAG_GEMMS_ONE_LAUNCH,
-                         "split": B.MOE_FLAG_SPLIT_GEMMS}[gemms])
+                         "split": B.MOE_FLAG_SPLIT_GEMMS}[gemms]
+                      | (B.MOE_FLAG_MXFP8 if fmt == "mxfp8" else 0))
         em = expected_m if expected_m is not None else max_rows
         ws, wb = B.moe_workspace_query(hidden, inter, num_experts, top_k, self.flags, em, max_rows,
                                        capacity_factor)
@@ -66,13 +73,21 @@ class MegaMoELayer:
 
     # -- weights ----------------------------------------------------------------
     @staticmethod
-    def quantize_weights(w: torch.Tensor, stream=None):
-        """float32 [n, rows, cols] on the GPU -> (E4M3 uint8, float scales [n, rows/128, cols/128])."""
+    def quantize_weights(w: torch.Tensor, stream=None, fmt: str = "deepseek"):
+        """float32 [n, rows, cols] on the GPU -> (E4M3 uint8, float scales
+        [n, rows/128, cols/128]; for fmt="mxfp8" [n, rows, cols/32])."""
         assert w.dtype == torch.float32 and w.is_cuda and w.is_contiguous() and w.dim() == 3
         n, r, c = w.shape
         q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
-        s = torch.empty((n, r // 128, c // 128), dtype=torch.float32, device=w.device)
-        B.moe_quantize_weights(w.data_ptr(), n, r, c, q.data_ptr(), s.data_ptr(), _stream_ptr(stream))
+        if fmt == "mxfp8":
+            s = torch.empty((n, r, c // 32), dtype=torch.float32, device=w.device)
+            B.moe_quantize_weights_mx(w.data_ptr(), n, r, c, q.data_ptr(), s.data_ptr(),
+                                      _stream_ptr(stream))
+        else:
+            assert fmt == "deepseek"
+            s = torch.empty((n, r // 128, c // 128), dtype=torch.float32, device=w.device)
+            B.moe_quantize_weights(w.data_ptr(), n, r, c, q.data_ptr(), s.data_ptr(),
+                                   _stream_ptr(stream))
         return q, s
 
     def bind_weights(self, w1_q, w1_s, w2_q, w2_s, stream=None) -> None:
@@ -80,6 +95,12 @@ class MegaMoELayer:
             assert t.is_cuda and t.is_contiguous()
         assert tuple(w1_q.shape) == (self.E, 2 * self.I, self.H) and w1_q.dtype == torch.uint8
         assert tuple(w2_q.shape) == (self.E, self.H, self.I) and w2_q.dtype == torch.uint8
+        if self.fmt == "mxfp8":
+            assert tuple(w1_s.shape) == (self.E, 2 * self.I, self.H // 32)
+            assert tuple(w2_s.shape) == (self.E, self.H, self.I // 32)
+        else:
+            assert tuple(w1_s.shape) == (self.E, 2 * self.I // 128, self.H // 128)
+            assert tuple(w2_s.shape) == (self.E, self.H // 128, self.I // 128)
         B.moe_bind_weights(self.handle, w1_q.data_ptr(), w1_s.data_ptr(), w2_q.data_ptr(),
                            w2_s.data_ptr(), _stream_ptr(stream))
 
@@ -141,6 +162,7 @@ class MegaMoELayer:
         blocked E4M3 buffers a and hq come as row-major copies."""
         v = B.moe_debug_views(self.handle)
         base = self.workspace.data_ptr()
+        mx = self.fmt == "mxfp8"
         R = v.rows_alloc
         H, I, E, K = self.H, self.I, self.E, self.K
 
@@ -158,9 +180,9 @@ class MegaMoELayer:
             inv=view(v.inv, 4 * self.max_rows * K, torch.int32, (self.max_rows * K,)),
             inv_pad=view(v.inv_pad, 4 * self.max_rows * K, torch.int32, (self.max_rows * K,)),
             a=unblock(view(v.a, R * H, torch.uint8, (R * H,)), R, H),
-            a_sf=view(v.a_sf, (R // 128) * kq(H) * 512, torch.uint8, (R // 128, kq(H), 512)),
+            a_sf=view(v.a_sf, (R // 128) * kq(H, mx) * 512, torch.uint8, (R // 128, kq(H, mx), 512)),
             hq=unblock(view(v.hq, R * I, torch.uint8, (R * I,)), R, I),
-            h_sf=view(v.h_sf, (R // 128) * kq(I) * 512, torch.uint8, (R // 128, kq(I), 512)),
+            h_sf=view(v.h_sf, (R // 128) * kq(I, mx) * 512, torch.uint8, (R // 128, kq(I, mx), 512)),
             y=view(v.y, R * H * 2, torch.bfloat16, (R, H)),
             rows_alloc=R,
             gemm_pair=bool(v.gemm_pair),
@@ -189,15 +211,17 @@ def unblock(flat: torch.Tensor, rows: int, cols: int) -> torch.Tensor:
     return flat.view(rows // 128, cols // 128, 128, 128).permute(0, 2, 1, 3).reshape(rows, cols)
 
 
-def kq(k: int) -> int:
-    """Scale atoms along a K extent: one per four 128-wide K blocks."""
-    return (k // 128 + 3) // 4
+def kq(k: int, mx: bool = False) -> int:
+    """Scale atoms along a K extent: one per four 128-wide K blocks, or one
+    per K block under MXFP8."""
+    return k // 128 if mx else (k // 128 + 3) // 4
 
 
 def sf_atom_rows(atoms: torch.Tensor, rows: int, kblocks: int) -> torch.Tensor:
     """Decode scale atoms [mblocks, kgroups, 512] into E8M0 bytes [rows, kblocks]:
-    row r of an m-block, K block 4q + j, sits at byte (r%32)*16 + (r//32)*4 + j
-    of atom q."""
+    row r of an m-block, scale unit 4q + j, sits at byte (r%32)*16 + (r//32)*4 + j
+    of atom q.  A unit is a 128-wide K block, or under MXFP8 a 32-wide chunk
+    (pass kblocks = K/32 then)."""
     mb, kg, _ = atoms.shape
     a = atoms.view(mb, kg, 32, 4, 4)             # [mb, q, r%32, r//32, j]
     a = a.permute(0, 3, 2, 1, 4)                 # [mb, r//32, r%32, q, j]
