@@ -367,6 +367,26 @@ def test_token_permutation_and_pow2_weight_scaling(lib, orc):
 
 
 @pytest.mark.parametrize("gemm", ["single", "pair"])
+@pytest.mark.parametrize("T,H,I,E,K", [
+    (64, 16384, 128, 2, 1),    # H at its limit: FC1 K = 16384 (128 K blocks), FC2 N = 16384
+    (64, 128, 16384, 2, 1),    # I at its limit: FC1 N = 32768, FC2 K = 16384
+    (40, 256, 128, 1024, 8),   # E at its limit: most experts empty
+])
+def test_dimension_limits(lib, orc, T, H, I, E, K, gemm):
+    """The largest H, I and E the ABI accepts, through the whole layer."""
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=H + I + E)
+    layer, wo = layer_from_float(lib, orc, T, H, I, E, K, w1, w2, fuse=True, emit=False, gemm=gemm)
+    ref = orc.forward(x, idx, w, *wo)
+    xt, it, wt = gh.to_device(x, idx, w)
+    out = layer.forward(xt, it, wt)
+    assert layer.read_status() == (0, 0)
+    dbg = layer.debug()
+    rows = check_routing(dbg, ref, T, K)
+    check_quant(lib, dbg, ref["xq"], ref["xs"], ref["perm"], rows, K)
+    compare_outputs(dbg, out, ref, rows, check_gu=False)
+
+
+@pytest.mark.parametrize("gemm", ["single", "pair"])
 def test_sm_budget_bit_identical(lib, orc, gemm):
     """moe_set_sm_budget changes only grid sizes: outputs are bit-identical for
     every budget (each GEMM tile and each element is computed the same way)."""
