@@ -61,10 +61,12 @@ class MegaMoELayer:
     @staticmethod
     def workspace_bytes(hidden: int, inter: int, num_experts: int, top_k: int, *, max_rows: int,
                         expected_m: int | None = None, capacity_factor: float = 1.0,
-                        fuse_fc1: bool = False, emit_fc1: bool = False, gemm: str = "auto") -> int:
+                        fuse_fc1: bool = False, emit_fc1: bool = False, gemm: str = "auto",
+                        fmt: str = "deepseek") -> int:
         """Workspace size a layer of these dims needs (for a shared workspace)."""
         flags = ((B.MOE_FLAG_FUSE_FC1_EPILOGUE if fuse_fc1 else 0)
                  | (B.MOE_FLAG_EMIT_FC1 if emit_fc1 else 0)
+                 | (B.MOE_FLAG_MXFP8 if fmt == "mxfp8" else 0)
                  | {"auto": 0, "single": B.MOE_FLAG_GEMM_SINGLE_CTA,
                     "pair": B.MOE_FLAG_GEMM_CTA_PAIR}[gemm])
         em = expected_m if expected_m is not None else max_rows

@@ -70,6 +70,10 @@ def test_workspace_query_capacity_and_tactic(B):
     with pytest.raises(B.MoEError):
         B.moe_workspace_query(512, 256, 8, 2, f | B.MOE_FLAG_SPLIT_GEMMS | B.MOE_FLAG_GEMMS_ONE_LAUNCH,
                               1, 128)
+    # MXFP8 keeps one scale atom per K block instead of per four: larger
+    # workspace and weight store, same for every other buffer
+    mx = B.moe_workspace_query(7168, 2048, 256, 8, f | B.MOE_FLAG_MXFP8, 1, 8192)
+    assert mx[0] > fused[0] and mx[1] > fused[1]
 
 
 def test_null_arguments_rejected_without_cuda(B):
