@@ -450,7 +450,9 @@ def main():
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
 
-    def timed_steps(n, profiled):
+    step_times = []  # the timed (unprofiled) steps, for the median / p10 / p90
+
+    def timed_steps(n, profiled, keep=False):
         tot = 0.0
         per_kernel = {k: 0.0 for k in KERNELS}
         for _ in range(n):
@@ -462,6 +464,8 @@ def main():
                 t_end.record(stream)
             stream.synchronize()
             tot += t_start.elapsed_time(t_end)
+            if keep:
+                step_times.append(t_start.elapsed_time(t_end))
             if profiled:
                 for i, k in enumerate(KERNELS):
                     per_kernel[k] += ev[i].elapsed_time(ev[i + 1])
@@ -476,7 +480,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
-    total_ms, _ = timed_steps(args.steps, False)
+    total_ms, _ = timed_steps(args.steps, False, keep=True)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
@@ -639,6 +643,8 @@ def main():
                            "fp8_peak_tflops": fp8_peak, "fp8_peak_regime": regime, "hbm_gbs": hbm,
                            "source": src},
         "roofline": roof,
+        "step_ms": {"median": float(np.median(step_times)), "p10": float(np.percentile(step_times, 10)),
+                    "p90": float(np.percentile(step_times, 90))},
         "kernel_ms": kern_ms,
         "kernel_ms_source": ("CUDA events before every kernel, a second capture of the same forward "
                              f"replayed for the same {K} steps right after the timed ones "

@@ -250,6 +250,31 @@ def test_all_masked_and_nan_masked_weights(lib, orc):
     compare_outputs(layer.debug(), out, ref, np.zeros(0, np.int64), check_gu=False)
 
 
+@pytest.mark.parametrize("gemm", ["single", "pair"])
+def test_poisoned_empty_experts_contribute_nothing(lib, orc, gemm):
+    """An expert with no route contributes nothing: with its W1 / W2 codes all
+    0x7F (E4M3 NaN) the output is bit-identical to the clean weights and finite."""
+    T, H, I, E, K = 200, 384, 256, 8, 2
+    empty = (2, 5)
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=71, empty=empty)
+    q1, s1 = lib.MegaMoELayer.quantize_weights(torch.from_numpy(w1).cuda())
+    q2, s2 = lib.MegaMoELayer.quantize_weights(torch.from_numpy(w2).cuda())
+    xt, it, wt = gh.to_device(x, idx, w)
+    outs = []
+    for poison in (False, True):
+        a1, a2 = q1.clone(), q2.clone()
+        if poison:
+            for e in empty:
+                a1[e].fill_(0x7F)
+                a2[e].fill_(0x7F)
+        layer = lib.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm=gemm)
+        layer.bind_weights(a1, s1, a2, s2)
+        outs.append(layer.forward(xt, it, wt).clone())
+        assert layer.read_status() == (0, 0)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.isfinite(outs[1].float()).all()
+
+
 def test_route_errors_set_status(lib, orc):
     import serving_route_gb300.binding as B
     T, H, I, E, K = 16, 256, 128, 4, 2
