@@ -104,12 +104,16 @@ template <bool MX>
 __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pad, int64_t T, int H, int K,
     uint8_t* __restrict__ a, uint8_t* __restrict__ a_sf) {
-  pdl_wait();
   const int lane = threadIdx.x & 31, grp = lane >> 3, l8 = lane & 7;
   const int KB = H >> 7;
   const int units = (KB + 3) >> 2;
   const int64_t total = T * units;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  // x is an input of the forward that no kernel of it writes: a warp's first
+  // loads are issued before the programmatic wait, so their latency overlaps
+  // the routing kernel's tail.  The routing tables (inv_pad) and every store
+  // come after the wait.
+  bool waited = false;
   for (int64_t u0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u0 < total;
        u0 += 2 * nwarps) {
     const int64_t u1 = u0 + nwarps;
@@ -126,6 +130,10 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
                  : make_uint4(0u, 0u, 0u, 0u);
       r1[h] = v1 ? *reinterpret_cast<const uint4*>(x + t1 * H + b1 * 128 + l8 * 16 + h * 8)
                  : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (!waited) {
+      pdl_wait();
+      waited = true;
     }
     const int p0 = (lane < K) ? inv_pad[t0 * K + lane] : -1;
     const int p1 = (lane < K && has1) ? inv_pad[t1 * K + lane] : -1;
