@@ -5,9 +5,11 @@
 // MegaMoE forward preparation": expert-id bounds, no duplicate routes, finite
 // scores on active routes, masked slots (-1) may carry any score).
 //
-// Three small kernels, no host synchronisation (the second and third are
-// launched as programmatic dependents, so their launch overlaps the previous
-// kernel):
+// By default one cooperative kernel (route_fused, below) when its blocks can
+// all be resident; otherwise -- and under an SM budget, and for the
+// no-allocation entry point -- three small kernels, no host synchronisation
+// (the second and third are launched as programmatic dependents, so their
+// launch overlaps the previous kernel):
 //   route_count   per 128-token block: validate, per-block expert histogram
 //   route_scan    one CTA: expert totals, unpadded and padded (128 or 256
 //                 rows per GEMM segment) exclusive scans, per-block bases,
@@ -205,10 +207,11 @@ __global__ void __launch_bounds__(kRouteTokens) route_scatter_kernel(
 //   barrier  every block arrives on a counter zeroed before the forward; the
 //            launch is cooperative (all blocks resident), and the wait is
 //            bounded all the same
-//   phase 2  every block reads the whole [nb][E] histogram: expert totals,
-//            its own prefix over earlier blocks, the unpadded and padded
-//            exclusive scans; the expert-level outputs (counts, offsets,
-//            m-tile table) are spread over the blocks
+//   phase 2  every block reads the whole [nb][E] histogram (eight loads in
+//            flight per thread, summed with shared-memory atomics): expert
+//            totals, its own prefix over earlier blocks, the unpadded and
+//            padded exclusive scans; the expert-level outputs (counts,
+//            offsets, m-tile table) are spread over the blocks
 //   phase 3  the stable scatter of route_scatter, bases from shared memory
 // ---------------------------------------------------------------------------
 // 512 tokens per block (a warp per 32 tokens, as in route_scatter): four
