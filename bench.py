@@ -93,13 +93,40 @@ def aggregate_rate(world: int, units_per_step: float, steps: int, max_total_ms: 
     return world * units_per_step * steps / (max_total_ms * 1e-3)
 
 
+def strip_c_comments(src: str) -> str:
+    """C/C++ source without comments and with whitespace collapsed, so that
+    editing a comment does not count as changing the code."""
+    import re
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":                       # string / char literal, kept whole
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def gemm_source_hash() -> str:
-    """sha256 over the sources the grouped-GEMM kernel is compiled from."""
+    """sha256 over the code (comments stripped) the grouped-GEMM kernel is
+    compiled from."""
     import hashlib
     h = hashlib.sha256()
     for f in ("gemm.cu", "common.cuh", "internal.h"):
-        with open(os.path.join(ROOT, "serving_route_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "serving_route_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(strip_c_comments(fh.read()).encode())
     return h.hexdigest()
 
 

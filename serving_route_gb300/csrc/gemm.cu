@@ -11,7 +11,9 @@
 //    memory: no per-K-block promotion through registers.  A scale atom holds
 //    the bytes of four K blocks; the four MMAs of K block 4q + j select byte j
 //    (the descriptor's scale-factor ids), so one tcgen05.cp per operand
-//    serves four K blocks.
+//    serves four K blocks.  MXFP8 (GemmArgs::mx): the four bytes are the
+//    scales of the four 32-wide chunks of one K block, so the atoms come
+//    with every K block and MMA k selects byte k.
 //  * Operands come from blocked buffers (every 128x128 block one contiguous
 //    16 KB box: the weights from the bind step, A / hq from the quantisers),
 //    one 3-D TMA box per block, 128-byte swizzle.
@@ -38,9 +40,14 @@
 //    and MMAs and probes the next stage while the current one computes,
 //    warps 2-9 the epilogue (two per TMEM lane quadrant).
 //  * Epilogues: FC2 -> BF16 y (TMA stores); FC1 unfused -> BF16 gate||up;
-//    FC1 fused -> BF16-rounded gate/up, SwiGLU, 1x128 re-quantisation to E4M3
-//    + E8M0 atoms (bit-equal to the unfused path, which runs the same device
-//    functions).
+//    FC1 fused -> BF16-rounded gate/up, SwiGLU, 1x128 (or MXFP8 1x32)
+//    re-quantisation to E4M3 + E8M0 atoms (bit-equal to the unfused path,
+//    which runs the same device functions).
+//  * kModeMega: FC1 then FC2 in one persistent launch.  Each fused FC1 tile
+//    publishes its m-tile's count (fc1_done, release add after proxy-fenced
+//    stores); an FC2 tile's producer waits for its m-tile's count before its
+//    first TMA load of hq.  Every CTA takes its FC1 units before its FC2
+//    units, so the waits always end (see the kernel's comment).
 //  * Launched as a programmatic dependent: the barrier / TMEM prologue
 //    overlaps the previous kernel, the wait comes before the first global
 //    read.
