@@ -83,3 +83,15 @@ def test_null_arguments_rejected_without_cuda(B):
     assert L.moe_forward(None, None, None, None, 1, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_debug_views(None, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_forward_plan(None, 1, None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_gemm_source_hash_ignores_comments_only():
+    """bench.py keeps a recorded DRAM-traffic figure only while the GEMM code is
+    unchanged; comments and whitespace do not count as code."""
+    import bench
+    a = 'int f(int x) { return x + 1; } // note\n/* block\n comment */ const char* s = "a // b";'
+    b = 'int f(int x)  {\n  return x + 1;\n}\nconst char* s = "a // b";  // other note'
+    c = 'int f(int x) { return x + 2; } const char* s = "a // b";'
+    assert bench.strip_c_comments(a) == bench.strip_c_comments(b)
+    assert bench.strip_c_comments(a) != bench.strip_c_comments(c)
+    assert '"a // b"' in bench.strip_c_comments(a)
