@@ -195,10 +195,15 @@ class ClockSampler:
 
 
 def cpu_threads() -> int:
+    """host threads the oracle uses: the cores this process may run on, or
+    OMP_NUM_THREADS when that is set lower (the oracle's parallel loops are
+    OpenMP)"""
     try:
-        return len(os.sched_getaffinity(0))
+        n = len(os.sched_getaffinity(0))
     except AttributeError:
-        return os.cpu_count() or 1
+        n = os.cpu_count() or 1
+    omp = os.environ.get("OMP_NUM_THREADS", "")
+    return min(n, int(omp)) if omp.isdigit() and int(omp) > 0 else n
 
 
 def oracle_sample(wl, x_bits, idx, w, tokens):
