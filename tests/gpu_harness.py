@@ -34,40 +34,45 @@ def bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return g.bf16_bits_to_f32(bits).astype(np.float64)
 
 
-def device_weights(wl: Workload, layer_cls, chunk_experts: int = 16, stream=None):
+def device_weights(wl: Workload, layer_cls, chunk_experts: int = 16, stream=None, fmt="deepseek"):
     """FP32 weights generated on the GPU and quantised there, in expert chunks
-    (bounded temporary memory).  Returns (w1q, w1s, w2q, w2s) on the device."""
+    (bounded temporary memory).  Returns (w1q, w1s, w2q, w2s) on the device.
+    fmt="mxfp8": scales per row and 32 columns."""
     E, H, I = wl.E, wl.H, wl.I
     dev = torch.device("cuda")
+    mx = fmt == "mxfp8"
     w1q = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=dev)
-    w1s = torch.empty((E, 2 * I // 128, H // 128), dtype=torch.float32, device=dev)
+    w1s = torch.empty((E, 2 * I, H // 32) if mx else (E, 2 * I // 128, H // 128),
+                      dtype=torch.float32, device=dev)
     w2q = torch.empty((E, H, I), dtype=torch.uint8, device=dev)
-    w2s = torch.empty((E, H // 128, I // 128), dtype=torch.float32, device=dev)
+    w2s = torch.empty((E, H, I // 32) if mx else (E, H // 128, I // 128),
+                      dtype=torch.float32, device=dev)
     sp = (stream or torch.cuda.current_stream()).cuda_stream
     n1, n2 = 2 * I * H, H * I
     for e0 in range(0, E, chunk_experts):
         ne = min(chunk_experts, E - e0)
         f1 = torch.empty((ne, 2 * I, H), dtype=torch.float32, device=dev)
         g.dev_normal_f32(wl.seed, g.STREAM_W1, e0 * n1, ne * n1, g.weight_sigma(H), f1.data_ptr(), sp)
-        q, s = layer_cls.quantize_weights(f1, stream)
+        q, s = layer_cls.quantize_weights(f1, stream, fmt=fmt)
         w1q[e0:e0 + ne].copy_(q)
         w1s[e0:e0 + ne].copy_(s)
         del f1, q, s
         f2 = torch.empty((ne, H, I), dtype=torch.float32, device=dev)
         g.dev_normal_f32(wl.seed, g.STREAM_W2, e0 * n2, ne * n2, g.weight_sigma(I), f2.data_ptr(), sp)
-        q, s = layer_cls.quantize_weights(f2, stream)
+        q, s = layer_cls.quantize_weights(f2, stream, fmt=fmt)
         w2q[e0:e0 + ne].copy_(q)
         w2s[e0:e0 + ne].copy_(s)
         del f2, q, s
     return w1q, w1s, w2q, w2s
 
 
-def oracle_weights(orc, wl: Workload, experts=None):
+def oracle_weights(orc, wl: Workload, experts=None, fmt="deepseek"):
     """Oracle-side weights: host generator + the oracle's quantiser.
     experts=None -> all experts; otherwise arrays hold only the listed experts
-    in the order given."""
-    w1q, w1s = orc.quant_weights(problem.w1_f32(wl, experts))
-    w2q, w2s = orc.quant_weights(problem.w2_f32(wl, experts))
+    in the order given.  fmt="mxfp8": the oracle's MXFP8 quantiser."""
+    quant = orc.quant_weights_mx if fmt == "mxfp8" else orc.quant_weights
+    w1q, w1s = quant(problem.w1_f32(wl, experts))
+    w2q, w2s = quant(problem.w2_f32(wl, experts))
     return w1q, w1s, w2q, w2s
 
 

@@ -68,6 +68,29 @@ def test_v2lite_full_layer(lib, orc):
     assert torch.equal(outs[False].view(torch.int16), outs[True].view(torch.int16))
 
 
+def test_v2lite_full_layer_mxfp8(lib, orc):
+    """The dsv2lite workload in the MXFP8 format, every output element against
+    the oracle (fmt=1); weight codes and per-chunk scales bit-exact."""
+    from tests.test_gpu_mxfp8 import check_quant_mx
+    wl = configs.V2LITE
+    wd = gh.device_weights(wl, lib.MegaMoELayer, fmt="mxfp8")
+    wo = gh.oracle_weights(orc, wl, fmt="mxfp8")
+    for a, b in zip(wd, wo):
+        assert np.array_equal(a.cpu().numpy(), b)
+    x, idx, w = gh.host_inputs(wl)
+    ref = orc.forward(x, idx, w, *wo, fmt=1)
+    xt, it, wt = gh.to_device(x, idx, w)
+    layer = lib.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, fuse_fc1=True, fmt="mxfp8")
+    layer.bind_weights(*wd)
+    out = layer.forward(xt, it, wt)
+    assert layer.read_status() == (0, 0)
+    dbg = layer.debug()
+    rows = check_routing(dbg, ref, wl.T, wl.K)
+    check_quant_mx(lib, dbg, ref["xq"], ref["xs"], ref["perm"], rows, wl.K)
+    stats = compare_outputs(dbg, out, ref, rows, check_gu=False)
+    print("v2lite mxfp8", stats)
+
+
 @pytest.fixture(scope="module")
 def v3_weights(lib):
     wd = gh.device_weights(configs.V3_PREFILL, lib.MegaMoELayer)
