@@ -1,0 +1,62 @@
+"""bench.py's one-line JSON contract, run end to end on the tiny workload.
+
+The reference arm (the oracle on the host cores) runs on the CPU; the main
+line, the MXFP8 format and the side-stream sweep need the GPU.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_bench(*args, timeout=600):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                       capture_output=True, text=True, timeout=timeout)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.strip().splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+BASE_KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+             "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"}
+
+
+def test_reference_arm_line():
+    d = run_bench("--impl", "reference", "--config", "tiny", "--steps", "1", "--warmup", "0")
+    assert BASE_KEYS <= set(d), set(d)
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"].startswith("tiny")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", ["deepseek", "mxfp8"])
+def test_main_line(fmt):
+    d = run_bench("--config", "tiny", "--steps", "5", "--warmup", "3", "--no-cpu-baseline",
+                  "--format", fmt)
+    assert (BASE_KEYS - {"cpu_baseline"}) <= set(d), set(d)
+    assert d["value"] > 0 and d["steps"] == 5 and d["warmup"] == 3 and d["n_gpus"] == 1
+    r = d["roofline"]
+    assert {"bound", "achieved", "peak", "unit", "frac", "traffic"} <= set(r)
+    assert r["bound"] in ("tensor", "hbm") and 0 < r["frac"] < 2
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] > 0 and d["gpu_launches"] % d["steps"] == 0
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    assert {"median", "p10", "p90"} <= set(d["step_ms"])
+    assert d["config"]["format"].startswith("MXFP8" if fmt == "mxfp8" else "E4M3")
+
+
+@pytest.mark.gpu
+def test_side_stream_sweep_line():
+    d = run_bench("--config", "tiny", "--side-mlp", "256", "--steps", "3", "--warmup", "1",
+                  "--no-cpu-baseline")
+    assert d["unit"] == "ms" and d["higher_is_better"] is False
+    assert d["layer_ms"] > 0 and d["mlp_ms"] > 0 and d["serial_ms"] > 0
+    assert len(d["concurrent"]) >= 2 and all(p["ms"] > 0 for p in d["concurrent"])
