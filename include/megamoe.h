@@ -296,7 +296,8 @@ MOE_API moe_status moe_set_profile_events(moe_handle* h, void* const* events, in
  * CTA pairs) and the routing keeps to its three small kernels (no
  * cooperative grid).  The short streaming kernels (quantisation, combine)
  * keep their full grids: their CTAs cannot be pinned to a subset of SMs, and
- * a grid of one CTA per budgeted SM made them several times slower.  Results
+ * grids of one CTA per budgeted SM made the dsv2lite-shaped layer 25% slower
+ * at a 144-SM budget (3% with full grids).  Results
  * are bit-identical for every budget.  Errors: MOE_ERR_INVALID_ARG for a NULL
  * handle or max_sms < 0 or == 1.
  */
