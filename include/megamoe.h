@@ -78,9 +78,10 @@ typedef enum moe_status {
 #define MOE_FLAG_GEMM_CTA_PAIR 0x10u
 /* Test only: exercises the device watchdog.  Every kernel wait is bounded
  * (1 s); with this flag the bound is 20 ms and the first GEMM CTA withholds one
- * pipeline stage, so its wait expires: the forward records MOE_DEV_TIMEOUT,
- * the kernel winds down (drains its copies, frees tensor memory) and the
- * context stays usable.  Single-CTA GEMM tactic only. */
+ * pipeline stage (with CTA pairs, the first pair's second CTA withholds its
+ * share of one stage), so the MMA wait expires: the forward records
+ * MOE_DEV_TIMEOUT, the kernel winds down (drains its copies, frees tensor
+ * memory) and the context stays usable. */
 #define MOE_FLAG_WATCHDOG_TEST 0x20u
 /* FC1 -> FC2 in one launch.  With the fused FC1 epilogue both GEMMs can run
  * as one persistent launch (the megakernel): every FC1 tile, then every FC2

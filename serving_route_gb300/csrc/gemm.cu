@@ -266,9 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (!PAIR && g.watchdog_test && blockIdx.x == 0 && u == unit0 && kb == 2) {
+        if (g.watchdog_test && blockIdx.x == (PAIR ? 1u : 0u) && u == unit0 && kb == 2) {
           // watchdog test: this stage is never filled, so the MMA wait on it
-          // expires; it is not counted as in flight for the drain below
+          // expires; it is not counted as in flight for the drain below.  In
+          // a pair the peer withholds its share: the leader still arms the
+          // stage for both shares, so its full barrier never completes
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;

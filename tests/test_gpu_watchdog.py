@@ -2,7 +2,9 @@
 
 Every wait inside the GEMM kernels is bounded.  With MOE_FLAG_WATCHDOG_TEST
 the first GEMM CTA withholds one pipeline stage -- a barrier that nothing
-completes -- and the wait bound drops to 20 ms: the kernel must record
+completes; on CTA pairs the first pair's second CTA withholds its share, which
+the leader's barrier still expects -- and the wait bound drops to 20 ms: the
+kernel must record
 MOE_DEV_TIMEOUT, wind down (drain its copies and MMAs, free tensor memory) and
 return, and the context must stay usable for the next forward.  No trap, no
 fault, no hang.
@@ -17,11 +19,15 @@ from tests.test_gpu_parity import compare_outputs, small_problem
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("gemm", ["single", "pair"])
 @pytest.mark.parametrize("split", [False, True])
-def test_watchdog_expires_with_status_and_context_survives(orc, split):
+def test_watchdog_expires_with_status_and_context_survives(orc, split, gemm):
     """split=False: the one-launch FC1 -> FC2 kernel, where the FC2 tiles of
-    the other CTAs also wait in vain for the m-tile counts that CTA 0 never
-    publishes, and expire on their own bound."""
+    the other CTAs also wait in vain for the m-tile counts that CTA 0 (or
+    pair 0) never publishes, and expire on their own bound.  gemm="pair": the
+    leader's MMA wait expires; the peer's waits on the leader's commits expire
+    too, and both CTAs meet at the cluster barrier before freeing the pair's
+    tensor memory."""
     import __graft_entry__ as ge
     ge.build()
     import serving_route_gb300 as S
@@ -33,7 +39,7 @@ def test_watchdog_expires_with_status_and_context_survives(orc, split):
     q2, s2 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w2).cuda())
     xt, it, wt = gh.to_device(x, idx, w)
 
-    bad = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm="single", watchdog_test=True,
+    bad = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm=gemm, watchdog_test=True,
                          gemms="split" if split else "one_launch")
     bad.bind_weights(q1, s1, q2, s2)
     bad.forward(xt, it, wt)
@@ -41,7 +47,7 @@ def test_watchdog_expires_with_status_and_context_survives(orc, split):
     assert st == B.MOE_ERR_DEVICE_TIMEOUT and bits & B.MOE_DEV_TIMEOUT, (st, bits)
 
     # the context is intact: a normal forward right after is correct
-    good = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm="single")
+    good = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm=gemm)
     good.bind_weights(q1, s1, q2, s2)
     out = good.forward(xt, it, wt)
     assert good.read_status() == (0, 0)
