@@ -449,6 +449,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g1.sfb = h->wst.w1_sfatoms;
   g1.mtile_expert = ws.mtile_expert;
   g1.total_mtiles = ws.total_mtiles;
+  g1.counts = ws.counts;
+  g1.pad_offsets = ws.pad_offsets;
   g1.KB = L.H / 128;
   g1.KQ = (int)atoms_along_k(g1.KB, L.mx);
   g1.mx = L.mx ? 1 : 0;
@@ -482,6 +484,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.sfb = h->wst.w2_sfatoms;
   g2.mtile_expert = ws.mtile_expert;
   g2.total_mtiles = ws.total_mtiles;
+  g2.counts = ws.counts;
+  g2.pad_offsets = ws.pad_offsets;
   g2.KB = L.I / 128;
   g2.KQ = (int)atoms_along_k(g2.KB, L.mx);
   g2.mx = L.mx ? 1 : 0;

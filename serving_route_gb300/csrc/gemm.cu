@@ -453,6 +453,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = m_of(u, ph);
       const int nt = nt_of(u, ph, m);
       const int mt = own_mtile(m);
+      // Routed rows of this m-tile, read before the accumulator wait (which
+      // hides the loads).  The rest of the tile is its expert segment's
+      // padding, which no later step reads: a warp whose 32 rows are all
+      // padding skips the drain, the arithmetic and the stores.
+      const int e_t = g.mtile_expert[mt];
+      const bool live = q * 32 < g.pad_offsets[e_t] + g.counts[e_t] - mt * 128;
       // the epilogue of this unit: the launch's mode, or per phase in the
       // megakernel (FC1 fused, with gate||up kept when its output is bound)
       const int em = kMega ? (ph ? kModeY : (g.out ? kModeFusedGU : kModeFused)) : MODE;
@@ -463,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t row = (int64_t)mt * 128 + row_in_tile;
       // FC2: the second column half of a tile past H holds no output
-      const bool active = !(em_y && half == 1 && nt * 256 + 128 >= (ph ? g2.N : g.N));
+      const bool active = live && !(em_y && half == 1 && nt * 256 + 128 >= (ph ? g2.N : g.N));
       uint32_t pk[64];  // BF16 pairs of this warp's 128 accumulator columns
       if (active) {
         uint32_t r[4][32];
@@ -537,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          pk[8 * v + 4], pk[8 * v + 5], pk[8 * v + 6], pk[8 * v + 7]);
         }
       }
-      if (em_gu) {
+      if (em_gu && active) {
         uint16_t* dg = g.out + row * g.ld_out + (int64_t)nt * 128 + half * 64;
         uint16_t* du = dg + g.inter;
 #pragma unroll
@@ -549,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        pk[32 + 8 * v + 6], pk[32 + 8 * v + 7]);
         }
       }
-      if (em_fused && g.mx) {
+      if (em_fused && g.mx && active) {
         // MXFP8: this thread's 64 h columns are two whole 32-wide chunks of
         // its row, so each gets its scale without any exchange
         float h[64];
@@ -576,7 +582,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           st_global_v8(dq + 32 * v, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
           g.h_sf[sf_atom_offset(row, 4 * nt + 2 * half + v, 4 * g.IB)] = (uint8_t)(e + 127);
         }
-      } else if (em_fused) {
+      } else if (em_fused && !g.mx && !active) {
+        // a padding quadrant (both of its warps decide alike) still completes
+        // this tile's phase of the amax exchange, which every 1x128 fused
+        // tile advances once (MXFP8 tiles have no exchange)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&amax_bar[q]));
+        if (!mbar_wait(smem_u32(&amax_bar[q]), tile_par, abort, g.status, g.wait_limit_ns)) break;
+      } else if (em_fused && !g.mx) {
         // gate pairs pk[0..31], up pairs pk[32..63] -> h[0..63]
         float h[64];
         float amax = 0.f;

@@ -107,6 +107,10 @@ struct GemmArgs {
   const uint8_t* sfb;          // scale atoms of B: [E][NB][KQ][512]
   const int32_t* mtile_expert;
   const int32_t* total_mtiles;
+  // routed rows and padded segment start per expert: an m-tile's rows past
+  // pad_offsets[e] + counts[e] are padding that nothing downstream reads
+  const int32_t* counts;
+  const int32_t* pad_offsets;
   int KB;                      // K / 128
   int KQ;                      // scale atoms along K (atoms_along_k)
   int mx;                      // MXFP8: an atom per K block, MMA k uses byte k
