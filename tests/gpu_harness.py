@@ -97,3 +97,34 @@ def padded_rows(offsets: np.ndarray, pad_offsets: np.ndarray, R: int) -> np.ndar
     e = np.searchsorted(offsets, pos, side="right") - 1
     e = np.clip(e, 0, E - 1)
     return pad_offsets[e] + (pos - offsets[e])
+
+
+def poison_padding(layer) -> int:
+    """Writes non-finite values into every padding row of the GEMM segments
+    (rows past an expert's routed rows, up to its padded end): E4M3 NaN
+    (0x7F) in A and hq, E8M0 NaN (0xFF) in their scale atoms, BF16 NaN in y
+    and in gu when it is kept.  Returns the number of padding rows."""
+    import serving_route_gb300.binding as B
+    d = layer.debug()
+    off = d["offsets"].cpu().numpy()
+    pad = d["pad_offsets"].cpu().numpy()
+    rows = [r for e in range(len(off) - 1) for r in range(pad[e] + off[e + 1] - off[e], pad[e + 1])]
+    if not rows:
+        return 0
+    r = torch.tensor(rows, dtype=torch.long, device="cuda")
+    rb, rr = r // 128, r % 128
+    v = B.moe_debug_views(layer.handle)
+    base, R = layer.workspace.data_ptr(), d["rows_alloc"]
+    for ptr, cols in ((v.a, layer.H), (v.hq, layer.I)):
+        # blocked [R/128][cols/128][128 rows][128 bytes]
+        blk = layer.workspace[ptr - base: ptr - base + R * cols].view(R // 128, cols // 128, 128, 128)
+        blk[rb, :, rr, :] = 0x7F
+    byte0 = (rr % 32) * 16 + (rr // 32) * 4       # a row's scale bytes in each 512-byte atom
+    for sf in (d["a_sf"], d["h_sf"]):
+        for j in range(4):
+            sf[rb, :, byte0 + j] = 0xFF
+    d["y"][r] = float("nan")
+    if "gu" in d:
+        d["gu"][r] = float("nan")
+    torch.cuda.synchronize()
+    return len(rows)

@@ -138,3 +138,22 @@ def test_mx_sm_budget_bit_identical(lib, orc, gemm, gemms):
     ref = orc.forward(x, idx, w, *wo, fmt=1)
     dbg = layer.debug()
     compare_outputs(dbg, full, ref, check_routing(dbg, ref, T, K), check_gu=False)
+
+
+@pytest.mark.parametrize("gemm", ["single", "pair"])
+def test_mx_poisoned_padding_rows_change_nothing(lib, orc, gemm):
+    """MXFP8: NaN codes, NaN per-chunk scales and NaN BF16 in every padding
+    row between two forwards leave the output bit-identical."""
+    T, H, I, E, K = 300, 512, 384, 8, 4
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=72)
+    layer, wo = mx_layer(lib, orc, T, H, I, E, K, w1, w2, fuse_fc1=True, gemm=gemm, gemms="one_launch")
+    xt, it, wt = gh.to_device(x, idx, w)
+    first = layer.forward(xt, it, wt).clone()
+    assert layer.read_status() == (0, 0)
+    assert gh.poison_padding(layer) > 0
+    again = layer.forward(xt, it, wt)
+    assert layer.read_status() == (0, 0)
+    assert torch.equal(again.view(torch.int16), first.view(torch.int16))
+    ref = orc.forward(x, idx, w, *wo, fmt=1)
+    dbg = layer.debug()
+    compare_outputs(dbg, again, ref, check_routing(dbg, ref, T, K), check_gu=False)

@@ -196,12 +196,12 @@ def small_problem(orc, T, H, I, E, K, seed, mask=0.0, empty=()):
 
 
 def layer_from_float(S, orc, T, H, I, E, K, w1, w2, fuse=True, emit=True, max_rows=None, cf=1.0,
-                     gemm="auto"):
+                     gemm="auto", gemms="auto"):
     q1, s1 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w1).cuda())
     q2, s2 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w2).cuda())
     wo = orc.quant_weights(w1) + orc.quant_weights(w2)
     layer = S.MegaMoELayer(H, I, E, K, max_rows=max_rows or max(T, 1), fuse_fc1=fuse,
-                           emit_fc1=emit, capacity_factor=cf, gemm=gemm)
+                           emit_fc1=emit, capacity_factor=cf, gemm=gemm, gemms=gemms)
     layer.bind_weights(q1, s1, q2, s2)
     return layer, wo
 
@@ -248,6 +248,29 @@ def test_all_masked_and_nan_masked_weights(lib, orc):
     out = layer.forward(xt, it, wt)
     assert layer.read_status() == (0, 0)
     compare_outputs(layer.debug(), out, ref, np.zeros(0, np.int64), check_gu=False)
+
+
+@pytest.mark.parametrize("gemm", ["single", "pair"])
+@pytest.mark.parametrize("fuse,gemms", [(True, "split"), (True, "one_launch"), (False, "split")])
+def test_poisoned_padding_rows_change_nothing(lib, orc, gemm, fuse, gemms):
+    """The padding rows of the expert segments are computed over but never
+    read into a routed row: filling them with NaN codes, NaN scales and NaN
+    BF16 between two forwards leaves the output bit-identical (the tensor
+    core keeps rows apart; the epilogues skip all-padding quadrants; combine
+    reads y through inv)."""
+    T, H, I, E, K = 300, 512, 384, 8, 4
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=71)
+    layer, wo = layer_from_float(lib, orc, T, H, I, E, K, w1, w2, fuse=fuse, gemm=gemm, gemms=gemms)
+    xt, it, wt = gh.to_device(x, idx, w)
+    first = layer.forward(xt, it, wt).clone()
+    assert layer.read_status() == (0, 0)
+    assert gh.poison_padding(layer) > 0
+    again = layer.forward(xt, it, wt)
+    assert layer.read_status() == (0, 0)
+    assert torch.equal(again.view(torch.int16), first.view(torch.int16))
+    ref = orc.forward(x, idx, w, *wo)
+    dbg = layer.debug()
+    compare_outputs(dbg, again, ref, check_routing(dbg, ref, T, K))
 
 
 @pytest.mark.parametrize("gemm", ["single", "pair"])
