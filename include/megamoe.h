@@ -242,12 +242,16 @@ MOE_API moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t
  */
 MOE_API moe_status moe_read_status(moe_handle* h, uint32_t* h_status, struct CUstream_st* stream);
 
-/* Device pointers to internal buffers and their layouts, for tests and tools. */
+/* Device pointers to internal buffers and their layouts, for tests and tools.
+ * The rows of a, gu, hq and y (and their scale bytes) that lie inside an
+ * expert's padded segment but past its routed rows hold unspecified values:
+ * the kernels compute over them but never store them or read them into a
+ * routed row. */
 typedef struct moe_debug_view {
   uint32_t* status;        /* device status word */
   int32_t* counts;         /* [E] rows per expert */
   int32_t* offsets;        /* [E+1] exclusive scan of counts (unpadded positions) */
-  int32_t* pad_offsets;    /* [E+1] scan of counts rounded up to 128 (GEMM rows) */
+  int32_t* pad_offsets;    /* [E+1] scan of counts rounded up to pad_rows (GEMM rows) */
   int32_t* perm;           /* [R] route id r = t*K + k at unpadded position pos */
   int32_t* inv;            /* [T*K] unpadded position of route r, or -1 */
   int32_t* inv_pad;        /* [T*K] padded GEMM row of route r, or -1 */
