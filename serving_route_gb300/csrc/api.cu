@@ -31,6 +31,7 @@ struct moe_handle {
   int pair_ctas;                            // grid of the CTA-pair GEMMs
   int sm_budget;                            // moe_set_sm_budget (0: every SM)
   int route_coop_blocks;                    // co-resident grid limit of the one-kernel routing
+  int quant_resident[2];                    // resident blocks of quant_dispatch, 2 / 4 units per pass
   bool bound;
   uint16_t* out;
   int num_sms;
@@ -294,6 +295,8 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   h->expected_m = expected_m;
   h->num_sms = sms;
   h->route_coop_blocks = route_fused_max_blocks(L.E);
+  h->quant_resident[0] = quant_dispatch_resident(L.mx, 2);
+  h->quant_resident[1] = quant_dispatch_resident(L.mx, 4);
   h->device = dev;
   uint8_t* b = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(d_workspace), kAlign));
   Workspace& w = h->ws;
@@ -440,7 +443,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   // cannot be confined to a subset of SMs, and one CTA per budgeted SM
   // starves them of memory parallelism.  The budget caps the persistent GEMM.
   const int stream_ctas = 16 * h->num_sms;
-  if (launch_quant_dispatch(ws, L, d_x, num_tokens, s, pdl, stream_ctas) != cudaSuccess)
+  if (launch_quant_dispatch(ws, L, d_x, num_tokens, s, pdl, stream_ctas, h->quant_resident[0],
+                            h->quant_resident[1]) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   GemmArgs g1;

@@ -83,10 +83,15 @@ cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* to
 int route_fused_max_blocks(int E);
 
 // quant.cu
+// Resident blocks (all SMs) of quant_dispatch with two or four units per
+// warp pass (batch 2 or 4); 0 if the query fails.
+int quant_dispatch_resident(bool mx, int batch);
 // pdl: launch as a programmatic dependent of the previous kernel on `s`;
-// max_ctas: grid cap of the streaming kernels
+// max_ctas: grid cap of the streaming kernels; resident2 / resident4: the
+// two forms' resident blocks (four units per warp where that makes one wave)
 cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
-                                  int64_t T, cudaStream_t s, bool pdl, int max_ctas);
+                                  int64_t T, cudaStream_t s, bool pdl, int max_ctas,
+                                  int resident2, int resident4);
 cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int max_ctas, cudaStream_t s,
                                 bool pdl);
 cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,

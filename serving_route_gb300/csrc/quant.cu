@@ -45,8 +45,8 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 p, float (&v)[8]) {
 
 // One warp handles four 128-column blocks of one token per unit: eight lanes
 // per block, each lane owning 16 consecutive columns (two 16-byte loads, one
-// 16-byte store per route).  Each iteration processes two units whose loads
-// are issued together, so every warp keeps 2 KB of reads in flight, and each
+// 16-byte store per route).  Each pass processes B units whose loads are
+// issued together, so every warp keeps B KB of reads in flight, and each
 // store instruction of the warp writes four whole 128-byte lines.
 __device__ __forceinline__ float group8_max(float v) {
 #pragma unroll
@@ -100,8 +100,11 @@ __device__ __forceinline__ void quant_dispatch_unit(const uint4 (&raw)[2], bool 
   }
 }
 
-template <bool MX>
-__global__ void __launch_bounds__(256) quant_dispatch_kernel(
+// B = 2: two units per pass, one unit per warp while the grid is not capped.
+// B = 4: four units per pass at 64 registers (four blocks per SM), for a grid
+// that then fits in one wave.
+template <bool MX, int B>
+__global__ void __launch_bounds__(256, B == 4 ? 4 : 1) quant_dispatch_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pad, int64_t T, int H, int K,
     uint8_t* __restrict__ a, uint8_t* __restrict__ a_sf) {
   const int lane = threadIdx.x & 31, grp = lane >> 3, l8 = lane & 7;
@@ -109,36 +112,43 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
   const int units = (KB + 3) >> 2;
   const int64_t total = T * units;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  // x is an input of the forward that no kernel of it writes: a warp's first
-  // loads are issued before the programmatic wait, so their latency overlaps
-  // the routing kernel's tail.  The routing tables (inv_pad) and every store
-  // come after the wait.
+  // x is an input of the forward that no kernel of it writes: a warp issues
+  // the loads of its first pass before the programmatic wait, so their
+  // latency overlaps the routing kernel's tail.  When every warp's work is
+  // that one pass and the grid is one wave, nothing is left to load after
+  // the routing ends.  The routing tables (inv_pad) and every store come
+  // after the wait.
   bool waited = false;
   for (int64_t u0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u0 < total;
-       u0 += 2 * nwarps) {
-    const int64_t u1 = u0 + nwarps;
-    const bool has1 = u1 < total;
-    const int64_t t0 = u0 / units, t1 = has1 ? u1 / units : t0;
-    const int b0 = (int)(u0 - t0 * units) * 4 + grp;
-    const int b1 = has1 ? (int)(u1 - t1 * units) * 4 + grp : b0;
-    const bool v0 = b0 < KB, v1 = has1 && b1 < KB;
-    // both units' loads first
-    uint4 r0[2], r1[2];
+       u0 += B * nwarps) {
+    uint4 r[B][2];
+    int t[B];  // tokens fit in 32 bits: route ids t*K+k are int32
+    int b[B];
+    bool v[B];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      r0[h] = v0 ? *reinterpret_cast<const uint4*>(x + t0 * H + b0 * 128 + l8 * 16 + h * 8)
-                 : make_uint4(0u, 0u, 0u, 0u);
-      r1[h] = v1 ? *reinterpret_cast<const uint4*>(x + t1 * H + b1 * 128 + l8 * 16 + h * 8)
-                 : make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 0; i < B; ++i) {
+      const int64_t u = u0 + i * nwarps;
+      const bool in = u < total;
+      t[i] = in ? (int)(u / units) : 0;
+      b[i] = in ? (int)(u - (int64_t)t[i] * units) * 4 + grp : KB;
+      v[i] = b[i] < KB;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        r[i][h] = v[i] ? *reinterpret_cast<const uint4*>(x + (int64_t)t[i] * H + b[i] * 128 +
+                                                         l8 * 16 + h * 8)
+                       : make_uint4(0u, 0u, 0u, 0u);
     }
     if (!waited) {
       pdl_wait();
       waited = true;
     }
-    const int p0 = (lane < K) ? inv_pad[t0 * K + lane] : -1;
-    const int p1 = (lane < K && has1) ? inv_pad[t1 * K + lane] : -1;
-    quant_dispatch_unit<MX>(r0, v0, p0, b0, H, K, l8, a, a_sf);
-    quant_dispatch_unit<MX>(r1, v1, p1, b1, H, K, l8, a, a_sf);
+    int p[B];
+#pragma unroll
+    for (int i = 0; i < B; ++i)
+      p[i] = (lane < K && u0 + i * nwarps < total) ? inv_pad[(int64_t)t[i] * K + lane] : -1;
+#pragma unroll
+    for (int i = 0; i < B; ++i)
+      quant_dispatch_unit<MX>(r[i], v[i], p[i], b[i], H, K, l8, a, a_sf);
   }
   pdl_trigger();
 }
@@ -341,12 +351,35 @@ static int stream_grid(int64_t work, int per_block, int64_t cap = 152 * 16) {
   return (int)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 
+int quant_dispatch_resident(bool mx, int batch) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  const void* k = batch == 4 ? (mx ? (const void*)quant_dispatch_kernel<true, 4>
+                                   : (const void*)quant_dispatch_kernel<false, 4>)
+                             : (mx ? (const void*)quant_dispatch_kernel<true, 2>
+                                   : (const void*)quant_dispatch_kernel<false, 2>);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 256, 0) != cudaSuccess) return 0;
+  return per_sm * sms;
+}
+
 cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
-                                  int64_t T, cudaStream_t s, bool pdl, int max_ctas) {
-  const int64_t warps = T * ((L.H / 128 + 3) / 4);
-  return launch_k(L.mx ? quant_dispatch_kernel<true> : quant_dispatch_kernel<false>,
-                  dim3(stream_grid(warps, 8, max_ctas)), dim3(256), 0, s, pdl, nullptr,
-                  x, (const int32_t*)ws.inv_pad, T, L.H, L.K, ws.a, ws.a_sf);
+                                  int64_t T, cudaStream_t s, bool pdl, int max_ctas,
+                                  int resident2, int resident4) {
+  // one unit = four 128-column blocks of a token, eight warps per block
+  const int64_t units = T * ((L.H / 128 + 3) / 4);
+  const int g2 = stream_grid(units, 8, max_ctas), g4 = stream_grid(units, 32, max_ctas);
+  // four units per warp only where one unit per warp would take more than
+  // one wave and four per warp fit in one
+  const bool b4 = g2 > resident2 && g4 <= resident4 && g4 < max_ctas;
+  if (b4)
+    return launch_k(L.mx ? quant_dispatch_kernel<true, 4> : quant_dispatch_kernel<false, 4>,
+                    dim3(g4), dim3(256), 0, s, pdl, nullptr, x, (const int32_t*)ws.inv_pad, T, L.H,
+                    L.K, ws.a, ws.a_sf);
+  return launch_k(L.mx ? quant_dispatch_kernel<true, 2> : quant_dispatch_kernel<false, 2>,
+                  dim3(g2), dim3(256), 0, s, pdl, nullptr, x, (const int32_t*)ws.inv_pad, T, L.H,
+                  L.K, ws.a, ws.a_sf);
 }
 
 cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int max_ctas,
