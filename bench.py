@@ -34,6 +34,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer routed TFLOPS & tokens/s on 1 GB300; % of FP8-peak/HBM roofline"
+L2_WARM_STEPS = 200  # back-to-back steps of the L2-warm figure
+
 KERNELS = ["status_reset", "route_count", "route_scan", "route_scatter", "quant_dispatch", "fc1",
            "swiglu_quant", "fc2", "combine"]
 
@@ -518,6 +520,19 @@ def main():
     if world > 1:
         dist.barrier()
     total_ms = reduce_max(total_ms, dev)
+    # beside the flushed figure: the same capture replayed back to back with
+    # nothing flushed between steps (whatever of the working set L2 keeps)
+    n_warm = min(L2_WARM_STEPS, args.steps)
+    with torch.cuda.stream(stream):
+        flush.zero_()
+        for _ in range(3):
+            step(graph, False)
+        t_start.record(stream)
+        for _ in range(n_warm):
+            step(graph, False)
+        t_end.record(stream)
+    stream.synchronize()
+    l2_warm_ms = reduce_max(t_start.elapsed_time(t_end), dev) / n_warm
     # per-kernel times: the same number of steps of the profiled capture
     timed_steps(min(args.warmup, 3), True)
     prof_ms, per_kernel = timed_steps(args.steps, True)
@@ -677,6 +692,8 @@ def main():
         "roofline": roof,
         "step_ms": {"median": float(np.median(step_times)), "p10": float(np.percentile(step_times, 10)),
                     "p90": float(np.percentile(step_times, 90))},
+        "l2_warm": {"ms_per_step": l2_warm_ms, "steps": n_warm,
+                    "how": "the same capture replayed back to back, L2 not flushed (not the value)"},
         "kernel_ms": kern_ms,
         "kernel_ms_source": ("CUDA events before every kernel, a second capture of the same forward "
                              f"replayed for the same {K} steps right after the timed ones "

@@ -50,6 +50,7 @@ def test_main_line(fmt):
     assert d["gpu_launches"] > 0 and d["gpu_launches"] % d["steps"] == 0
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     assert {"median", "p10", "p90"} <= set(d["step_ms"])
+    assert d["l2_warm"]["ms_per_step"] > 0 and d["l2_warm"]["steps"] >= 1
     assert d["config"]["format"].startswith("MXFP8" if fmt == "mxfp8" else "E4M3")
 
 
