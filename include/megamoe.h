@@ -105,6 +105,13 @@ typedef enum moe_status {
  * #4069).  The tensor core applies every scale (one per 32-wide MMA K step),
  * so the GEMMs copy one scale atom per K block instead of one per four. */
 #define MOE_FLAG_MXFP8 0x100u
+/* Test only: exercises the routing kernel's grid barrier.  With this flag the
+ * one-kernel routing waits at most 20 ms at its barrier, and its last block
+ * withholds its arrival (forwards that route in one kernel with at least two
+ * blocks, i.e. more than 512 tokens): every block records MOE_DEV_TIMEOUT and
+ * marks its routes unrouted, so the forward computes no expert and writes a
+ * zero output, and the context stays usable. */
+#define MOE_FLAG_WATCHDOG_ROUTE_TEST 0x200u
 
 typedef struct moe_dims {
   int32_t hidden;      /* H: multiple of 128, 128..16384 */

@@ -41,6 +41,7 @@ MOE_FLAG_WATCHDOG_TEST = 0x20
 MOE_FLAG_SPLIT_GEMMS = 0x40
 MOE_FLAG_GEMMS_ONE_LAUNCH = 0x80
 MOE_FLAG_MXFP8 = 0x100
+MOE_FLAG_WATCHDOG_ROUTE_TEST = 0x200
 
 # every function the header declares (checked against include/megamoe.h by a test)
 API_NAMES = ("moe_workspace_query", "moe_create", "moe_quantize_weights", "moe_quantize_weights_mx",

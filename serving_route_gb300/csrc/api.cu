@@ -432,7 +432,7 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   // cooperative grid would have to be resident beside the side-stream work.
   const int coop = plan.route_kernels == 1 ? h->route_coop_blocks : 0;
   if (launch_route(ws, L, d_topk_idx, d_topk_w, num_tokens, check, s, ev ? ev + 1 : nullptr,
-                   coop) != cudaSuccess)
+                   coop, (h->dims.flags & MOE_FLAG_WATCHDOG_ROUTE_TEST) != 0) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[4], s);
   // Kernels after the first are programmatic dependents of their predecessor

@@ -228,7 +228,8 @@ __global__ void __launch_bounds__(kFusedTokens) route_fused_kernel(
     uint32_t* __restrict__ grid_sync, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ pad_offsets, int32_t* __restrict__ mtile_expert,
     int32_t* __restrict__ total_mtiles, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-    int32_t* __restrict__ inv_pad, uint32_t* __restrict__ status, uint64_t wait_limit_ns) {
+    int32_t* __restrict__ inv_pad, uint32_t* __restrict__ status, uint64_t wait_limit_ns,
+    int withhold) {
   extern __shared__ int32_t sm[];
   int32_t* wh = sm;                   // [warps][E]: per-warp counts, then running bases
   int32_t* bu = sm + kRouteWarps * E;  // [E]: expert totals, then this block's unpadded bases
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(kFusedTokens) route_fused_kernel(
   __syncthreads();
   if (tid == 0) {
     __threadfence();  // this block's histogram row before its arrival
-    atomicAdd(grid_sync, 1u);
+    if (b != withhold) atomicAdd(grid_sync, 1u);  // withhold: the barrier test's missing block
     bool ok = true;
     const uint64_t t0 = globaltimer_ns();
     while (ld_acquire_gpu_u32(grid_sync) < (uint32_t)nb) {
@@ -434,7 +435,7 @@ int route_fused_max_blocks(int E) {
 
 cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* topk_idx,
                          const float* topk_w, int64_t T, bool check, cudaStream_t s,
-                         cudaEvent_t const* ev, int coop_max_blocks) {
+                         cudaEvent_t const* ev, int coop_max_blocks, bool watchdog_test) {
   const int nb = (int)((T + kRouteTokens - 1) / kRouteTokens);
   const int E = L.E;
   const int max_mtiles = (int)(L.rows_alloc / 128);
@@ -449,7 +450,9 @@ cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* to
         route_fused_kernel, dim3(nb_fused), dim3(kFusedTokens), route_fused_smem(E), s, false, &coop,
         topk_idx, topk_w, (int)T, L.K, E, check ? 1 : 0, pad_rows, L.rows_alloc, max_mtiles,
         ws.block_counts, ws.grid_sync, ws.counts, ws.offsets, ws.pad_offsets, ws.mtile_expert,
-        ws.total_mtiles, ws.perm, ws.inv, ws.inv_pad, ws.status, (uint64_t)kWaitLimitNs);
+        ws.total_mtiles, ws.perm, ws.inv, ws.inv_pad, ws.status,
+        watchdog_test ? (uint64_t)20000000ull : (uint64_t)kWaitLimitNs,
+        watchdog_test && nb_fused > 1 ? nb_fused - 1 : -1);
     if (ev) {  // the scan and scatter are inside the one kernel: zero-length spans
       record_event(ev[1], s);
       record_event(ev[2], s);

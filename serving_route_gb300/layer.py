@@ -18,7 +18,7 @@ class MegaMoELayer:
                  fuse_fc1: bool = False, check_routes: bool = True, emit_fc1: bool = False,
                  gemm: str = "auto", watchdog_test: bool = False, device="cuda",
                  workspace: torch.Tensor | None = None, gemms: str = "auto",
-                 fmt: str = "deepseek"):
+                 fmt: str = "deepseek", watchdog_route_test: bool = False):
         """gemm: "auto" (tactic from expected_m), "single" (one CTA per SM) or
         "pair" (CTA pairs, tcgen05 cta_group::2).  gemms (fused epilogue only):
         "auto" (FC1 -> FC2 in one persistent launch for short forwards, two
@@ -40,6 +40,7 @@ class MegaMoELayer:
                       | {"auto": 0, "single": B.MOE_FLAG_GEMM_SINGLE_CTA,
                          "pair": B.MOE_FLAG_GEMM_CTA_PAIR}[gemm]
                       | (B.MOE_FLAG_WATCHDOG_TEST if watchdog_test else 0)
+                      | (B.MOE_FLAG_WATCHDOG_ROUTE_TEST if watchdog_route_test else 0)
                       | {"auto": 0, "one_launch": B.MOE_FLAG_GEMMS_ONE_LAUNCH,
                          "split": B.MOE_FLAG_SPLIT_GEMMS}[gemms]
                       | (B.MOE_FLAG_MXFP8 if fmt == "mxfp8" else 0))

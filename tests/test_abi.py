@@ -32,6 +32,15 @@ def test_every_declared_symbol_is_exported(B):
     assert sorted(B.API_NAMES) == names
 
 
+def test_header_constants_match_the_binding(B):
+    """every #define MOE_* of the header has the same value in the binding"""
+    src = open(os.path.join(ROOT, "include", "megamoe.h")).read()
+    defs = dict(re.findall(r"#define\s+(MOE_\w+)\s+(0x[0-9a-fA-F]+|\d+)u?\b", src))
+    assert len(defs) >= 15 and "MOE_FLAG_WATCHDOG_ROUTE_TEST" in defs
+    for name, val in defs.items():
+        assert getattr(B, name) == int(val, 0), name
+
+
 def test_status_strings(B):
     assert B.status_str(B.MOE_OK) == "ok"
     assert "capacity" in B.status_str(B.MOE_ERR_CAPACITY)

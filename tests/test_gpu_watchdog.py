@@ -1,6 +1,7 @@
 """Device watchdog (failure detection without a GPU fault).
 
-Every wait inside the GEMM kernels is bounded.  With MOE_FLAG_WATCHDOG_TEST
+Every wait inside the GEMM kernels and the routing kernel's grid barrier is
+bounded.  With MOE_FLAG_WATCHDOG_TEST
 the first GEMM CTA withholds one pipeline stage -- a barrier that nothing
 completes; on CTA pairs the first pair's second CTA withholds its share, which
 the leader's barrier still expects -- and the wait bound drops to 20 ms: the
@@ -48,6 +49,39 @@ def test_watchdog_expires_with_status_and_context_survives(orc, split, gemm):
 
     # the context is intact: a normal forward right after is correct
     good = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm=gemm)
+    good.bind_weights(q1, s1, q2, s2)
+    out = good.forward(xt, it, wt)
+    assert good.read_status() == (0, 0)
+    ref = orc.forward(x, idx, w, *orc.quant_weights(w1), *orc.quant_weights(w2))
+    compare_outputs(good.debug(), out, ref, np.zeros(0, np.int64), check_gu=False)
+
+
+def test_routing_barrier_expires_with_status_and_context_survives(orc):
+    """MOE_FLAG_WATCHDOG_ROUTE_TEST: the one-kernel routing's last block never
+    arrives at the grid barrier.  Every block gives up after 20 ms, records
+    MOE_DEV_TIMEOUT and marks its routes unrouted, so no expert is computed
+    and the output is zero; a normal forward on the same context right after
+    is correct."""
+    import __graft_entry__ as ge
+    ge.build()
+    import serving_route_gb300 as S
+    import serving_route_gb300.binding as B
+
+    T, H, I, E, K = 1100, 256, 256, 8, 2           # three routing blocks of 512 tokens
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=33)
+    q1, s1 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w1).cuda())
+    q2, s2 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w2).cuda())
+    xt, it, wt = gh.to_device(x, idx, w)
+
+    bad = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, watchdog_route_test=True)
+    assert bad.route_kernels(T) == 1
+    bad.bind_weights(q1, s1, q2, s2)
+    out = bad.forward(xt, it, wt)
+    st, bits = bad.read_status()
+    assert st == B.MOE_ERR_DEVICE_TIMEOUT and bits & B.MOE_DEV_TIMEOUT, (st, bits)
+    assert not torch.any(out[:T].view(torch.int16))
+
+    good = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True)
     good.bind_weights(q1, s1, q2, s2)
     out = good.forward(xt, it, wt)
     assert good.read_status() == (0, 0)
