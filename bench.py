@@ -158,12 +158,13 @@ def algorithmic_bytes(wl, counts):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    """nvidia-smi SM and memory clocks, power and throttle reasons, sampled
+    every 100 ms."""
 
     def __init__(self, index: int):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,clocks.mem")
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={q}",
                                        "--format=csv,noheader,nounits", "-lms", "100"],
@@ -177,7 +178,7 @@ class ClockSampler:
         time.sleep(0.25)
         self.p.terminate()
         out, _ = self.p.communicate(timeout=10)
-        sm, smax, reasons = [], [], set()
+        sm, smax, mem, power, reasons = [], [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
@@ -191,8 +192,15 @@ class ClockSampler:
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+            for dst, v in ((power, f[3]), (mem, f[9] if len(f) > 9 else "")):
+                try:
+                    dst.append(float(v))
+                except ValueError:
+                    pass
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "mem_mhz": statistics.median(mem) if mem else None,
+                "power_w": statistics.median(power) if power else None,
                 "reasons": sorted(reasons)}
 
 
