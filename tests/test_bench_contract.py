@@ -61,3 +61,26 @@ def test_side_stream_sweep_line():
     assert d["unit"] == "ms" and d["higher_is_better"] is False
     assert d["layer_ms"] > 0 and d["mlp_ms"] > 0 and d["serial_ms"] > 0
     assert len(d["concurrent"]) >= 2 and all(p["ms"] > 0 for p in d["concurrent"])
+
+
+@pytest.mark.parametrize("name,touched,gb", [
+    ("v2lite", 64, 0.5875),      # every expert routed
+    ("v3prefill", 256, 11.512),
+    ("v3decode8", 52, 2.29),     # the experts seed 0 touches at T = 8
+])
+def test_layer_roofline_bytes(name, touched, gb):
+    """The layer roofline's compulsory bytes: FP8 weights and scales of every
+    routed expert, x and out in BF16, the routes; experts with no route cost
+    nothing."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    from gen import configs
+    wl = configs.WORKLOADS[name]
+    counts = np.zeros(wl.E, np.int64)
+    counts[:touched] = 1
+    b, t = bench.algorithmic_bytes(wl, counts)
+    assert t == touched
+    per_expert = 3 * wl.I * wl.H + (2 * wl.I // 128 + wl.I // 128) * (wl.H // 128) * 4
+    assert b == touched * per_expert + wl.T * wl.H * 4 + wl.T * wl.K * 8
+    assert abs(b / 1e9 - gb) < 0.01 * gb
