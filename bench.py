@@ -9,10 +9,17 @@ The timed capture has no events between its kernels; per-kernel times come
 from a second capture with an event before every kernel, replayed for the
 same number of steps right after.
 
+The main line is the DeepSeek-V3-shaped prefill layer (T=8192, H=7168,
+I=2048, E=256, top-8) unless --config says otherwise.  Beside it, under
+"per_workload", the same run times the decode sweep (T = 8, 64, 256, 1024 on
+the same weights), the skewed layer and the DeepSeek-V2-Lite-shaped layer the
+same way (--no-records skips them).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
 --impl reference times the CPU oracle (plain C, float64) as it stands on the
-host cores, on a bounded token sample of the same workload per step.
+host cores, each step a bounded sample of the same workload (every routed row
+of a few random experts).
 Under torchrun (N > 1) every rank runs its own replica of the workload (no
 data-path collective: the layer does not shard on one-GPU machines); the time is
 the max over ranks and the value counts the work of all ranks.
@@ -35,6 +42,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer routed TFLOPS & tokens/s on 1 GB300; % of FP8-peak/HBM roofline"
 L2_WARM_STEPS = 200  # back-to-back steps of the L2-warm figure
+L2_BYTES = 129 << 20  # GB300 L2
+REF_STEP_S = 4.0      # oracle seconds per reference-arm step
+CPU_BASELINE_S = 15.0  # oracle seconds of the cpu_baseline leg
+# the per-workload record printed beside the main line (same run, same method)
+RECORD_CONFIGS = ("v3prefill", "v3decode8", "v3decode64", "v3decode256", "v3decode1024", "skew",
+                  "v2lite")
 
 KERNELS = ["status_reset", "route_count", "route_scan", "route_scatter", "quant_dispatch", "fc1",
            "swiglu_quant", "fc2", "combine"]
@@ -47,7 +60,7 @@ def parse():
                    help="timed steps (0: as many as fill about a second, at least 20, so the "
                         "clock samples fall inside the timed region)")
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--config", default="v2lite")
+    p.add_argument("--config", default="v3prefill")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--unfused", action="store_true", help="time the unfused reference path")
     p.add_argument("--gemm", default="auto", choices=["auto", "single", "pair"])
@@ -66,7 +79,11 @@ def parse():
                    help="cap the SMs the layer occupies (moe_set_sm_budget; 0: every SM)")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-sample-tokens", type=int, default=0)
+    p.add_argument("--no-records", action="store_true",
+                   help="skip the per-workload record beside the main line")
+    p.add_argument("--records", default=",".join(RECORD_CONFIGS),
+                   help="comma-separated workloads of the per-workload record (the main one is "
+                        "skipped there)")
     return p.parse_args()
 
 
@@ -216,36 +233,94 @@ def cpu_threads() -> int:
     return min(n, int(omp)) if omp.isdigit() and int(omp) > 0 else n
 
 
-def oracle_sample(wl, x_bits, idx, w, tokens):
-    """Times the oracle on the listed tokens (a mini-problem of those tokens and
-    the experts they route to); returns (seconds, routed FLOPs of the sample)."""
-    import oracle
-    from gen import problem
-    sub = idx[tokens]
-    experts = sorted(set(int(e) for e in sub.ravel() if e >= 0))
-    remap = {e: i for i, e in enumerate(experts)}
-    mini = np.vectorize(lambda e: remap.get(int(e), -1))(sub).astype(np.int32)
-    w1q, w1s = oracle.quant_weights(problem.w1_f32(wl, experts))
-    w2q, w2s = oracle.quant_weights(problem.w2_f32(wl, experts))
-    t0 = time.perf_counter()
-    r = oracle.forward(x_bits[tokens], mini, w[tokens], w1q, w1s, w2q, w2s)
-    dt = time.perf_counter() - t0
-    assert r["err"] == 0
-    routes = int((sub >= 0).sum())
-    return dt, 6 * routes * wl.H * wl.I
+class OracleSampler:
+    """Times the oracle on bounded samples of a workload, drawn by expert: a
+    sample is every routed row of a few random non-empty experts (their expert
+    FFN), with the tokens that route there (their quantisation and the combine
+    of those routes).  This keeps the rows per expert of the real workload,
+    which is what the oracle's cost and parallelism depend on (it decodes each
+    expert's weights once per call and runs that expert's rows in parallel),
+    while bounding a sample's work.  Weights are generated and quantised by the
+    oracle's own quantiser for the sampled experts only, outside the timed
+    span, and kept for later samples."""
+
+    def __init__(self, wl, x_bits, idx, w, keep_experts: int = 64):
+        self.wl, self.x, self.idx, self.w = wl, x_bits, idx, w
+        flat = idx.ravel()
+        self.counts = np.bincount(flat[flat >= 0], minlength=wl.E)
+        self.nonempty = np.nonzero(self.counts)[0]
+        self.cache = {}
+        self.keep = keep_experts
+
+    def weights(self, experts):
+        import oracle
+        from gen import problem
+        missing = [e for e in experts if e not in self.cache]
+        for c in range(0, len(missing), 8):
+            part = missing[c:c + 8]
+            w1q, w1s = oracle.quant_weights(problem.w1_f32(self.wl, part))
+            w2q, w2s = oracle.quant_weights(problem.w2_f32(self.wl, part))
+            for i, e in enumerate(part):
+                self.cache[e] = (w1q[i], w1s[i], w2q[i], w2s[i])
+        out = tuple(np.stack([self.cache[e][j] for e in experts]) for j in range(4))
+        while len(self.cache) > self.keep:        # bounded host memory
+            self.cache.pop(next(iter(self.cache)))
+        return out
+
+    def sample(self, n_experts: int, rng):
+        """-> (seconds, routed FLOPs, routed rows, experts) of one timed oracle call."""
+        import oracle
+        n = int(max(1, min(n_experts, len(self.nonempty))))
+        S = np.sort(rng.choice(self.nonempty, size=n, replace=False))
+        inS = np.isin(self.idx, S)
+        tokens = np.nonzero(inS.any(axis=1))[0]
+        remap = np.full(self.wl.E, -1, np.int32)
+        remap[S] = np.arange(n, dtype=np.int32)
+        sub = self.idx[tokens]
+        mini = np.where(inS[tokens], remap[np.clip(sub, 0, self.wl.E - 1)], -1).astype(np.int32)
+        W = self.weights([int(e) for e in S])
+        x = np.ascontiguousarray(self.x[tokens])
+        w = np.ascontiguousarray(self.w[tokens])
+        t0 = time.perf_counter()
+        r = oracle.forward(x, mini, w, *W)
+        dt = time.perf_counter() - t0
+        assert r["err"] == 0
+        rows = int(self.counts[S].sum())
+        return dt, 6 * rows * self.wl.H * self.wl.I, rows, n
+
+    def per_expert_seconds(self, rng) -> float:
+        """calibration: one untimed call on one expert"""
+        dt, _, _, _ = self.sample(1, rng)
+        return max(dt, 1e-3)
 
 
-def cpu_sample_tokens(wl, requested):
-    """tokens whose FFN the oracle times: about 15 s of work on a 16-core host
-    (the oracle sustains roughly 90 GFLOP/s of exact float64 block sums there),
-    or the whole batch when that is smaller"""
-    if requested:
-        return requested
-    routes = 1.4e12 / (6.0 * wl.H * wl.I)
-    return int(max(8, min(wl.T, routes / wl.K)))
+def oracle_bounded_run(wl, x_bits, idx, w, target_s: float, rng):
+    """One bounded sample of about target_s seconds of oracle work: experts are
+    added in doubling batches until the timed calls reach target_s or every
+    non-empty expert has been sampled.  Returns the cpu_baseline fields."""
+    smp = OracleSampler(wl, x_bits, idx, w)
+    total_t = total_f = total_r = total_e = 0
+    n = 1
+    while total_t < target_s and total_e < len(smp.nonempty):
+        n = min(n, len(smp.nonempty) - total_e)
+        dt, fl, rows, ne = smp.sample(n, rng)
+        total_t += dt
+        total_f += fl
+        total_r += rows
+        total_e += ne
+        n *= 2
+    return {"value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+            "kind": "oracle", "seconds": total_t,
+            "sample": f"every routed row of {total_e} random experts of {wl.name} ({total_r} rows; "
+                      "their expert FFN, the quantisation of the tokens routed there and the "
+                      "combine of those routes), in doubling batches up to about "
+                      f"{target_s:.0f} s of oracle time; weights quantised untimed"}
 
 
 def run_reference(args):
+    """The reference arm: the oracle as it stands on the host cores, each step a
+    bounded sample of the workload (every routed row of a few random experts,
+    sized from an untimed one-expert calibration to about REF_STEP_S seconds)."""
     from gen import configs, problem
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -255,26 +330,30 @@ def run_reference(args):
     wl = configs.WORKLOADS[args.config]
     x = problem.x_bits(wl)
     idx, w = wl.make_routes()
-    n_tok = max(1, cpu_sample_tokens(wl, args.cpu_sample_tokens) // max(1, args.steps // 4))
+    smp = OracleSampler(wl, x, idx, w)
     rng = np.random.default_rng(0)
-    times, flops = [], []
+    per_expert = smp.per_expert_seconds(rng)
+    n_exp = int(max(1, min(len(smp.nonempty), round(REF_STEP_S / per_expert))))
+    times, flops, rows = [], [], []
     for s in range(args.warmup + args.steps):
-        toks = np.sort(rng.choice(wl.T, size=min(n_tok, wl.T), replace=False))
-        dt, fl = oracle_sample(wl, x, idx, w, toks)
+        dt, fl, r, _ = smp.sample(n_exp, rng)
         if s >= args.warmup:
             times.append(dt)
             flops.append(fl)
+            rows.append(r)
     total = sum(times)
     value = sum(flops) / total / 1e12
+    sample = (f"every routed row of {n_exp} random experts of {wl.name} per step (mean "
+              f"{statistics.mean(rows):.0f} rows: their expert FFN, the quantisation of the tokens "
+              "routed there and the combine of those routes); weights quantised untimed")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "sample_tokens_per_step": int(n_tok)},
+        "config": {"workload": wl.name, "experts_per_step": n_exp},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
-                         "sample": f"{n_tok} random tokens of {wl.name} per step (their experts' "
-                                   "FFN + combine; routing of the whole batch)"},
+                         "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -360,6 +439,246 @@ def side_stream_sweep(args, torch, layer, x, idx, wts, wl, dev, flush):
         "all_sms_vs_serial": points[0]["ms"] / serial_ms}))
 
 
+def gpu_weights(torch, g, layer_cls, wl, fmt, dev, stream):
+    """Weights of a workload generated on the GPU by the shared seeded
+    generator and quantised there (moe_quantize_weights), in expert chunks."""
+    mx = fmt == "mxfp8"
+    sp = stream.cuda_stream
+    w1q = torch.empty((wl.E, 2 * wl.I, wl.H), dtype=torch.uint8, device=dev)
+    w1s = torch.empty((wl.E, 2 * wl.I, wl.H // 32) if mx else (wl.E, 2 * wl.I // 128, wl.H // 128),
+                      dtype=torch.float32, device=dev)
+    w2q = torch.empty((wl.E, wl.H, wl.I), dtype=torch.uint8, device=dev)
+    w2s = torch.empty((wl.E, wl.H, wl.I // 32) if mx else (wl.E, wl.H // 128, wl.I // 128),
+                      dtype=torch.float32, device=dev)
+    chunk = 16
+    with torch.cuda.stream(stream):
+        for e0 in range(0, wl.E, chunk):
+            ne = min(chunk, wl.E - e0)
+            f = torch.empty((ne, 2 * wl.I, wl.H), dtype=torch.float32, device=dev)
+            g.dev_normal_f32(wl.seed, g.STREAM_W1, e0 * 2 * wl.I * wl.H, f.numel(),
+                             g.weight_sigma(wl.H), f.data_ptr(), sp)
+            q, s = layer_cls.quantize_weights(f, stream, fmt=fmt)
+            w1q[e0:e0 + ne].copy_(q)
+            w1s[e0:e0 + ne].copy_(s)
+            f = torch.empty((ne, wl.H, wl.I), dtype=torch.float32, device=dev)
+            g.dev_normal_f32(wl.seed, g.STREAM_W2, e0 * wl.H * wl.I, f.numel(),
+                             g.weight_sigma(wl.I), f.data_ptr(), sp)
+            q, s = layer_cls.quantize_weights(f, stream, fmt=fmt)
+            w2q[e0:e0 + ne].copy_(q)
+            w2s[e0:e0 + ne].copy_(s)
+            del f, q, s
+    stream.synchronize()
+    return w1q, w1s, w2q, w2s
+
+
+def device_inputs(torch, g, wl, dev, stream):
+    """x on the GPU from the device generator; routes from the host recipe."""
+    x = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
+    g.dev_normal_bf16(wl.seed, g.STREAM_X, 0, wl.T * wl.H, x.data_ptr(), stream.cuda_stream)
+    idx_np, w_np = wl.make_routes()
+    idx = torch.from_numpy(idx_np).to(dev)
+    wts = torch.from_numpy(w_np).to(dev)
+    flat = idx_np.ravel()
+    counts = np.bincount(flat[flat >= 0], minlength=wl.E)
+    return x, idx, wts, idx_np, w_np, counts
+
+
+class StepTimer:
+    """Device timing of whole forwards, the same way for every workload: two CUDA
+    graph captures of the forward -- the timed one has no events between its
+    kernels (each kernel after the first launches as a programmatic dependent
+    of the previous one); the profiled one records an event before every
+    kernel, which gives the per-kernel times.  L2 is flushed (a 256 MiB write on
+    the stream, outside the timed span) before every step; each step is
+    bracketed by CUDA events on the launching stream."""
+
+    def __init__(self, torch, layer, x, idx, wts, stream, flush, use_graph):
+        self.torch, self.layer, self.stream, self.flush = torch, layer, stream, flush
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)]
+        self.t0 = torch.cuda.Event(enable_timing=True)
+        self.t1 = torch.cuda.Event(enable_timing=True)
+        self.fwd = lambda: layer.forward(x, idx, wts, stream=stream)
+        with torch.cuda.stream(stream):
+            self.fwd()
+        stream.synchronize()
+        st, bits = layer.read_status(stream)
+        if st != 0:
+            raise RuntimeError(f"forward reported device status {bits:#x}")
+        self.graph = self._capture() if use_graph else None
+        layer.set_profile_events(self.ev)
+        self.graph_prof = self._capture() if use_graph else None
+        layer.set_profile_events([])
+
+    def _capture(self):
+        torch = self.torch
+        try:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=self.stream):
+                self.fwd()
+            self.stream.synchronize()
+            return gr
+        except Exception as e:  # fall back to direct launches
+            print(f"# graph capture failed ({e}); timing direct launches", file=sys.stderr)
+            return None
+
+    def _step(self, profiled):
+        torch = self.torch
+        gr = self.graph_prof if profiled else self.graph
+        if profiled:
+            self.layer.set_profile_events(self.ev)
+        with torch.cuda.stream(self.stream):
+            if gr is not None:
+                gr.replay()
+            else:
+                self.fwd()
+        if profiled:
+            self.layer.set_profile_events([])
+
+    def steps(self, n, profiled=False, keep=None):
+        """n flushed, event-timed steps -> (total ms, per-kernel ms summed)"""
+        torch, s = self.torch, self.stream
+        tot = 0.0
+        per_kernel = {k: 0.0 for k in KERNELS}
+        for _ in range(n):
+            with torch.cuda.stream(s):
+                self.flush.zero_()
+                self.t0.record(s)
+            self._step(profiled)
+            with torch.cuda.stream(s):
+                self.t1.record(s)
+            s.synchronize()
+            dt = self.t0.elapsed_time(self.t1)
+            tot += dt
+            if keep is not None:
+                keep.append(dt)
+            if profiled:
+                for i, k in enumerate(KERNELS):
+                    per_kernel[k] += self.ev[i].elapsed_time(self.ev[i + 1])
+        return tot, per_kernel
+
+    def l2_warm(self, n):
+        """ms per step of the same capture replayed back to back, nothing flushed"""
+        torch, s = self.torch, self.stream
+        with torch.cuda.stream(s):
+            self.flush.zero_()
+            for _ in range(3):
+                self._step(False)
+            self.t0.record(s)
+            for _ in range(n):
+                self._step(False)
+            self.t1.record(s)
+        s.synchronize()
+        return self.t0.elapsed_time(self.t1) / n
+
+    def check_status(self, what):
+        st, bits = self.layer.read_status(self.stream)
+        if st != 0:
+            raise RuntimeError(f"{what} reported device status {bits:#x}")
+
+
+def kernel_times(layer, T, per_kernel, K):
+    """per-kernel ms per step, named by what ran (one routing kernel or three)"""
+    kern_ms = {k: v / K for k, v in per_kernel.items()}
+    plan = layer.plan(T)
+    if plan["route_kernels"] == 1:  # one cooperative routing kernel: its whole time is in the first span
+        kern_ms["route_fused"] = kern_ms.pop("route_count")
+        kern_ms.pop("route_scan")
+        kern_ms.pop("route_scatter")
+    return kern_ms, plan
+
+
+def rooflines(wl, counts, kern_ms, ms_step):
+    """The layer roofline and the dominant kernel's (FC1).  FP8 dense peak = 2 x
+    the measured BF16 burst figure (the nominal FP8:BF16 ratio, 4.5 : 2.25): a
+    forward is a kernel chain timed in isolation, so the burst figure is its
+    denominator; the fraction of 2 x the sustained figure (measured back to
+    back under the power cap) is reported beside it, never in its place."""
+    hbm, bf16, bf16_sus, src = peaks()
+    fp8 = 2.0 * bf16
+    fp8_sus = 2.0 * bf16_sus if bf16_sus else None
+    flops = wl.routed_flops
+    b_alg, touched = algorithmic_bytes(wl, counts)
+    t_fp8, t_hbm = flops / (fp8 * 1e12), b_alg / (hbm * 1e9)
+    t_roof = max(t_fp8, t_hbm)
+    tflops = flops / (ms_step * 1e-3) / 1e12
+    layer = {"t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
+             "bound": "fp8 tensor" if t_fp8 >= t_hbm else "hbm",
+             "b_alg_bytes": b_alg, "experts_touched": touched,
+             "fp8_peak_tflops": fp8, "fp8_peak": "2 x measured bf16 burst", "hbm_gbs": hbm,
+             "fp8_peak_frac": tflops / fp8,
+             "fp8_peak_frac_vs_sustained": (tflops / fp8_sus) if fp8_sus else None,
+             "source": src}
+    R = int(counts.sum())
+    fc1_flops = 2 * R * wl.H * 2 * wl.I
+    fc1_ms = kern_ms["fc1"]
+    fc1_bytes = touched * (2 * wl.I * wl.H) + R * wl.H
+    if fc1_flops / fc1_bytes >= fp8 * 1e12 / (hbm * 1e9):
+        roof = {"bound": "tensor", "achieved": fc1_flops / (fc1_ms * 1e-3) / 1e12, "peak": fp8,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": fc1_bytes / (fc1_ms * 1e-3) / 1e9, "peak": hbm,
+                "unit": "GB/s"}
+    roof.update({"frac": roof["achieved"] / roof["peak"],
+                 "traffic": recorded_traffic(wl.name, "fc1"), "kernel": "fc1",
+                 "algorithmic_flops": fc1_flops, "algorithmic_bytes": fc1_bytes,
+                 "peak_source": f"{src}: FP8 = 2 x bf16 burst" if roof["bound"] == "tensor"
+                 else f"{src}: hbm copy"})
+    return layer, roof, tflops
+
+
+def tactic_str(layer, plan):
+    t = layer.tactic()
+    return {"gemm": ("cta pairs" if t["gemm_pair"] else "single cta") + f" x{t['gemm_ctas']}",
+            "routing": "one cooperative kernel" if plan["route_kernels"] == 1 else "three kernels",
+            "gemms": ("FC1 + FC2 in one persistent launch" if plan["gemm_launches"] == 1
+                      else "two launches")}
+
+
+def l2_note(wl, b_alg):
+    return ("flushed before every step (256 MiB write, untimed)"
+            + (f"; the step also streams {b_alg / 1e9:.2f} GB of compulsory bytes, more than L2"
+               if b_alg > L2_BYTES else ""))
+
+
+def measure_record(torch, S, g, name, args, dev, stream, flush, weights_cache):
+    """One workload of the per-workload record: the main line's device timing
+    method (graph replay, L2 flushed before every step, W warm-up and K timed
+    steps, per-kernel times from the profiled capture)."""
+    from gen import configs
+    wl = configs.WORKLOADS[name]
+    key = (wl.H, wl.I, wl.E, wl.seed)
+    if key not in weights_cache:
+        weights_cache.clear()
+        torch.cuda.empty_cache()
+        weights_cache[key] = gpu_weights(torch, g, S.MegaMoELayer, wl, args.format, dev, stream)
+    layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, expected_m=wl.T,
+                           fuse_fc1=not args.unfused, check_routes=True, gemm=args.gemm,
+                           gemms=args.gemms, fmt=args.format)
+    layer.bind_weights(*weights_cache[key], stream)
+    x, idx, wts, _, _, counts = device_inputs(torch, g, wl, dev, stream)
+    torch.cuda.synchronize()
+    timer = StepTimer(torch, layer, x, idx, wts, stream, flush, not args.no_graph)
+    K = max(args.steps, 1)
+    timer.steps(args.warmup)
+    times = []
+    total, _ = timer.steps(K, keep=times)
+    timer.steps(min(args.warmup, 3), True)
+    _, per_kernel = timer.steps(K, True)
+    timer.check_status(f"{name} forwards")
+    ms = total / K
+    kern_ms, plan = kernel_times(layer, wl.T, per_kernel, K)
+    lroof, roof, tflops = rooflines(wl, counts, kern_ms, ms)
+    rec = {"workload": wl.name, "T": wl.T, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+           "step_ms": {"median": float(np.median(times)), "p10": float(np.percentile(times, 10)),
+                       "p90": float(np.percentile(times, 90))},
+           "tflops": tflops, "tokens_per_s": wl.T / (ms * 1e-3), "layer_roofline": lroof,
+           "roofline": roof, "kernel_ms": kern_ms, **tactic_str(layer, plan),
+           "l2": l2_note(wl, lroof["b_alg_bytes"])}
+    del timer, layer, x, idx, wts
+    torch.cuda.synchronize()
+    return rec
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -391,49 +710,23 @@ def main():
         wl = Workload(name, T, wl.H, wl.I, E, wl.K, wl.routing, wl.seed)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream()
-    sp = stream.cuda_stream
     fused = not args.unfused
 
     layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, expected_m=wl.T,
                            fuse_fc1=fused, check_routes=True, gemm=args.gemm,
                            gemms=args.gemms, fmt=args.format)
-    # weights: generated and quantised on the GPU, bound once
-    mx = args.format == "mxfp8"
-    w1q = torch.empty((wl.E, 2 * wl.I, wl.H), dtype=torch.uint8, device=dev)
-    w1s = torch.empty((wl.E, 2 * wl.I, wl.H // 32) if mx else (wl.E, 2 * wl.I // 128, wl.H // 128),
-                      dtype=torch.float32, device=dev)
-    w2q = torch.empty((wl.E, wl.H, wl.I), dtype=torch.uint8, device=dev)
-    w2s = torch.empty((wl.E, wl.H, wl.I // 32) if mx else (wl.E, wl.H // 128, wl.I // 128),
-                      dtype=torch.float32, device=dev)
-    chunk = 16
-    with torch.cuda.stream(stream):
-        for e0 in range(0, wl.E, chunk):
-            ne = min(chunk, wl.E - e0)
-            f = torch.empty((ne, 2 * wl.I, wl.H), dtype=torch.float32, device=dev)
-            g.dev_normal_f32(wl.seed, g.STREAM_W1, e0 * 2 * wl.I * wl.H, f.numel(),
-                             g.weight_sigma(wl.H), f.data_ptr(), sp)
-            q, s = layer.quantize_weights(f, stream, fmt=args.format)
-            w1q[e0:e0 + ne].copy_(q)
-            w1s[e0:e0 + ne].copy_(s)
-            f = torch.empty((ne, wl.H, wl.I), dtype=torch.float32, device=dev)
-            g.dev_normal_f32(wl.seed, g.STREAM_W2, e0 * wl.H * wl.I, f.numel(),
-                             g.weight_sigma(wl.I), f.data_ptr(), sp)
-            q, s = layer.quantize_weights(f, stream, fmt=args.format)
-            w2q[e0:e0 + ne].copy_(q)
-            w2s[e0:e0 + ne].copy_(s)
-            del f, q, s
-        layer.bind_weights(w1q, w1s, w2q, w2s, stream)
-    del w1q, w1s, w2q, w2s
+    # weights: generated and quantised on the GPU, bound once; kept for the
+    # per-workload record when workloads there share them (dsv3 prefill/decode)
+    weights = gpu_weights(torch, g, S.MegaMoELayer, wl, args.format, dev, stream)
+    layer.bind_weights(*weights, stream)
+    weights_cache = {}
+    if not (args.experts or args.tokens):
+        weights_cache[(wl.H, wl.I, wl.E, wl.seed)] = weights
+    del weights
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
 
-    # inputs: x on the GPU from the device generator; routes from the host recipe
-    x = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
-    g.dev_normal_bf16(wl.seed, g.STREAM_X, 0, wl.T * wl.H, x.data_ptr(), sp)
-    idx_np, w_np = wl.make_routes()
-    idx = torch.from_numpy(idx_np).to(dev)
-    wts = torch.from_numpy(w_np).to(dev)
-    counts = np.bincount(idx_np.ravel()[idx_np.ravel() >= 0], minlength=wl.E)
+    x, idx, wts, idx_np, w_np, counts = device_inputs(torch, g, wl, dev, stream)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
@@ -442,78 +735,9 @@ def main():
         return
     if args.sm_budget:
         layer.set_sm_budget(args.sm_budget)
-    dbg = layer.tactic()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
 
-    def fwd():
-        layer.forward(x, idx, wts, stream=stream)
-
-    use_graph = not args.no_graph
-    with torch.cuda.stream(stream):
-        fwd()
-    stream.synchronize()
-    st, bits = layer.read_status(stream)
-    if st != 0:
-        raise RuntimeError(f"forward reported device status {bits:#x}")
-
-    def capture():
-        if not use_graph:
-            return None
-        try:
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=stream):
-                fwd()
-            stream.synchronize()
-            return gr
-        except Exception as e:  # fall back to direct launches
-            print(f"# graph capture failed ({e}); timing direct launches", file=sys.stderr)
-            return None
-
-    # Two captures of the same forward: the timed one has no events between
-    # its kernels (each kernel after the first launches as a programmatic
-    # dependent of the previous one); the profiled one records an event
-    # before every kernel, which gives the per-kernel times.
-    graph = capture()
-    layer.set_profile_events(ev)
-    graph_prof = capture()
-    layer.set_profile_events([])
-
-    def step(gr, profiled):
-        if profiled:
-            layer.set_profile_events(ev)
-        with torch.cuda.stream(stream):
-            if gr is not None:
-                gr.replay()
-            else:
-                fwd()
-        if profiled:
-            layer.set_profile_events([])
-
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-
-    step_times = []  # the timed (unprofiled) steps, for the median / p10 / p90
-
-    def timed_steps(n, profiled, keep=False):
-        tot = 0.0
-        per_kernel = {k: 0.0 for k in KERNELS}
-        for _ in range(n):
-            with torch.cuda.stream(stream):
-                flush.zero_()
-                t_start.record(stream)
-            step(graph_prof if profiled else graph, profiled)
-            with torch.cuda.stream(stream):
-                t_end.record(stream)
-            stream.synchronize()
-            tot += t_start.elapsed_time(t_end)
-            if keep:
-                step_times.append(t_start.elapsed_time(t_end))
-            if profiled:
-                for i, k in enumerate(KERNELS):
-                    per_kernel[k] += ev[i].elapsed_time(ev[i + 1])
-        return tot, per_kernel
-
-    warm_ms, _ = timed_steps(args.warmup, False)
+    timer = StepTimer(torch, layer, x, idx, wts, stream, flush, not args.no_graph)
+    warm_ms, _ = timer.steps(args.warmup)
     if args.steps <= 0:
         # about a second of timed work (at least 20 steps, at most 5000)
         est = reduce_max(warm_ms / max(1, args.warmup), dev)
@@ -522,7 +746,8 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
-    total_ms, _ = timed_steps(args.steps, False, keep=True)
+    step_times = []
+    total_ms, _ = timer.steps(args.steps, keep=step_times)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
@@ -531,31 +756,24 @@ def main():
     # beside the flushed figure: the same capture replayed back to back with
     # nothing flushed between steps (whatever of the working set L2 keeps)
     n_warm = min(L2_WARM_STEPS, args.steps)
-    with torch.cuda.stream(stream):
-        flush.zero_()
-        for _ in range(3):
-            step(graph, False)
-        t_start.record(stream)
-        for _ in range(n_warm):
-            step(graph, False)
-        t_end.record(stream)
-    stream.synchronize()
-    l2_warm_ms = reduce_max(t_start.elapsed_time(t_end), dev) / n_warm
+    l2_warm_ms = reduce_max(timer.l2_warm(n_warm), dev)
     # per-kernel times: the same number of steps of the profiled capture
-    timed_steps(min(args.warmup, 3), True)
-    prof_ms, per_kernel = timed_steps(args.steps, True)
-    st, bits = layer.read_status(stream)
-    if st != 0:
-        raise RuntimeError(f"timed forwards reported device status {bits:#x}")
+    timer.steps(min(args.warmup, 3), True)
+    prof_ms, per_kernel = timer.steps(args.steps, True)
+    timer.check_status("timed forwards")
+    graph_used = timer.graph is not None
+    del timer
 
     # ---------------------------------------------------------------- e2e
     # The public call a user makes with host buffers: every step copies its x
     # and routes from pinned host memory and reads its output back, all inside
     # the timed span.  Two figures: (1) serial -- copy in, forward, copy out,
-    # one step after the other on one stream; (2) pipelined, the way a serving
-    # loop runs it -- two device slots, copies on their own streams, so step
-    # i+1's inputs and step i-1's output move while step i computes.  The
-    # value is the pipelined figure; the serial one is reported beside it.
+    # one step after the other on one stream, L2 flushed before each step;
+    # (2) pipelined, the way a serving loop runs it -- two device slots, copies
+    # on their own streams, so step i+1's inputs and step i-1's output move
+    # while step i computes; nothing is flushed between its steps (the value
+    # says whether the step's compulsory bytes exceed L2).  The value is the
+    # pipelined figure; the serial one is reported beside it.
     x_host = torch.from_numpy(problem.x_bits(wl).view(np.int16).copy()).view(torch.bfloat16).pin_memory()
     idx_host = torch.from_numpy(idx_np).pin_memory()
     w_host = torch.from_numpy(w_np).pin_memory()
@@ -567,6 +785,8 @@ def main():
     h2d = x_host.numel() * 2 + idx_host.numel() * 4 + w_host.numel() * 4
     d2h = out_host[0].numel() * 2
     layer.set_profile_events([])
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
 
     def e2e_serial_step():
         with torch.cuda.stream(stream):
@@ -642,41 +862,9 @@ def main():
     ms_step = total_ms / K
     value = aggregate_rate(world, flops, K, total_ms) / 1e12
     e2e_value = aggregate_rate(world, flops, K, e2e_ms) / 1e12
-    hbm, bf16, bf16_sus, src = peaks()
-    # FP8 dense = 2x BF16 dense (nominal 4.5 vs 2.25 PFLOP/s).  The BF16 figure
-    # follows the regime the timed steps ran in: the sustained one (measured
-    # back to back under the power cap) when the clock samples of the timed
-    # region show the power cap engaged, else the burst one.
-    regime = "sustained" if (bf16_sus and "sw_power_cap" in (clk.get("reasons") or [])) else "burst"
-    fp8_peak = 2.0 * (bf16_sus if regime == "sustained" else bf16)
-    b_alg, touched = algorithmic_bytes(wl, counts)
-    t_roof = max(flops / (fp8_peak * 1e12), b_alg / (hbm * 1e9))
-    kern_ms = {k: v / K for k, v in per_kernel.items()}
-    plan = layer.plan(wl.T)
-    route_k = plan["route_kernels"]
-    mega = plan["gemm_launches"] == 1
-    if route_k == 1:  # one cooperative routing kernel: its whole time is in the first span
-        kern_ms["route_fused"] = kern_ms.pop("route_count")
-        kern_ms.pop("route_scan")
-        kern_ms.pop("route_scatter")
-    # dominant kernel: FC1 (fused epilogue), a dense FP8 contraction
-    R = int(counts.sum())
-    fc1_flops = 2 * R * wl.H * 2 * wl.I
-    fc1_ms = kern_ms["fc1"]
-    fc1_bytes = touched * (2 * wl.I * wl.H) + R * wl.H
-    fc1_ai = fc1_flops / fc1_bytes
-    ridge = fp8_peak * 1e12 / (hbm * 1e9)
-    if fc1_ai >= ridge:
-        roof = {"bound": "tensor", "achieved": fc1_flops / (fc1_ms * 1e-3) / 1e12, "peak": fp8_peak,
-                "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": fc1_bytes / (fc1_ms * 1e-3) / 1e9, "peak": hbm,
-                "unit": "GB/s"}
-    roof.update({"frac": roof["achieved"] / roof["peak"],
-                 "traffic": recorded_traffic(wl.name, "fc1"), "kernel": "fc1",
-                 "algorithmic_bytes": fc1_bytes,
-                 "peak_source": f"{src}: FP8 = 2 x bf16 {regime}" if roof["bound"] == "tensor"
-                 else f"{src}: hbm copy"})
+    kern_ms, plan = kernel_times(layer, wl.T, per_kernel, K)
+    lroof, roof, _ = rooflines(wl, counts, kern_ms, ms_step)
+    big = lroof["b_alg_bytes"] > L2_BYTES
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -685,18 +873,13 @@ def main():
                    "fc1_epilogue": "fused" if fused else "unfused",
                    "format": ("MXFP8: E4M3, E8M0 scale per 32 along K" if args.format == "mxfp8"
                               else "E4M3, 1x128 activation / 128x128 weight scales"),
-                   "l2": "flushed before every step (256 MiB write, untimed)",
-                   "launch": "cuda graph replay" if graph is not None else "direct launches",
-                   "gemm": ("cta pairs" if dbg["gemm_pair"] else "single cta") + f" x{dbg['gemm_ctas']}",
-                   "routing": "one cooperative kernel" if route_k == 1 else "three kernels",
-                   "gemms": ("FC1 + FC2 in one persistent launch" if mega else "two launches"),
+                   "l2": l2_note(wl, lroof["b_alg_bytes"]),
+                   "launch": "cuda graph replay" if graph_used else "direct launches",
+                   **tactic_str(layer, plan),
                    "sm_budget": args.sm_budget or None,
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": aggregate_rate(world, wl.T, K, total_ms),
-        "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
-                           "b_alg_bytes": b_alg, "experts_touched": touched,
-                           "fp8_peak_tflops": fp8_peak, "fp8_peak_regime": regime, "hbm_gbs": hbm,
-                           "source": src},
+        "layer_roofline": lroof,
         "roofline": roof,
         "step_ms": {"median": float(np.median(step_times)), "p10": float(np.percentile(step_times, 10)),
                     "p90": float(np.percentile(step_times, 90))},
@@ -713,18 +896,30 @@ def main():
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / K,
                 "copies": "pipelined: two device slots; H2D and D2H on their own streams overlap the "
                           "neighbouring steps' forwards",
+                "l2": ("not flushed between the pipelined steps; each step's compulsory bytes exceed L2"
+                       if big else "not flushed between the pipelined steps (L2-warm)"),
                 "serial": {"value": aggregate_rate(world, flops, K, e2e_serial_ms) / 1e12,
-                           "ms_per_step": e2e_serial_ms / K}},
+                           "ms_per_step": e2e_serial_ms / K,
+                           "l2": "flushed before every step (untimed)"}},
     }
+    del x_d, idx_d, w_d, out_d, layer
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x_bits = x_host.view(torch.int16).numpy().view(np.uint16)
-        n = cpu_sample_tokens(wl, args.cpu_sample_tokens)
-        toks = np.sort(np.random.default_rng(0).choice(wl.T, size=n, replace=False))
-        dt, fl = oracle_sample(wl, x_bits, idx_np, w_np, toks)
-        line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
-                                "kind": "oracle", "seconds": dt,
-                                "sample": f"{n} random tokens of {wl.name} (their experts' FFN + "
-                                          "combine; routing of the whole batch)"}
+        line["cpu_baseline"] = oracle_bounded_run(wl, x_bits, idx_np, w_np, CPU_BASELINE_S,
+                                                  np.random.default_rng(0))
+    if world == 1 and not args.no_records:
+        torch.cuda.empty_cache()
+        names = [n for n in args.records.split(",") if n and configs.WORKLOADS[n].name != wl.name]
+        clocks = ClockSampler(local)
+        recs = {}
+        for n in names:
+            recs[n] = measure_record(torch, S, g, n, args, dev, stream, flush, weights_cache)
+        line["per_workload"] = {
+            "how": ("each workload as the main line times it (CUDA graph replay, L2 flushed before "
+                    f"every step, {args.warmup} warm-up and {K} timed steps, per-kernel times "
+                    "from the profiled capture), in this run, after the main line"),
+            "clocks": clocks.stop(), "records": recs}
+    weights_cache.clear()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -29,6 +29,7 @@ BASE_KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_ste
 def test_reference_arm_line():
     d = run_bench("--impl", "reference", "--config", "tiny", "--steps", "1", "--warmup", "0")
     assert BASE_KEYS <= set(d), set(d)
+    assert d["config"]["experts_per_step"] >= 1 and "experts" in d["cpu_baseline"]["sample"]
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
@@ -39,7 +40,7 @@ def test_reference_arm_line():
 @pytest.mark.parametrize("fmt", ["deepseek", "mxfp8"])
 def test_main_line(fmt):
     d = run_bench("--config", "tiny", "--steps", "5", "--warmup", "3", "--no-cpu-baseline",
-                  "--format", fmt)
+                  "--format", fmt, "--records", "v2lite")
     assert (BASE_KEYS - {"cpu_baseline"}) <= set(d), set(d)
     assert d["value"] > 0 and d["steps"] == 5 and d["warmup"] == 3 and d["n_gpus"] == 1
     r = d["roofline"]
@@ -52,6 +53,12 @@ def test_main_line(fmt):
     assert {"median", "p10", "p90"} <= set(d["step_ms"])
     assert d["l2_warm"]["ms_per_step"] > 0 and d["l2_warm"]["steps"] >= 1
     assert d["config"]["format"].startswith("MXFP8" if fmt == "mxfp8" else "E4M3")
+    lr = d["layer_roofline"]
+    assert lr["fp8_peak"] == "2 x measured bf16 burst" and 0 < lr["fp8_peak_frac"] < 2
+    # the per-workload record: the same timing method on another workload
+    rec = d["per_workload"]["records"]["v2lite"]
+    assert rec["workload"].startswith("dsv2lite") and rec["steps"] == 5 and rec["ms_per_step"] > 0
+    assert {"fc1", "fc2", "combine"} <= set(rec["kernel_ms"]) and 0 < rec["layer_roofline"]["frac"] < 2
 
 
 @pytest.mark.gpu
@@ -84,3 +91,21 @@ def test_layer_roofline_bytes(name, touched, gb):
     per_expert = 3 * wl.I * wl.H + (2 * wl.I // 128 + wl.I // 128) * (wl.H // 128) * 4
     assert b == touched * per_expert + wl.T * wl.H * 4 + wl.T * wl.K * 8
     assert abs(b / 1e9 - gb) < 0.01 * gb
+
+
+def test_oracle_sample_is_every_row_of_its_experts():
+    """A bounded oracle sample is every routed row of the experts it draws:
+    the mini-problem keeps exactly those routes (others masked) and its FLOPs
+    count 6*H*I per kept row."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    from gen import configs, problem
+    wl = configs.TINY
+    idx, w = wl.make_routes()
+    smp = bench.OracleSampler(wl, problem.x_bits(wl), idx, w)
+    dt, fl, rows, n = smp.sample(3, np.random.default_rng(5))
+    assert n == 3 and dt > 0
+    counts = np.bincount(idx.ravel(), minlength=wl.E)
+    assert rows in {int(counts[list(s)].sum()) for s in __import__("itertools").combinations(range(wl.E), 3)}
+    assert fl == 6 * rows * wl.H * wl.I
