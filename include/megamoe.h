@@ -145,7 +145,10 @@ MOE_API moe_status moe_workspace_query(const moe_dims* dims, int64_t expected_m,
                                size_t* weight_bytes);
 
 /*
- * moe_create -- binds dims and caller-owned device regions; creates no CUDA
+ * moe_create -- the stateful layer object of flashinfer PR #4069 ("Contracts
+ * introduced by this PR": a backend instance is set up once per layer with its
+ * capacity and bound buffers, and forwards then only pass activations and
+ * routes).  Binds dims and caller-owned device regions; creates no CUDA
  * stream and allocates no device memory.  Sets kernel attributes, so call it
  * before any stream capture.  *out receives a host handle.
  * Workspace pooling: a forward leaves nothing in the workspace that a later
@@ -242,14 +245,23 @@ MOE_API moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t
                        const float* d_topk_w, int64_t num_tokens, struct CUstream_st* stream);
 
 /*
- * moe_read_status -- copies the device status word of the latest forward on
+ * moe_read_status -- the read-back of the device-side route checker of
+ * flashinfer PR #6398 ("perf(moe_ep): fuse Rubin MegaMoE forward
+ * preparation", Description and the follow-up on the fused routing checker:
+ * routes are validated on the device inside the forward, which stays
+ * asynchronous, and the caller reads the result when it chooses).  Copies
+ * the device status word of the latest forward on
  * `stream` to *h_status (MOE_DEV_* bits) and synchronises that stream: the
  * caller chooses this sync point.  Returns MOE_OK when the word is 0, else
  * the matching error (route, capacity, timeout).
  */
 MOE_API moe_status moe_read_status(moe_handle* h, uint32_t* h_status, struct CUstream_st* stream);
 
-/* Device pointers to internal buffers and their layouts, for tests and tools.
+/* moe_debug_views -- device pointers to internal buffers and their layouts,
+ * for tests and tools: the debug output of flashinfer PR #4688 (the pull
+ * kernel's generate_c mode keeps the raw pre-SwiGLU gate+up as BF16 so the
+ * FC1 result can be checked on its own), here together with the routing
+ * tables and the quantised operands.
  * The rows of a, gu, hq and y (and their scale bytes) that lie inside an
  * expert's padded segment but past its routed rows hold unspecified values:
  * the kernels compute over them but never store them or read them into a
@@ -348,17 +360,25 @@ MOE_API moe_status moe_forward_plan(moe_handle* h, int64_t num_tokens, moe_plan*
  * (-1 for masked slots).  Inputs as for moe_forward.  check_routes != 0 adds
  * the duplicate and finite-weight checks.
  *
- * Scratch: a fixed file-scope device array of about 0.9 MiB, present on every
- * GPU that loads the library until the process exits.  Limits:
+ * Scratch: a fixed file-scope device array of about 0.9 MiB, present in every
+ * CUDA context that loads the library until that context is destroyed (for
+ * the runtime's primary context: until the process exits).  Limits:
  * num_tokens * top_k <= 131072, ceil(num_tokens / 128) * num_experts <= 32768,
  * num_experts <= 1024; larger inputs return MOE_ERR_CAPACITY before anything
- * is enqueued.  The first call made with a given device current looks up the
- * array's device address (cudaGetSymbolAddress) and caches it: make that
- * first call before any stream capture.  Every call uses the same array, so
- * calls that overlap on the GPU (other streams, other threads) race and
- * corrupt each other's results: order them on one stream.  The array keeps
- * the last call's contents; nothing in it needs to start at zero.
- * num_tokens == 0 returns MOE_OK and writes nothing.  Asynchronous on stream.
+ * is enqueued.  The array's device address belongs to one context: the first
+ * call made in a context (the one current on the calling thread, primary or a
+ * context the caller made current) looks it up (cudaGetSymbolAddress) and
+ * caches it under the context's unique id, so make that first call before
+ * any stream capture.  Every call in a context uses the same array, so calls
+ * that overlap on the GPU (other streams, other threads) race and corrupt
+ * each other's results: order them on one stream.  The array keeps the last
+ * call's contents; nothing in it needs to start at zero.
+ * Errors: MOE_ERR_UNSUPPORTED for top_k or num_experts outside the set above;
+ * MOE_ERR_INVALID_ARG for num_tokens < 0 or a NULL pointer (d_topk_idx,
+ * d_topk_w, d_perm and d_inv may be NULL when num_tokens == 0);
+ * MOE_ERR_CAPACITY as above; MOE_ERR_CUDA when a CUDA call fails.
+ * num_tokens == 0 clears *d_status, zeroes d_counts and d_offsets and writes
+ * nothing else.  Asynchronous on stream.
  */
 MOE_API moe_status moe_route_noalloc(const int32_t* d_topk_idx, const float* d_topk_w,
                                      int64_t num_tokens, int32_t top_k, int32_t num_experts,
@@ -366,7 +386,11 @@ MOE_API moe_status moe_route_noalloc(const int32_t* d_topk_idx, const float* d_t
                                      int32_t* d_perm, int32_t* d_inv, uint32_t* d_status,
                                      struct CUstream_st* stream);
 
+/* moe_destroy -- frees the host handle (lifecycle only; the pages have no
+ * passage on it).  Device memory stays the caller's.  NULL is a no-op. */
 MOE_API void moe_destroy(moe_handle* h);
+/* moe_status_str -- a static text for a status code (error reporting only;
+ * the pages have no passage on it). */
 MOE_API const char* moe_status_str(moe_status s);
 
 #ifdef __cplusplus

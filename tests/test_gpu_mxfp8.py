@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from tests import gpu_harness as gh
-from tests.test_gpu_parity import OUT_TOL, check_routing, compare_outputs, small_problem
+from tests.test_gpu_parity import check_routing, compare_outputs, gate_out, small_problem
 
 pytestmark = pytest.mark.gpu
 
@@ -102,7 +102,7 @@ def test_mx_fused_bit_equal_unfused_and_one_launch_equal_split(lib, orc):
         for a, b in zip(res[0], other):
             assert torch.equal(a, b)
     ref = orc.forward(x, idx, w, *wo, fmt=1)
-    assert gh.rel_l2(gh.bf16_np(res[0][0].view(torch.bfloat16)), gh.bits_to_f64(ref["out"])) <= OUT_TOL
+    gate_out(gh.bf16_np(res[0][0].view(torch.bfloat16)), gh.bits_to_f64(ref["out"]))
 
 
 def test_mx_bind_rejects_non_power_of_two_scale(lib, orc):

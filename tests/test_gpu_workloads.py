@@ -4,11 +4,14 @@
   oracle (every output element).
 * dsv3 prefill / decode sweep / skew: routing tables, every quantised byte and
   scale of the gathered activations -- in full; the expert FFN and combine on
-  sampled tokens: the oracle runs on a mini-problem made of those tokens and
-  the experts they route to (relabelled 0..n-1; a token's output depends only
-  on its own row, routes and those experts' weights).  The launch
-  configuration is the one bench.py times (fused FC1 epilogue); a second run
-  of the unfused reference path must give the same output bit for bit.
+  sampled tokens chosen to reach every expert and every position of the GEMM
+  tiles: the oracle runs on a problem made of those tokens with the routes
+  they have (a token's output depends only on its own row, its routes and
+  those experts' weights).  The prefill and decode samples share the dsv3
+  weights, so one oracle call covers all of them.  The launch configuration
+  is the one bench.py times (fused FC1 epilogue); a second run of the
+  unfused reference path must give the same output bit for bit, and its
+  gate||up is compared with the oracle's on every sampled route.
 """
 import numpy as np
 import pytest
@@ -17,7 +20,7 @@ import torch
 from gen import configs, problem
 from tests import gpu_harness as gh
 from tests.test_gpu_parity import (GU_TOL, check_quant, check_routing, compare_outputs,
-                                   make_layer)
+                                   gate_out, make_layer)
 
 pytestmark = pytest.mark.gpu
 
@@ -30,18 +33,27 @@ def lib():
     return S
 
 
-_orc_w_cache = {}
+_orc_full = {}
 
 
-def oracle_expert_weights(orc, wl, experts):
-    key = (wl.H, wl.I, wl.seed)
-    cache = _orc_w_cache.setdefault(key, {})
-    missing = [e for e in experts if e not in cache]
-    if missing:
-        w = gh.oracle_weights(orc, wl, missing)
-        for i, e in enumerate(missing):
-            cache[e] = tuple(a[i] for a in w)
-    return tuple(np.stack([cache[e][j] for e in experts]) for j in range(4))
+def oracle_all_experts(orc, wl, chunk=8):
+    """The oracle's weights for every expert of a workload (host generator and
+    the oracle's quantiser), built in expert chunks into preallocated arrays and
+    kept for the module (the dsv3 prefill and decode workloads share them)."""
+    key = (wl.H, wl.I, wl.E, wl.seed)
+    if key not in _orc_full:
+        _orc_full.clear()
+        E, H, I = wl.E, wl.H, wl.I
+        w1q = np.empty((E, 2 * I, H), np.uint8)
+        w1s = np.empty((E, 2 * I // 128, H // 128), np.float32)
+        w2q = np.empty((E, H, I), np.uint8)
+        w2s = np.empty((E, H // 128, I // 128), np.float32)
+        for e0 in range(0, E, chunk):
+            ex = list(range(e0, min(E, e0 + chunk)))
+            w1q[ex], w1s[ex] = orc.quant_weights(problem.w1_f32(wl, ex))
+            w2q[ex], w2s[ex] = orc.quant_weights(problem.w2_f32(wl, ex))
+        _orc_full[key] = (w1q, w1s, w2q, w2s)
+    return _orc_full[key]
 
 
 def test_v2lite_full_layer(lib, orc):
@@ -99,13 +111,92 @@ def v3_weights(lib):
     torch.cuda.empty_cache()
 
 
-def sampled_check(lib, orc, wl, wd, tokens):
+# --------------------------------------------------------------------------
+# sampled tokens
+# --------------------------------------------------------------------------
+# dsv3 prefill: block-permutation routing gives every block of E/K = 32 tokens
+# exactly one route to every expert, so expert e's routed row j (in token
+# order) comes from block j.  CTA pairs pad segments to 256 rows: rows 0-127
+# belong to the pair's first CTA, 128-255 to its second, 32 rows per TMEM lane
+# quadrant.  These blocks put rows 0, 40, 72, 127 (first CTA: quadrants 0-3)
+# and 128, 168, 200, 255 (second CTA) of EVERY expert into the sample.
+PREFILL_BLOCKS = (0, 40, 72, 127, 128, 168, 200, 255)
+
+
+def sample_tokens(name: str, wl, idx) -> np.ndarray:
+    if name == "v3prefill":
+        B = wl.E // wl.K
+        return np.concatenate([np.arange(b * B, (b + 1) * B) for b in PREFILL_BLOCKS])
+    if name.startswith("v3decode"):
+        if wl.T <= 256:
+            return np.arange(wl.T)                      # every token
+        rng = np.random.default_rng(wl.T)
+        rest = rng.choice(np.arange(1, wl.T - 1), size=254, replace=False)
+        return np.unique(np.concatenate([[0, wl.T - 1], rest]))
+    if name == "skew":
+        # the hottest expert's first 256-row tile and its last two (the partial
+        # tail and the full one before it; every token routed into them), the
+        # token of every non-empty expert's last routed row (each expert's
+        # tail tile), and 128 random tokens
+        flat = idx.ravel()
+        counts = np.bincount(flat[flat >= 0], minlength=wl.E)
+        hot = int(np.argmax(counts))
+        toks_hot = np.nonzero((idx == hot).any(axis=1))[0]   # token order = row order
+        last0 = max(0, (len(toks_hot) - 1) // 256 * 256 - 256)
+        tail = [int(np.nonzero((idx == e).any(axis=1))[0][-1]) for e in np.nonzero(counts)[0]]
+        rng = np.random.default_rng(3)
+        return np.unique(np.concatenate([toks_hot[:256], toks_hot[last0:], tail,
+                                         rng.choice(wl.T, 128, replace=False)]))
+    raise ValueError(name)
+
+
+def oracle_on_tokens(orc, parts, W):
+    """One oracle call over the union of several workloads' sampled tokens that
+    share the weights W: rows stacked, each with its own routes.  Returns, per
+    part, the oracle's output rows and a map (token i of the part, k) ->
+    oracle row of gate||up."""
+    X = np.concatenate([p["x"] for p in parts])
+    IDX = np.concatenate([p["idx"] for p in parts]).astype(np.int32)
+    WT = np.concatenate([p["w"] for p in parts]).astype(np.float32)
+    ref = orc.forward(X, IDX, WT, *W)
+    assert ref["err"] == 0
+    K = IDX.shape[1]
+    res, t0 = {}, 0
+    for p in parts:
+        n = len(p["x"])
+        res[p["name"]] = dict(out=ref["out"][t0:t0 + n],
+                              inv=ref["inv"][t0 * K:(t0 + n) * K].reshape(n, K), gu=ref["gu"])
+        t0 += n
+    return res
+
+
+@pytest.fixture(scope="module")
+def dsv3_reference(orc):
+    """The oracle on the sampled tokens of the prefill and of every decode size,
+    in one call (the expert weights are decoded once for all of them)."""
+    parts = []
+    for name in ["v3prefill"] + [f"v3decode{t}" for t in configs.DECODE_TOKENS]:
+        wl = configs.WORKLOADS[name]
+        x, idx, w = gh.host_inputs(wl)
+        toks = sample_tokens(name, wl, idx)
+        parts.append(dict(name=name, tokens=toks, x=x[toks], idx=idx[toks], w=w[toks]))
+    res = oracle_on_tokens(orc, parts, oracle_all_experts(orc, configs.V3_PREFILL))
+    for p in parts:
+        res[p["name"]]["tokens"] = p["tokens"]
+    return res
+
+
+def gpu_run_and_compare(lib, orc, wl, wd, tokens, ref_part, check_cta_halves=False):
+    """Full-size forwards of the workload on the GPU (the bench configuration,
+    then the unfused path with gate||up kept): routing tables and every
+    quantised activation byte in full against the oracle; fused = unfused bit
+    for bit; the sampled tokens' outputs and every sampled route's gate||up
+    against the oracle."""
     x, idx, w = gh.host_inputs(wl)
     ref_route = orc.route(idx, w, wl.E)
     assert ref_route["err"] == 0
     xq, xs = orc.quant_rows_bf16(x)
     xt, it, wt = gh.to_device(x, idx, w)
-    # bench configuration: fused epilogue, no debug copy of gate||up
     layer = make_layer(lib, wl, wd, fuse=True, emit=False)
     out_f = layer.forward(xt, it, wt).clone()
     assert layer.read_status() == (0, 0)
@@ -114,67 +205,83 @@ def sampled_check(lib, orc, wl, wd, tokens):
     check_quant(lib, dbg, xq, xs, ref_route["perm"], rows, wl.K)
     rows_t = torch.from_numpy(rows).cuda()
     hq_f = dbg["hq"][rows_t].clone()
+    pair = dbg["gemm_pair"]
     del layer, dbg
-    # unfused reference path keeps gate||up
     layer = make_layer(lib, wl, wd, fuse=False, emit=True)
     out_u = layer.forward(xt, it, wt).clone()
     assert layer.read_status() == (0, 0)
     dbg = layer.debug()
     assert torch.equal(out_f.view(torch.int16), out_u.view(torch.int16))
     assert torch.equal(hq_f, dbg["hq"][rows_t])
-    # mini-problem of the sampled tokens
-    tokens = np.asarray(sorted(set(int(t) for t in tokens)))
-    sub_idx = idx[tokens]
-    experts = sorted(set(int(e) for e in sub_idx.ravel() if e >= 0))
-    remap = {e: i for i, e in enumerate(experts)}
-    mini_idx = np.vectorize(lambda e: remap.get(int(e), -1))(sub_idx).astype(np.int32)
-    W = oracle_expert_weights(orc, wl, experts)
-    ref = orc.forward(x[tokens], mini_idx, w[tokens], *W)
-    assert ref["err"] == 0
+    # outputs of the sampled tokens
+    tokens = np.asarray(tokens)
     o = gh.bf16_np(out_f[torch.from_numpy(tokens).cuda()])
-    r = gh.bits_to_f64(ref["out"])
-    rel = gh.rel_l2(o, r)
-    maxabs = float(np.max(np.abs(o - r)))
-    rms = float(np.sqrt(np.mean(r * r)))
-    # gate||up of the sampled routes: GPU padded row of route (t, k) vs the
-    # oracle's mini-problem row of the same route
-    inv_pad = dbg["inv_pad"][:wl.T * wl.K].cpu().numpy()
-    gpu_rows, orc_rows = [], []
-    for i, t in enumerate(tokens):
-        for k in range(wl.K):
-            if idx[t, k] >= 0:
-                gpu_rows.append(inv_pad[t * wl.K + k])
-                orc_rows.append(ref["inv"][i * wl.K + k])
-    gu = gh.bf16_np(dbg["gu"][torch.tensor(gpu_rows).cuda()])
-    gu_rel = gh.rel_l2(gu, gh.bits_to_f64(ref["gu"][orc_rows]))
-    print(wl.name, dict(tokens=len(tokens), experts=len(experts), out_rel_l2=rel,
-                        out_maxabs=maxabs, rms=rms, gu_rel_l2=gu_rel))
-    assert gu_rel <= GU_TOL
-    assert rel <= 1e-2 and maxabs <= 5e-2 * rms
+    stats = gate_out(o, gh.bits_to_f64(ref_part["out"]))
+    # gate||up of every sampled route: GPU padded row vs the oracle's row
+    inv_pad = dbg["inv_pad"][:wl.T * wl.K].cpu().numpy().reshape(wl.T, wl.K)
+    sub = idx[tokens]
+    act = sub >= 0
+    gpu_rows = inv_pad[tokens][act]
+    orc_rows = ref_part["inv"][act]
+    gu = gh.bf16_np(dbg["gu"][torch.from_numpy(gpu_rows).cuda()])
+    stats["gu_rel_l2"] = gh.rel_l2(gu, gh.bits_to_f64(ref_part["gu"][orc_rows]))
+    assert stats["gu_rel_l2"] <= GU_TOL, stats
+    # where the sampled routes sit in their experts' GEMM tiles
+    pad = dbg["pad_offsets"].cpu().numpy()
+    in_seg = gpu_rows - pad[sub[act]]
+    stats.update(tokens=len(tokens), routes=int(act.sum()),
+                 experts=len(np.unique(sub[act])), gemm_pair=bool(pair))
+    if check_cta_halves:
+        # every sampled expert has sampled rows in both CTAs of its pair tile
+        # and in all four lane quadrants of each
+        assert pair
+        for e in np.unique(sub[act]):
+            r = in_seg[sub[act] == e]
+            assert {int(v) // 32 for v in r} == set(range(8)), (e, sorted(r))
+    print(wl.name, stats)
     del layer, dbg
+    return stats
 
 
-def pick_tokens(T, n, seed=0):
-    rng = np.random.default_rng(seed)
-    base = [0, T - 1, T // 2]
-    return np.unique(np.concatenate([base, rng.integers(0, T, max(0, n - 3))]))[:n]
-
-
-def test_v3_prefill_sampled(lib, orc, v3_weights):
-    sampled_check(lib, orc, configs.V3_PREFILL, v3_weights, pick_tokens(8192, 4))
+def test_v3_prefill_sampled(lib, orc, v3_weights, dsv3_reference):
+    """Eight whole routing blocks: every one of the 256 experts, rows in both
+    CTAs of its pair tile and in all four TMEM lane quadrants of each."""
+    r = dsv3_reference["v3prefill"]
+    st = gpu_run_and_compare(lib, orc, configs.V3_PREFILL, v3_weights, r["tokens"], r,
+                             check_cta_halves=True)
+    assert st["experts"] == 256 and st["tokens"] == 256
 
 
 @pytest.mark.parametrize("T", configs.DECODE_TOKENS)
-def test_v3_decode_sampled(lib, orc, v3_weights, T):
-    sampled_check(lib, orc, configs.V3_DECODE.with_tokens(T), v3_weights, pick_tokens(T, min(T, 3), T))
+def test_v3_decode_sampled(lib, orc, v3_weights, dsv3_reference, T):
+    """T = 8, 64, 256: every token; T = 1024: 256 tokens (the first and last
+    among them)."""
+    r = dsv3_reference[f"v3decode{T}"]
+    st = gpu_run_and_compare(lib, orc, configs.V3_DECODE.with_tokens(T), v3_weights, r["tokens"], r)
+    assert st["tokens"] == min(T, 256)
 
 
 def test_skew_sampled(lib, orc):
+    """Every token routed into the hottest expert's first and last two 256-row
+    tiles, the last routed row of every non-empty expert, and 128 random
+    tokens."""
     wl = configs.SKEW
     wd = gh.device_weights(wl, lib.MegaMoELayer)
     x, idx, w = gh.host_inputs(wl)
     counts = np.bincount(idx.ravel(), minlength=wl.E)
     assert (counts == 0).sum() == 38 and counts.max() > 8000   # ragged M, empty groups
-    sampled_check(lib, orc, wl, wd, pick_tokens(wl.T, 4, 1))
+    toks = sample_tokens("skew", wl, idx)
+    assert len(toks) >= 512
+    # the oracle on the non-empty experts only (relabelled; empty experts have no route)
+    experts = np.nonzero(counts)[0]
+    remap = np.full(wl.E, -1, np.int32)
+    remap[experts] = np.arange(len(experts), dtype=np.int32)
+    sub = idx[toks]
+    mini = np.where(sub >= 0, remap[np.clip(sub, 0, wl.E - 1)], -1).astype(np.int32)
+    W = gh.oracle_weights(orc, wl, [int(e) for e in experts])
+    part = dict(name="skew", x=x[toks], idx=mini, w=w[toks])
+    ref = oracle_on_tokens(orc, [part], W)["skew"]
+    st = gpu_run_and_compare(lib, orc, wl, wd, toks, ref)
+    assert st["experts"] == len(experts) == 90
     del wd
     torch.cuda.empty_cache()
