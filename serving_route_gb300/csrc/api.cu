@@ -303,6 +303,7 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   w.status = reinterpret_cast<uint32_t*>(b + L.o_status);
   w.total_mtiles = reinterpret_cast<int32_t*>(b + L.o_status + 4);
   w.grid_sync = reinterpret_cast<uint32_t*>(b + L.o_status + 8);
+  w.gemm_sched = reinterpret_cast<int32_t*>(b + L.o_status + 12);
   w.fc1_done = reinterpret_cast<int32_t*>(b + L.o_fc1_done);
   w.counts = reinterpret_cast<int32_t*>(b + L.o_counts);
   w.offsets = reinterpret_cast<int32_t*>(b + L.o_offsets);
@@ -425,9 +426,10 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   // (events between kernels need two launches to time FC1 and FC2).
   const moe_plan plan = forward_plan(h, num_tokens);
   const bool mega = ev == nullptr && plan.gemm_launches == 1;
-  // status word, total_mtiles, the routing kernel's arrival counter and (for
-  // the megakernel) the per-m-tile FC1 counters
-  cudaMemsetAsync(ws.status, 0, mega ? 1024 + 4 * (size_t)(L.rows_alloc / 128) : 12, s);
+  // status word, total_mtiles, the routing kernel's arrival counter, the
+  // GEMM launches' unit counters and (for the megakernel) the per-m-tile FC1
+  // counters
+  cudaMemsetAsync(ws.status, 0, mega ? 1024 + 4 * (size_t)(L.rows_alloc / 128) : 20, s);
   // Under an SM budget the routing keeps to its three small kernels: a
   // cooperative grid would have to be resident beside the side-stream work.
   const int coop = plan.route_kernels == 1 ? h->route_coop_blocks : 0;
@@ -472,6 +474,16 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   const bool wd_test = (h->dims.flags & MOE_FLAG_WATCHDOG_TEST) != 0;
   g1.wait_limit_ns = wd_test ? 20000000ull : 1000000000ull;
   g1.watchdog_test = wd_test ? 1 : 0;
+  // Single CTAs take units from a counter when the forward routes fewer rows
+  // than one full 128-row m-tile per expert: its tiles then mostly stream
+  // weights and their durations vary with memory contention (and FC1 units
+  // cost several FC2 units), which the counter evens out (decode T = 8:
+  // 0.3745 -> 0.3634 ms).  With full m-tiles the tiles are compute-shaped and
+  // of equal cost, the static round robin is already balanced and the
+  // counter only adds jitter (dsv2lite: 0.2591 -> 0.2650 ms).  CTA pairs
+  // keep the static order.
+  const bool dyn_sched = !L.pair && num_tokens * L.K < 128 * (int64_t)L.E;
+  g1.sched = dyn_sched ? ws.gemm_sched : nullptr;
   const GemmMode m1 = fused ? (emit ? kModeFusedGU : kModeFused) : kModeGU;
   if (ev) record_event(ev[5], s);
   const bool pair = L.pair;
@@ -501,6 +513,7 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.ld_out = L.H;
   g2.status = ws.status;
   g2.wait_limit_ns = g1.wait_limit_ns;
+  g2.sched = dyn_sched ? ws.gemm_sched + 1 : nullptr;
   if (ev) record_event(ev[7], s);
   if (mega) {
     // the FC1 epilogue publishes, per m-tile, how many of its NT tiles are stored

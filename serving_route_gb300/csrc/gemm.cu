@@ -107,10 +107,15 @@ __device__ __noinline__ bool wait_count_geq(const int32_t* count, int target, vo
 // One launch runs the tiles of one GEMM (phase 0), or with MODE == kModeMega
 // the FC1 tiles (phase 0: tmA/tmB/tmSfa/tmSfb, g) and then the FC2 tiles
 // (phase 1: tmA2/tmB2/tmSfa2/tmSfb2, g2, tmY).  Units are numbered phase 0
-// first; each CTA (pair) takes every ustride-th unit in order, so a CTA has
-// issued all of its FC1 tiles before any FC2 tile, and FC2 tiles -- which
-// wait for their m-tile's fc1_done count -- never hold up an FC1 tile:
-// with every CTA resident the waits always end.
+// first.  A CTA pair takes every ustride-th unit in order.  A single CTA
+// (g.sched set) takes unit blockIdx.x first and then the next unhanded one
+// from a device counter (an atomic add), so CTAs that drew lighter units
+// take more of them and the launch ends evenly; its producer passes each
+// unit id to the MMA and epilogue roles through a small shared-memory ring.
+// Either way units are handed out in increasing order, so every FC1 unit is
+// taken by a running CTA before any FC2 unit, and FC2 tiles -- which wait
+// for their m-tile's fc1_done count -- never hold up an FC1 tile: with every
+// CTA resident the waits always end.
 template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -131,6 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t accf_bar, acce_bar, drain_bar;
   __shared__ __align__(8) uint64_t amax_bar[4];  // per quadrant: both column halves posted
   __shared__ __align__(8) uint64_t fc1_bar[2];   // kModeMega: the epilogue warps' FC1 stores, by tile parity
+  // the dynamic schedule's unit ring (single CTA): producer -> MMA + epilogue
+  constexpr int kUnitSlots = 4;
+  __shared__ int unit_ring[kUnitSlots];
+  __shared__ __align__(8) uint64_t unit_full[kUnitSlots], unit_empty[kUnitSlots];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ float amax_sh[2][2][128];  // [tile parity][column half][row] (fused epilogue)
@@ -143,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool leader = rank == 0;
   const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int ustride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const bool dyn = !PAIR && g.sched != nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -154,6 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&drain_bar), 1);
     for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&amax_bar[i]), 2);
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&fc1_bar[i]), kEpiWarps);
+    for (int i = 0; i < kUnitSlots; ++i) {
+      mbar_init(smem_u32(&unit_full[i]), 1);
+      mbar_init(smem_u32(&unit_empty[i]), 1 + kEpiWarps);  // the MMA thread + every epilogue warp
+    }
     abort_sh = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmA);
@@ -221,17 +235,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                  ? ld_relaxed_gpu_s32(g2.fc1_done + own_mtile(m_of(u, 1)))
                  : 0;
     };
-    int e_next = expert_of(unit0);
-    int count_next = count_of(unit0);
-    for (int u = unit0; u < total && !*abort; u += ustride) {
+    // Dynamic schedule: the unit after the next is drawn (lane 0's atomic
+    // add) at the start of each unit and read at its end, so the add's
+    // latency overlaps the unit's loads; the unit ids go to the MMA and
+    // epilogue roles through the ring (the last one, `total`, ends them).
+    int slot = 0;
+    uint32_t slot_ph = 0;
+    auto publish = [&](int v) -> bool {
+      if (!mbar_wait(smem_u32(&unit_empty[slot]), slot_ph ^ 1u, abort, g.status, g.wait_limit_ns))
+        return false;
+      if (lane == 0) {
+        unit_ring[slot] = v;
+        mbar_arrive(smem_u32(&unit_full[slot]));
+      }
+      __syncwarp();
+      if (++slot == kUnitSlots) {
+        slot = 0;
+        slot_ph ^= 1u;
+      }
+      return true;
+    };
+    auto draw = [&]() -> int {  // lane 0 only
+      return (int)gridDim.x + atomicAdd(g.sched, 1);
+    };
+    int u = unit0;
+    int u_next = unit0 + ustride;
+    if (dyn) {
+      int v = 0;
+      if (lane == 0 && u < total) v = draw();
+      u_next = u < total ? __shfl_sync(0xFFFFFFFFu, v, 0) : total;
+    }
+    int e_next = expert_of(u);
+    int count_next = count_of(u);
+    for (; u < total && !*abort;) {
+      if (dyn && !publish(u)) break;
+      int pending = total;
+      if (dyn && lane == 0 && u_next < total) pending = draw();
       const int ph = phase_of(u);
       const int m = m_of(u, ph);
       const int nt = nt_of(u, ph, m);
       const int mt = own_mtile(m);
       const int e = e_next;
-      e_next = expert_of(u + ustride);
+      e_next = expert_of(u_next);
       const int count_seen = count_next;
-      count_next = count_of(u + ustride);
+      count_next = count_of(u_next);
       const int KB = ph ? g2.KB : g.KB, NB = ph ? g2.NB : g.NB, KQ = ph ? g2.KQ : g.KQ;
       const CUtensorMap* mA = ph ? &tmA2 : &tmA;
       const CUtensorMap* mB = ph ? &tmB2 : &tmB;
@@ -319,7 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
+      const int drawn = __shfl_sync(0xFFFFFFFFu, pending, 0);
+      u = u_next;
+      u_next = dyn ? drawn : u + ustride;
     }
+    if (dyn && !*abort) publish(total);  // ends the MMA and epilogue roles
     // Drain: every copy this CTA issued must have landed before the CTA exits
     // (the leader's full barriers also count the peer's bytes; the peer is
     // held by the cluster barrier at the end until the leader has drained).
@@ -359,7 +410,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool ready = probe(0, 0);
       uint32_t sf = tmem + kColSf;
-      for (int u = unit0; u < total; u += ustride) {
+      // the dynamic schedule's next unit, from the producer's ring
+      int slot = 0;
+      uint32_t slot_ph = 0;
+      auto take = [&]() -> int {
+        if (!mbar_wait(smem_u32(&unit_full[slot]), slot_ph, abort, g.status, g.wait_limit_ns))
+          return total;
+        const int v = unit_ring[slot];
+        mbar_arrive(smem_u32(&unit_empty[slot]));
+        if (++slot == kUnitSlots) {
+          slot = 0;
+          slot_ph ^= 1u;
+        }
+        return v;
+      };
+      for (int u = dyn ? take() : unit0; u < total; u = dyn ? take() : u + ustride) {
         if (!mbar_wait<PAIR>(smem_u32(&acce_bar), acc_phase ^ 1u, abort, g.status, g.wait_limit_ns)) break;
         tc_fence_after();
         bool ok = true;
@@ -448,7 +513,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acce_addr = PAIR ? mapa_shared(smem_u32(&acce_bar), 0) : smem_u32(&acce_bar);
     uint32_t acc_phase = 0;
     uint32_t fc1_tiles = 0;  // kModeMega: FC1 tiles this CTA has published
-    for (int u = unit0; u < total; u += ustride) {
+    // the dynamic schedule's next unit: lane 0 takes it from the ring for the warp
+    int slot = 0;
+    uint32_t slot_ph = 0;
+    auto take = [&]() -> int {
+      int v = total;
+      if (lane == 0 &&
+          mbar_wait(smem_u32(&unit_full[slot]), slot_ph, abort, g.status, g.wait_limit_ns)) {
+        v = unit_ring[slot];
+        mbar_arrive(smem_u32(&unit_empty[slot]));
+      }
+      if (++slot == kUnitSlots) {
+        slot = 0;
+        slot_ph ^= 1u;
+      }
+      return __shfl_sync(0xFFFFFFFFu, v, 0);
+    };
+    for (int u = dyn ? take() : unit0; u < total; u = dyn ? take() : u + ustride) {
       const int ph = phase_of(u);
       const int m = m_of(u, ph);
       const int nt = nt_of(u, ph, m);

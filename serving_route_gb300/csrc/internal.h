@@ -15,6 +15,7 @@ struct Workspace {
   uint32_t* status;        // device status word (MOE_DEV_* bits)
   int32_t* total_mtiles;   // number of 128-row GEMM tiles of this forward
   uint32_t* grid_sync;     // arrival counter of the one-kernel routing (zeroed before each forward)
+  int32_t* gemm_sched;     // [2] unit counters of the FC1 and FC2 launches (zeroed before each forward)
   int32_t* fc1_done;       // [max_mtiles] FC1 tiles published per m-tile (zeroed before each forward)
   int32_t* counts;         // [E]
   int32_t* offsets;        // [E+1]
@@ -139,6 +140,9 @@ struct GemmArgs {
   // m-tile start loading when it reaches fc1_ntiles
   int32_t* fc1_done;
   int fc1_ntiles;
+  // single-CTA launches: the dynamic schedule's unit counter (zeroed before
+  // each forward; one per launch), or nullptr for the static order
+  int32_t* sched;
 };
 cudaError_t gemm_set_attributes();
 int gemm_max_pairs();
