@@ -11,12 +11,14 @@ marshals numpy arrays through ctypes.
 
 Formats: ``fmt=0`` is the DeepSeek layout (1x128 activation, 128x128 weight
 scales); ``fmt=1`` is MXFP8 (one scale per 32 elements along K, for
-activations and for every weight row).
+activations and for every weight row); the per-tensor format (one scale per
+expert weight matrix, static calibrated activation scales) has its own
+functions, ``quant_weights_pt`` and ``forward_pt``.
 
 Parity status per function (pins live in ``tests/test_oracle_*.py``):
   e4m3 encode/decode, bf16 rounding, pow2 scale rule, 1x128 / 128x128 and
   MXFP8 1x32 quantisation, routing, FC1/FC2 block-scaled products in both
-  formats, combine: pinned.
+  formats, combine, the per-tensor quantisers and products: pinned.
   SwiGLU's exp: parity unpinned at the ulp level (host ``exp`` versus the
   GPU's ``expf``); covered by tolerance only.
   Combine summation order: parity unpinned at the ulp level (float64 here,
@@ -75,6 +77,14 @@ def lib():
         L.or_forward.restype = ctypes.c_uint32
         L.or_forward_fmt.argtypes = [i32] + L.or_forward.argtypes
         L.or_forward_fmt.restype = ctypes.c_uint32
+        f32 = ctypes.c_float
+        L.or_pt_weight_scale.argtypes = [vp, i64]
+        L.or_pt_weight_scale.restype = f32
+        L.or_quant_weights_pt.argtypes = [vp, i64, i64, i64, vp, vp]
+        L.or_quant_values_pt.argtypes = [vp, i64, f32, vp]
+        L.or_forward_pt.argtypes = ([i64, i32, i32, i32, i32, i32] + [vp] * 7 + [f32, f32]
+                                    + [vp] * 11)
+        L.or_forward_pt.restype = ctypes.c_uint32
         _lib = L
     return _lib
 
@@ -232,3 +242,64 @@ def forward(x_bits, idx, w, W1, W1s, W2, W2s, check=True, tok_sel=None, fmt=0):
     return dict(err=int(err), counts=counts, offsets=offsets, perm=perm[:R], inv=inv[:T * K],
                 xq=xq, xs=xs, A=A[:R], As=As[:R], gu=gu[:R], hq=hq[:R], hs=hs[:R], y=y[:R],
                 out=out)
+
+
+# --------------------------------------------------------------------------
+# per-tensor format
+# --------------------------------------------------------------------------
+def pt_weight_scale(w: np.ndarray) -> float:
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    return float(lib().or_pt_weight_scale(_p(w), w.size))
+
+
+def quant_weights_pt(w: np.ndarray):
+    """Per-tensor quantisation of float32 [nmat, rows, cols]: one scale per
+    matrix, s = float(amax / 448) -> (q uint8, s float32 [nmat])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    nmat, rows, cols = w.shape
+    q = np.empty(w.shape, np.uint8)
+    s = np.empty(nmat, np.float32)
+    lib().or_quant_weights_pt(_p(w), nmat, rows, cols, _p(q), _p(s))
+    return q, s
+
+
+def quant_values_pt(v: np.ndarray, scale: float) -> np.ndarray:
+    """E4M3 codes of float values (each exactly a float32) with a static scale."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    q = np.empty(v.shape, np.uint8)
+    lib().or_quant_values_pt(_p(v), v.size, float(np.float32(scale)), _p(q))
+    return q
+
+
+def forward_pt(x_bits, idx, w, W1, W1s, W2, W2s, x_scale, h_scale, check=True, tok_sel=None):
+    """Whole layer in the per-tensor format: W1s, W2s float32 [E]; x_scale and
+    h_scale the static activation scales.  Returns a dict like ``forward``
+    (no per-row scale arrays: the block scales are all 1)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    T, H = x.shape
+    K = idx.shape[1]
+    E, twoI, _ = W1.shape
+    I = twoI // 2
+    RK = max(T * K, 1)
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    perm = np.full(RK, -1, np.int32)
+    inv = np.empty(RK, np.int32)
+    xq = np.empty((T, H), np.uint8)
+    A = np.zeros((RK, H), np.uint8)
+    gu = np.zeros((RK, 2 * I), np.uint16)
+    hq = np.zeros((RK, I), np.uint8)
+    y = np.zeros((RK, H), np.uint16)
+    out = np.zeros((T, H), np.uint16)
+    ins = [np.ascontiguousarray(a) for a in (W1, np.asarray(W1s, np.float32), W2,
+                                             np.asarray(W2s, np.float32))]
+    ts = None if tok_sel is None else np.ascontiguousarray(tok_sel, dtype=np.uint8)
+    err = lib().or_forward_pt(T, H, I, E, K, int(check), _p(x), _p(idx), _p(w),
+                              *[_p(a) for a in ins], float(np.float32(x_scale)),
+                              float(np.float32(h_scale)), _p(ts), _p(counts), _p(offsets),
+                              _p(perm), _p(inv), _p(xq), _p(A), _p(gu), _p(hq), _p(y), _p(out))
+    R = int(offsets[E]) if err == 0 else 0
+    return dict(err=int(err), counts=counts, offsets=offsets, perm=perm[:R], inv=inv[:T * K],
+                xq=xq, A=A[:R], gu=gu[:R], hq=hq[:R], y=y[:R], out=out)

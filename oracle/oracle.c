@@ -37,6 +37,9 @@
  * one BF16 rounding.  Because block sums are exact, the compiler may evaluate
  * them in any order (the simd pragma); no result changes.
  *
+ * Format 2 (per-tensor scales, the "per_tensor" mode of flashinfer PR #4688)
+ * is defined beside its functions below.
+ *
  * Format 1 (MXFP8, "32e4m3xe8m0" on flashinfer PR #4688 and the SM100 MXFP8
  * megakernels of PR #4069's kernel drops): E4M3 values with one power-of-two
  * scale per 32 consecutive elements along K -- activations 1x32 (steps 2 and
@@ -413,6 +416,125 @@ uint32_t or_forward_fmt(int fmt, int64_t T, int H, int I, int E, int K, int chec
   or_expert_ffn_fmt(fmt, H, I, E, offsets, A, As, W1, W1s, W2, W2s, sel, gu, hq, hs, y);
   or_combine(T, K, H, inv, w, y, tok_sel, out);
   free(sel);
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Format 2: per-tensor FP8, the "per_tensor" scale mode of flashinfer PR #4688
+ * (Description, the scale-mode-equalized comparison: per_tensor needs
+ * offline-calibrated activation scales, blockwise needs none).  One FP32 scale
+ * per expert weight matrix and one static, calibrated FP32 scale per
+ * activation tensor (x, and the SwiGLU output h); no block scales.
+ *
+ *   quantise v with scale s:  q = E4M3_RNE_sat( float(v) * r ),  r = float(1 / s)
+ *       (r is the float division 1/s rounded once; the float product is rounded
+ *       once and then encoded; |v * r| >= 448 saturates to +-448)
+ *   weight scale of a matrix: s = float(amax / 448), or 1 for an all-zero matrix
+ *   FC1:  gu[pos, n] = BF16( (sum_j dec(A[pos,j]) * dec(W1[e,n,j])) * s_x * s_w1[e] )
+ *   FC2:  y[pos, c]  = BF16( (sum_j dec(hq[pos,j]) * dec(W2[e,c,j])) * s_h * s_w2[e] )
+ *
+ * Every product of two E4M3 values is a multiple of 2^-18 below 2^18, so a sum
+ * of up to 2^17 of them is an integer multiple of 2^-18 below 2^53 of those
+ * units: exact in double.  The two float scales multiply exactly in double
+ * (24-bit significands).  Only the final BF16 rounding rounds.  SwiGLU and
+ * combine are as in format 0.
+ * ------------------------------------------------------------------------- */
+
+/* one quantisation step of format 2: float product, then the E4M3 encoder */
+static uint8_t pt_encode(float v, float r) {
+  const float p = v * r;
+  return or_e4m3_encode((double)p);
+}
+
+/* scale of one weight matrix of n floats */
+float or_pt_weight_scale(const float* w, int64_t n) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    const float a = fabsf(w[i]);
+    if (a > amax) amax = a;
+  }
+  return amax > 0.0f ? amax / 448.0f : 1.0f;
+}
+
+/* w [nmat, rows, cols] float -> q (same shape), s [nmat] */
+void or_quant_weights_pt(const float* w, int64_t nmat, int64_t rows, int64_t cols, uint8_t* q,
+                         float* s) {
+  const int64_t n = rows * cols;
+  for (int64_t m = 0; m < nmat; ++m) {
+    const float sc = or_pt_weight_scale(w + m * n, n);
+    const float r = 1.0f / sc;
+    s[m] = sc;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) q[m * n + i] = pt_encode(w[m * n + i], r);
+  }
+}
+
+/* n float values (given as double, each exactly a float) with static scale s */
+void or_quant_values_pt(const double* v, int64_t n, float s, uint8_t* q) {
+  const float r = 1.0f / s;
+  for (int64_t i = 0; i < n; ++i) q[i] = pt_encode((float)v[i], r);
+}
+
+/* exact sum_j dec(a[j]) * dec(w[j]) over n terms (decoded values) */
+static double dot_exact(const double* a, const double* w, int64_t n) {
+  double acc = 0.0;
+#pragma omp simd reduction(+ : acc)
+  for (int64_t j = 0; j < n; ++j) acc += a[j] * w[j];
+  return acc;
+}
+
+/* The whole forward in format 2.  W1s / W2s are [E]; x_scale and h_scale the
+ * static activation scales.  Outputs as or_forward_fmt, without the per-row
+ * scale arrays (the block scales are all 1).  Returns the route error bits. */
+uint32_t or_forward_pt(int64_t T, int H, int I, int E, int K, int check, const uint16_t* x,
+                       const int32_t* idx, const float* w, const uint8_t* W1, const float* W1s,
+                       const uint8_t* W2, const float* W2s, float x_scale, float h_scale,
+                       const uint8_t* tok_sel, int32_t* counts, int32_t* offsets, int32_t* perm,
+                       int32_t* inv, uint8_t* xq, uint8_t* A, uint16_t* gu, uint8_t* hq,
+                       uint16_t* y, uint16_t* out) {
+  uint32_t err = or_route(T, K, E, idx, w, check, counts, offsets, perm, inv);
+  if (err) return err;
+  const int64_t R = offsets[E];
+  /* 1. quantise x with the static scale */
+  {
+    const float rx = 1.0f / x_scale;
+    for (int64_t i = 0; i < T * (int64_t)H; ++i) xq[i] = pt_encode((float)or_bf16_decode(x[i]), rx);
+  }
+  /* 2. gather */
+  for (int64_t p = 0; p < R; ++p) memcpy(A + p * H, xq + (int64_t)(perm[p] / K) * H, (size_t)H);
+  /* 3. expert FFN, expert by expert */
+  const float rh = 1.0f / h_scale;
+  double* w1d = (double*)malloc(sizeof(double) * (size_t)(2 * I) * (size_t)H);
+  double* w2d = (double*)malloc(sizeof(double) * (size_t)H * (size_t)I);
+  for (int e = 0; e < E; ++e) {
+    const int64_t p0 = offsets[e], p1 = offsets[e + 1];
+    int any = 0;
+    for (int64_t p = p0; p < p1; ++p)
+      if (!tok_sel || tok_sel[perm[p] / K]) any = 1;
+    if (!any) continue;
+    decode_e4m3_array(W1 + (int64_t)e * 2 * I * H, (int64_t)2 * I * H, w1d);
+    decode_e4m3_array(W2 + (int64_t)e * H * I, (int64_t)H * I, w2d);
+    const double f1 = (double)x_scale * (double)W1s[e];
+    const double f2 = (double)h_scale * (double)W2s[e];
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t p = p0; p < p1; ++p) {
+      if (tok_sel && !tok_sel[perm[p] / K]) continue;
+      double* a = (double*)malloc(sizeof(double) * (size_t)H);
+      double* hd = (double*)malloc(sizeof(double) * (size_t)I);
+      uint16_t* gup = gu + p * 2 * I;
+      decode_e4m3_array(A + p * H, H, a);
+      for (int n = 0; n < 2 * I; ++n) gup[n] = or_bf16_round(dot_exact(a, w1d + (int64_t)n * H, H) * f1);
+      for (int n = 0; n < I; ++n) hq[p * I + n] = pt_encode(or_swiglu(gup[n], gup[I + n]), rh);
+      decode_e4m3_array(hq + p * I, I, hd);
+      for (int c = 0; c < H; ++c)
+        y[p * H + c] = or_bf16_round(dot_exact(hd, w2d + (int64_t)c * I, I) * f2);
+      free(a);
+      free(hd);
+    }
+  }
+  free(w1d);
+  free(w2d);
+  or_combine(T, K, H, inv, w, y, tok_sel, out);
   return 0;
 }
 
