@@ -64,8 +64,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--unfused", action="store_true", help="time the unfused reference path")
     p.add_argument("--gemm", default="auto", choices=["auto", "single", "pair"])
-    p.add_argument("--format", default="deepseek", choices=["deepseek", "mxfp8"],
-                   help="block scales: DeepSeek 1x128 / 128x128, or MXFP8 1x32 along K")
+    p.add_argument("--format", default="deepseek", choices=["deepseek", "mxfp8", "per_tensor"],
+                   help="scales: DeepSeek 1x128 / 128x128 blocks, MXFP8 1x32 along K, or per "
+                        "tensor (one per expert weight matrix, static activation scales)")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling only: the workload with this many experts (smaller weights)")
     p.add_argument("--tokens", type=int, default=0,
@@ -442,13 +443,15 @@ def side_stream_sweep(args, torch, layer, x, idx, wts, wl, dev, flush):
 def gpu_weights(torch, g, layer_cls, wl, fmt, dev, stream):
     """Weights of a workload generated on the GPU by the shared seeded
     generator and quantised there (moe_quantize_weights), in expert chunks."""
-    mx = fmt == "mxfp8"
+    mx, pt = fmt == "mxfp8", fmt == "per_tensor"
     sp = stream.cuda_stream
     w1q = torch.empty((wl.E, 2 * wl.I, wl.H), dtype=torch.uint8, device=dev)
-    w1s = torch.empty((wl.E, 2 * wl.I, wl.H // 32) if mx else (wl.E, 2 * wl.I // 128, wl.H // 128),
+    w1s = torch.empty((wl.E,) if pt else ((wl.E, 2 * wl.I, wl.H // 32) if mx
+                                          else (wl.E, 2 * wl.I // 128, wl.H // 128)),
                       dtype=torch.float32, device=dev)
     w2q = torch.empty((wl.E, wl.H, wl.I), dtype=torch.uint8, device=dev)
-    w2s = torch.empty((wl.E, wl.H, wl.I // 32) if mx else (wl.E, wl.H // 128, wl.I // 128),
+    w2s = torch.empty((wl.E,) if pt else ((wl.E, wl.H, wl.I // 32) if mx
+                                          else (wl.E, wl.H // 128, wl.I // 128)),
                       dtype=torch.float32, device=dev)
     chunk = 16
     with torch.cuda.stream(stream):
@@ -469,6 +472,22 @@ def gpu_weights(torch, g, layer_cls, wl, fmt, dev, stream):
             del f, q, s
     stream.synchronize()
     return w1q, w1s, w2q, w2s
+
+
+def bind(layer, weights, fmt, stream):
+    """bind the weights; a per-tensor layer also gets the workloads' static
+    activation scales"""
+    from gen import configs
+    layer.bind_weights(*weights, stream)
+    if fmt == "per_tensor":
+        layer.set_activation_scales(float(configs.PT_X_SCALE), float(configs.PT_H_SCALE), stream)
+
+
+def fmt_name(fmt):
+    return {"mxfp8": "MXFP8: E4M3, E8M0 scale per 32 along K",
+            "per_tensor": "E4M3, per-tensor scales (one per expert weight matrix; static x and h "
+                          "scales 6/448 and 24/448)"}.get(fmt, "E4M3, 1x128 activation / 128x128 "
+                                                              "weight scales")
 
 
 def device_inputs(torch, g, wl, dev, stream):
@@ -654,7 +673,7 @@ def measure_record(torch, S, g, name, args, dev, stream, flush, weights_cache):
     layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, expected_m=wl.T,
                            fuse_fc1=not args.unfused, check_routes=True, gemm=args.gemm,
                            gemms=args.gemms, fmt=args.format)
-    layer.bind_weights(*weights_cache[key], stream)
+    bind(layer, weights_cache[key], args.format, stream)
     x, idx, wts, _, _, counts = device_inputs(torch, g, wl, dev, stream)
     torch.cuda.synchronize()
     timer = StepTimer(torch, layer, x, idx, wts, stream, flush, not args.no_graph)
@@ -718,7 +737,7 @@ def main():
     # weights: generated and quantised on the GPU, bound once; kept for the
     # per-workload record when workloads there share them (dsv3 prefill/decode)
     weights = gpu_weights(torch, g, S.MegaMoELayer, wl, args.format, dev, stream)
-    layer.bind_weights(*weights, stream)
+    bind(layer, weights, args.format, stream)
     weights_cache = {}
     if not (args.experts or args.tokens):
         weights_cache[(wl.H, wl.I, wl.E, wl.seed)] = weights
@@ -871,8 +890,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "K": wl.K,
                    "fc1_epilogue": "fused" if fused else "unfused",
-                   "format": ("MXFP8: E4M3, E8M0 scale per 32 along K" if args.format == "mxfp8"
-                              else "E4M3, 1x128 activation / 128x128 weight scales"),
+                   "format": fmt_name(args.format),
                    "l2": l2_note(wl, lroof["b_alg_bytes"]),
                    "launch": "cuda graph replay" if graph_used else "direct launches",
                    **tactic_str(layer, plan),

@@ -112,6 +112,18 @@ typedef enum moe_status {
  * marks its routes unrouted, so the forward computes no expert and writes a
  * zero output, and the context stays usable. */
 #define MOE_FLAG_WATCHDOG_ROUTE_TEST 0x200u
+/* Per-tensor FP8 instead of block scales: the "per_tensor" scale mode of
+ * flashinfer PR #4688 (Description; the scale-mode-equalized comparison:
+ * per_tensor needs offline-calibrated activation scales identical on every
+ * rank, blockwise needs none).  One FP32 scale per expert weight matrix
+ * (moe_quantize_weights_pt) and one static, calibrated FP32 scale per
+ * activation tensor -- x and the SwiGLU output h -- given with
+ * moe_set_activation_scales.  A value v with scale s is stored as
+ * E4M3_RNE_sat(float(v) * float(1/s)) (saturating to +-448); the GEMMs run
+ * with unit block scales and multiply their FP32 accumulators by
+ * x_scale * s_w1[e] (FC1) and h_scale * s_w2[e] (FC2) before the BF16
+ * rounding.  Not combinable with MOE_FLAG_MXFP8 (MOE_ERR_INVALID_ARG). */
+#define MOE_FLAG_PER_TENSOR 0x400u
 
 typedef struct moe_dims {
   int32_t hidden;      /* H: multiple of 128, 128..16384 */
@@ -192,6 +204,22 @@ MOE_API moe_status moe_quantize_weights_mx(const float* d_w, int64_t num_mats, i
                                            struct CUstream_st* stream);
 
 /*
+ * moe_quantize_weights_pt -- FP32 expert weights to the per-tensor form that
+ * moe_bind_weights takes under MOE_FLAG_PER_TENSOR: one scale per matrix,
+ * s = float(amax / 448) (1 for an all-zero matrix), codes =
+ * E4M3_RNE_sat(w * float(1 / s)) (the per_tensor mode of flashinfer PR #4688).
+ *   d_w     float [num_mats, rows, cols]; rows and cols multiples of 128,
+ *           num_mats <= 65535.
+ *   d_q     uint8 [num_mats, rows, cols] (output).
+ *   d_scale float [num_mats] (output; also the pass's only scratch).
+ * Asynchronous on `stream`.  MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED as
+ * moe_quantize_weights.
+ */
+MOE_API moe_status moe_quantize_weights_pt(const float* d_w, int64_t num_mats, int32_t rows,
+                                           int32_t cols, uint8_t* d_q, float* d_scale,
+                                           struct CUstream_st* stream);
+
+/*
  * moe_bind_weights -- the layer holds its static weights in a transformed,
  * kernel-ready form that is built once, at set-up (flashinfer PR #4069,
  * "Contracts introduced by this PR": the stateful backend contract).  Copies
@@ -203,6 +231,8 @@ MOE_API moe_status moe_quantize_weights_mx(const float* d_w, int64_t num_mats, i
  *               (MOE_FLAG_MXFP8: [E, 2I, H/32], one per row and 32 columns).
  *   d_w2        E4M3 [E, H, I].
  *   d_w2_scale  float [E, H/128, I/128], powers of two (MXFP8: [E, H, I/32]).
+ *   Under MOE_FLAG_PER_TENSOR: d_w1_scale and d_w2_scale are float [E], one
+ *   positive finite scale per expert matrix (MOE_ERR_BAD_SCALE otherwise).
  * Enqueued on `stream`, then waits for that stream: the caller may free the
  * inputs when this returns.  Returns MOE_ERR_BAD_SCALE if any scale is not a
  * power of two within the E8M0 range.
@@ -210,6 +240,22 @@ MOE_API moe_status moe_quantize_weights_mx(const float* d_w, int64_t num_mats, i
 MOE_API moe_status moe_bind_weights(moe_handle* h, const uint8_t* d_w1, const float* d_w1_scale,
                             const uint8_t* d_w2, const float* d_w2_scale,
                             struct CUstream_st* stream);
+
+/*
+ * moe_set_activation_scales -- the static, offline-calibrated activation
+ * scales of a per-tensor layer (MOE_FLAG_PER_TENSOR; the pages' per_tensor
+ * mode needs them calibrated ahead of time, identical on every rank):
+ * x_scale for the layer input x, h_scale for the SwiGLU output h.  Both must
+ * be positive and finite (MOE_ERR_INVALID_ARG).  MOE_ERR_UNSUPPORTED for a
+ * block-scaled layer.  A per-tensor forward returns MOE_ERR_NOT_BOUND until
+ * this has been called.  Enqueued on `stream` when the weights are bound
+ * (the per-expert epilogue factors are computed on the device from the bound
+ * weight scales), else applied by the next moe_bind_weights; may be called
+ * again to change the scales, also between graph replays (the kernels read
+ * them from the weight store).
+ */
+MOE_API moe_status moe_set_activation_scales(moe_handle* h, float x_scale, float h_scale,
+                                             struct CUstream_st* stream);
 
 /*
  * moe_stage_inputs -- binds the caller's BF16 output tensor d_out [max_rows, H]

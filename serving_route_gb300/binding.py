@@ -42,10 +42,11 @@ MOE_FLAG_SPLIT_GEMMS = 0x40
 MOE_FLAG_GEMMS_ONE_LAUNCH = 0x80
 MOE_FLAG_MXFP8 = 0x100
 MOE_FLAG_WATCHDOG_ROUTE_TEST = 0x200
+MOE_FLAG_PER_TENSOR = 0x400
 
 # every function the header declares (checked against include/megamoe.h by a test)
 API_NAMES = ("moe_workspace_query", "moe_create", "moe_quantize_weights", "moe_quantize_weights_mx",
-             "moe_bind_weights",
+             "moe_quantize_weights_pt", "moe_bind_weights", "moe_set_activation_scales",
              "moe_stage_inputs", "moe_forward", "moe_read_status", "moe_debug_views",
              "moe_set_profile_events", "moe_set_sm_budget", "moe_forward_plan", "moe_route_noalloc",
              "moe_destroy", "moe_status_str")
@@ -97,6 +98,8 @@ def lib() -> ctypes.CDLL:
                                  ctypes.c_size_t, vp, ctypes.c_size_t, ctypes.POINTER(vp)]
         L.moe_quantize_weights.argtypes = [vp, i64, i32, i32, vp, vp, vp]
         L.moe_quantize_weights_mx.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+        L.moe_quantize_weights_pt.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+        L.moe_set_activation_scales.argtypes = [vp, ctypes.c_float, ctypes.c_float, vp]
         L.moe_bind_weights.argtypes = [vp, vp, vp, vp, vp, vp]
         L.moe_stage_inputs.argtypes = [vp, vp]
         L.moe_forward.argtypes = [vp, vp, vp, vp, i64, vp]
@@ -155,6 +158,16 @@ def moe_quantize_weights(d_w, num_mats, rows, cols, d_q, d_scale, stream) -> Non
 def moe_quantize_weights_mx(d_w, num_mats, rows, cols, d_q, d_scale, stream) -> None:
     _check(lib().moe_quantize_weights_mx(d_w, num_mats, rows, cols, d_q, d_scale, stream),
            "moe_quantize_weights_mx")
+
+
+def moe_quantize_weights_pt(d_w, num_mats, rows, cols, d_q, d_scale, stream) -> None:
+    _check(lib().moe_quantize_weights_pt(d_w, num_mats, rows, cols, d_q, d_scale, stream),
+           "moe_quantize_weights_pt")
+
+
+def moe_set_activation_scales(h, x_scale, h_scale, stream) -> None:
+    _check(lib().moe_set_activation_scales(h, x_scale, h_scale, stream),
+           "moe_set_activation_scales")
 
 
 def moe_bind_weights(h, d_w1, d_w1s, d_w2, d_w2s, stream) -> None:

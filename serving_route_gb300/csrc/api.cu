@@ -33,6 +33,8 @@ struct moe_handle {
   int route_coop_blocks;                    // co-resident grid limit of the one-kernel routing
   int quant_resident[2];                    // resident blocks of quant_dispatch, 2 / 4 units per pass
   bool bound;
+  bool pt_scales;                           // per-tensor: activation scales given
+  float pt_x_scale, pt_h_scale;
   uint16_t* out;
   int num_sms;
   int device;
@@ -212,6 +214,8 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
   L->nb_max = (max_rows + 127) / 128;
   L->keep_gu = !(d->flags & MOE_FLAG_FUSE_FC1_EPILOGUE) || (d->flags & MOE_FLAG_EMIT_FC1);
   L->mx = (d->flags & MOE_FLAG_MXFP8) != 0;
+  L->pt = (d->flags & MOE_FLAG_PER_TENSOR) != 0;
+  if (L->mx && L->pt) return MOE_ERR_INVALID_ARG;
   const size_t H = L->H, I = L->I, E = L->E, R = L->rows_alloc, MB = R / 128;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -248,6 +252,7 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
   L->o_w2_sf = take(E * (H / 128) * (I / 128));
   L->o_w1_sfatoms = take(E * (2 * I / 128) * atoms_along_k(H / 128, L->mx) * kSfAtomBytes);
   L->o_w2_sfatoms = take(E * (H / 128) * atoms_along_k(I / 128, L->mx) * kSfAtomBytes);
+  L->o_pt = L->pt ? take(4 * (4 * E + 2)) : 0;
   L->w_bytes = o + kAlign;
   return MOE_OK;
 }
@@ -295,8 +300,9 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   h->expected_m = expected_m;
   h->num_sms = sms;
   h->route_coop_blocks = route_fused_max_blocks(L.E);
-  h->quant_resident[0] = quant_dispatch_resident(L.mx, 2);
-  h->quant_resident[1] = quant_dispatch_resident(L.mx, 4);
+  const int fmt = L.pt ? 2 : (L.mx ? 1 : 0);
+  h->quant_resident[0] = quant_dispatch_resident(fmt, 2);
+  h->quant_resident[1] = quant_dispatch_resident(fmt, 4);
   h->device = dev;
   uint8_t* b = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(d_workspace), kAlign));
   Workspace& w = h->ws;
@@ -329,6 +335,7 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   h->wst.w2_sf = wb + L.o_w2_sf;
   h->wst.w1_sfatoms = wb + L.o_w1_sfatoms;
   h->wst.w2_sfatoms = wb + L.o_w2_sfatoms;
+  h->wst.pt = L.pt ? reinterpret_cast<float*>(wb + L.o_pt) : nullptr;
   if (!encode_blocked_map(&h->tm_a, w.a, L.H / 128, (uint64_t)(L.rows_alloc / 128)) ||
       !encode_blocked_map(&h->tm_hq, w.hq, L.I / 128, (uint64_t)(L.rows_alloc / 128)) ||
       !encode_atom_map(&h->tm_asf, w.a_sf, (uint64_t)(L.rows_alloc / 128) * atoms_along_k(L.H / 128, L.mx)) ||
@@ -374,6 +381,35 @@ moe_status moe_quantize_weights_mx(const float* d_w, int64_t num_mats, int32_t r
   return MOE_OK;
 }
 
+moe_status moe_quantize_weights_pt(const float* d_w, int64_t num_mats, int32_t rows, int32_t cols,
+                                   uint8_t* d_q, float* d_scale, struct CUstream_st* stream) {
+  if (!d_w || !d_q || !d_scale || num_mats < 0 || rows <= 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+  if (rows % 128 || cols % 128) return MOE_ERR_UNSUPPORTED;
+  if (num_mats > 65535) return MOE_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(d_w) % 16 || reinterpret_cast<uintptr_t>(d_q) % 16 ||
+      reinterpret_cast<uintptr_t>(d_scale) % 4)
+    return MOE_ERR_INVALID_ARG;
+  if (launch_quantize_weights_pt(d_w, num_mats, rows, cols, d_q, d_scale, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_set_activation_scales(moe_handle* h, float x_scale, float h_scale,
+                                     struct CUstream_st* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (!h->L.pt) return MOE_ERR_UNSUPPORTED;
+  if (!(x_scale > 0.f) || !std::isfinite(x_scale) || !(h_scale > 0.f) || !std::isfinite(h_scale))
+    return MOE_ERR_INVALID_ARG;
+  h->pt_x_scale = x_scale;
+  h->pt_h_scale = h_scale;
+  h->pt_scales = true;
+  // the epilogue factors need the bound weight scales; before the bind they
+  // are computed there
+  if (h->bound && launch_pt_set_scales(h->wst, h->L, x_scale, h_scale, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status moe_bind_weights(moe_handle* h, const uint8_t* d_w1, const float* d_w1_scale,
                             const uint8_t* d_w2, const float* d_w2_scale,
                             struct CUstream_st* stream) {
@@ -384,6 +420,9 @@ moe_status moe_bind_weights(moe_handle* h, const uint8_t* d_w1, const float* d_w
   if (cudaMemsetAsync(h->ws.status, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_bind_transform(h->wst, L, d_w1, d_w1_scale, d_w2, d_w2_scale, h->ws.status, stream) !=
       cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (L.pt && h->pt_scales &&
+      launch_pt_set_scales(h->wst, L, h->pt_x_scale, h->pt_h_scale, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   uint32_t st = 0;
   if (cudaMemcpyAsync(&st, h->ws.status, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
@@ -407,7 +446,7 @@ moe_status moe_stage_inputs(moe_handle* h, uint16_t* d_out) {
 moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk_idx,
                        const float* d_topk_w, int64_t num_tokens, struct CUstream_st* stream) {
   if (!h) return MOE_ERR_INVALID_ARG;
-  if (!h->bound || !h->out) return MOE_ERR_NOT_BOUND;
+  if (!h->bound || !h->out || (h->L.pt && !h->pt_scales)) return MOE_ERR_NOT_BOUND;
   if (num_tokens < 0) return MOE_ERR_INVALID_ARG;
   if (num_tokens > h->L.max_rows) return MOE_ERR_CAPACITY;
   if (num_tokens == 0) return MOE_OK;
@@ -445,8 +484,11 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   // cannot be confined to a subset of SMs, and one CTA per budgeted SM
   // starves them of memory parallelism.  The budget caps the persistent GEMM.
   const int stream_ctas = 16 * h->num_sms;
+  // per-tensor: the reciprocals and per-expert factors in the weight store
+  const float* pt_rx = L.pt ? h->wst.pt + 4 * L.E : nullptr;
+  const float* pt_rh = L.pt ? h->wst.pt + 4 * L.E + 1 : nullptr;
   if (launch_quant_dispatch(ws, L, d_x, num_tokens, s, pdl, stream_ctas, h->quant_resident[0],
-                            h->quant_resident[1]) != cudaSuccess)
+                            h->quant_resident[1], pt_rx) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   GemmArgs g1;
@@ -484,6 +526,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   // keep the static order.
   const bool dyn_sched = !L.pair && num_tokens * L.K < 128 * (int64_t)L.E;
   g1.sched = dyn_sched ? ws.gemm_sched : nullptr;
+  g1.pt_scale = L.pt ? h->wst.pt + 2 * L.E : nullptr;
+  g1.pt_rh = pt_rh;
   const GemmMode m1 = fused ? (emit ? kModeFusedGU : kModeFused) : kModeGU;
   if (ev) record_event(ev[5], s);
   const bool pair = L.pair;
@@ -492,7 +536,8 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
                            ctas, s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[6], s);
-  if (!fused && launch_swiglu_quant(ws, L, stream_ctas, s, pdl) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!fused && launch_swiglu_quant(ws, L, stream_ctas, s, pdl, pt_rh) != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   GemmArgs g2;
   memset(&g2, 0, sizeof(g2));
@@ -514,6 +559,7 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.status = ws.status;
   g2.wait_limit_ns = g1.wait_limit_ns;
   g2.sched = dyn_sched ? ws.gemm_sched + 1 : nullptr;
+  g2.pt_scale = L.pt ? h->wst.pt + 3 * L.E : nullptr;
   if (ev) record_event(ev[7], s);
   if (mega) {
     // the FC1 epilogue publishes, per m-tile, how many of its NT tiles are stored

@@ -540,6 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // padding skips the drain, the arithmetic and the stores.
       const int e_t = g.mtile_expert[mt];
       const bool live = q * 32 < g.pad_offsets[e_t] + g.counts[e_t] - mt * 128;
+      // per-tensor format: the expert's factor on the FP32 accumulator (1
+      // for the block-scaled formats, whose scales the tensor core applied)
+      const float* pts = (kMega && ph) ? g2.pt_scale : g.pt_scale;
+      const float acc_f = pts ? pts[e_t] : 1.0f;  // (unused without per-tensor scales)
       // the epilogue of this unit: the launch's mode, or per phase in the
       // megakernel (FC1 fused, with gate||up kept when its output is bound)
       const int em = kMega ? (ph ? kModeY : (g.out ? kModeFusedGU : kModeFused)) : MODE;
@@ -564,12 +568,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tlane + 128 + half * 64 + 32, r[3]);
         }
         tmem_ld_wait();
+        if (pts) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[c * 16 + j] =
-                pack_bf16x2(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1]));
+            for (int j = 0; j < 16; ++j)
+              pk[c * 16 + j] = pack_bf16x2(__fmul_rn(__uint_as_float(r[c][2 * j]), acc_f),
+                                           __fmul_rn(__uint_as_float(r[c][2 * j + 1]), acc_f));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[c * 16 + j] =
+                  pack_bf16x2(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1]));
+        }
       }
       // The TMEM reads above have completed (tcgen05.wait::ld); the arrive
       // passes no data through memory, so in the pair it is relaxed: a
@@ -636,7 +649,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                        pk[32 + 8 * v + 6], pk[32 + 8 * v + 7]);
         }
       }
-      if (em_fused && g.mx && active) {
+      if (em_fused && g.pt_rh && active) {
+        // per-tensor: h * (1 / h_scale) rounded once in float, then E4M3;
+        // the block scale is 1 (no amax exchange)
+        float h[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          h[2 * i] = swiglu(bf16_bits_to_float(pk[i] & 0xFFFFu),
+                            bf16_bits_to_float(pk[32 + i] & 0xFFFFu));
+          h[2 * i + 1] = swiglu(bf16_bits_to_float(pk[i] >> 16), bf16_bits_to_float(pk[32 + i] >> 16));
+        }
+        const float rh = *g.pt_rh;
+        uint8_t* dq = g.hq + blocked_offset(row, (int64_t)nt * 128 + half * 64, g.inter);
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          uint32_t w[8];
+#pragma unroll
+          for (int uu = 0; uu < 8; ++uu) {
+            const int j = 32 * v + 4 * uu;
+            w[uu] = e4m3x4(__fmul_rn(h[j], rh), __fmul_rn(h[j + 1], rh), __fmul_rn(h[j + 2], rh),
+                           __fmul_rn(h[j + 3], rh));
+          }
+          st_global_v8(dq + 32 * v, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+        }
+        if (half == 0) g.h_sf[sf_atom_offset(row, nt, g.IB)] = (uint8_t)127;
+      } else if (em_fused && g.mx && active) {
         // MXFP8: this thread's 64 h columns are two whole 32-wide chunks of
         // its row, so each gets its scale without any exchange
         float h[64];
@@ -663,14 +700,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           st_global_v8(dq + 32 * v, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
           g.h_sf[sf_atom_offset(row, 4 * nt + 2 * half + v, 4 * g.IB)] = (uint8_t)(e + 127);
         }
-      } else if (em_fused && !g.mx && !active) {
+      } else if (em_fused && !g.mx && !g.pt_rh && !active) {
         // a padding quadrant (both of its warps decide alike) still completes
         // this tile's phase of the amax exchange, which every 1x128 fused
         // tile advances once (MXFP8 tiles have no exchange)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&amax_bar[q]));
         if (!mbar_wait(smem_u32(&amax_bar[q]), tile_par, abort, g.status, g.wait_limit_ns)) break;
-      } else if (em_fused && !g.mx) {
+      } else if (em_fused && !g.mx && !g.pt_rh) {
         // gate pairs pk[0..31], up pairs pk[32..63] -> h[0..63]
         float h[64];
         float amax = 0.f;

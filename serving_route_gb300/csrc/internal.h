@@ -43,11 +43,16 @@ struct WeightStore {
   uint8_t* w2_sf;  // [E, H/128, I/128] E8M0
   uint8_t* w1_sfatoms;  // [E][2I/128][ceil(H/512)][512]: w1_sf as GEMM scale atoms
   uint8_t* w2_sfatoms;  // [E][H/128][ceil(I/512)][512]
+  // per-tensor format: float [4E + 2] = the weight scales s_w1[E], s_w2[E],
+  // the epilogue factors x_scale * s_w1[E], h_scale * s_w2[E], then the
+  // reciprocals 1/x_scale, 1/h_scale (nullptr in the block-scaled formats)
+  float* pt;
 };
 
 struct Layout {
   int H, I, E, K;
   bool mx;             // MXFP8: one scale per 32-wide K chunk (else 1x128 / 128x128)
+  bool pt;             // per-tensor scales (block scales all 1; factors in the epilogues)
   int pad_rows;        // expert segments padded to this many rows (128, or 256 for CTA pairs)
   bool pair;           // GEMMs run on CTA pairs (tcgen05 cta_group::2)
   int64_t max_rows;
@@ -60,7 +65,7 @@ struct Layout {
   size_t o_fc1_done;   // [max_mtiles] int32 counters of the megakernel, right after the status
   size_t o_status, o_counts, o_offsets, o_pad_offsets, o_mtile_expert, o_block_counts, o_base_u,
       o_base_p, o_perm, o_inv, o_inv_pad, o_a, o_a_sf, o_gu, o_hq, o_h_sf, o_y;
-  size_t o_w1, o_w2, o_w1_sf, o_w2_sf, o_w1_sfatoms, o_w2_sfatoms;
+  size_t o_w1, o_w2, o_w1_sf, o_w2_sf, o_w1_sfatoms, o_w2_sfatoms, o_pt;
 };
 
 // Scale atoms along K: one per four 128-wide K blocks (one byte per block),
@@ -87,16 +92,22 @@ int route_fused_max_blocks(int E);
 
 // quant.cu
 // Resident blocks (all SMs) of quant_dispatch with two or four units per
-// warp pass (batch 2 or 4); 0 if the query fails.
-int quant_dispatch_resident(bool mx, int batch);
+// warp pass (batch 2 or 4) for format fmt (0 1x128, 1 MXFP8, 2 per-tensor);
+// 0 if the query fails.
+int quant_dispatch_resident(int fmt, int batch);
 // pdl: launch as a programmatic dependent of the previous kernel on `s`;
 // max_ctas: grid cap of the streaming kernels; resident2 / resident4: the
 // two forms' resident blocks (four units per warp where that makes one wave)
+// pt_rx / pt_rh: the per-tensor reciprocals in the weight store (per-tensor only)
 cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
                                   int64_t T, cudaStream_t s, bool pdl, int max_ctas,
-                                  int resident2, int resident4);
+                                  int resident2, int resident4, const float* pt_rx);
 cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int max_ctas, cudaStream_t s,
-                                bool pdl);
+                                bool pdl, const float* pt_rh);
+cudaError_t launch_quantize_weights_pt(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
+                                       float* scale, cudaStream_t s);
+cudaError_t launch_pt_set_scales(const WeightStore& wst, const Layout& L, float x_scale,
+                                 float h_scale, cudaStream_t s);
 cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
                                     float* scale, cudaStream_t s);
 cudaError_t launch_quantize_weights_mx(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
@@ -143,6 +154,11 @@ struct GemmArgs {
   // single-CTA launches: the dynamic schedule's unit counter (zeroed before
   // each forward; one per launch), or nullptr for the static order
   int32_t* sched;
+  // per-tensor format: per-expert factors applied to the FP32 accumulator
+  // before the BF16 rounding, and (FC1) the h scale's float reciprocal;
+  // nullptr in the block-scaled formats
+  const float* pt_scale;
+  const float* pt_rh;
 };
 cudaError_t gemm_set_attributes();
 int gemm_max_pairs();

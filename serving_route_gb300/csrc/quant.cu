@@ -34,6 +34,15 @@ __device__ __forceinline__ uint2 quant8(const float (&v)[8], int e) {
   return q;
 }
 
+// 8 floats -> 8 E4M3 codes of v * r (the per-tensor rule: one float product,
+// then round to nearest even, saturating).
+__device__ __forceinline__ uint2 quant8_rcp(const float (&v)[8], float r) {
+  uint2 q;
+  q.x = e4m3x4(__fmul_rn(v[0], r), __fmul_rn(v[1], r), __fmul_rn(v[2], r), __fmul_rn(v[3], r));
+  q.y = e4m3x4(__fmul_rn(v[4], r), __fmul_rn(v[5], r), __fmul_rn(v[6], r), __fmul_rn(v[7], r));
+  return q;
+}
+
 __device__ __forceinline__ void unpack_bf16x8(const uint4 p, float (&v)[8]) {
   const uint32_t w[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
@@ -54,12 +63,15 @@ __device__ __forceinline__ float group8_max(float v) {
   return v;
 }
 
-// MX: MXFP8, one scale per 32 columns (a lane pair) instead of per 128.
-template <bool MX>
+// FMT 0: one power-of-two scale per 128 columns; 1 (MXFP8): one per 32
+// columns (a lane pair); 2 (per-tensor): the static scale's float reciprocal
+// rx for every value, block scales 1.
+template <int FMT>
 __device__ __forceinline__ void quant_dispatch_unit(const uint4 (&raw)[2], bool valid, int p_lane,
-                                                    int b, int H, int K, int l8,
+                                                    int b, int H, int K, int l8, float rx,
                                                     uint8_t* __restrict__ a,
                                                     uint8_t* __restrict__ a_sf) {
+  constexpr bool MX = FMT == 1;
   float v[16];
   if (valid) {
     float lo[8], hi[8];
@@ -74,12 +86,16 @@ __device__ __forceinline__ void quant_dispatch_unit(const uint4 (&raw)[2], bool 
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = 0.f;
   }
-  float amax = 0.f;
+  int e = 0;
+  float inv = rx;
+  if (FMT != 2) {
+    float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  amax = MX ? fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1)) : group8_max(amax);
-  const int e = pow2_scale_exp(amax);
-  const float inv = pow2_neg(e);
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = MX ? fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1)) : group8_max(amax);
+    e = pow2_scale_exp(amax);
+    inv = pow2_neg(e);
+  }
   uint4 q;
   q.x = e4m3x4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
   q.y = e4m3x4(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
@@ -103,10 +119,10 @@ __device__ __forceinline__ void quant_dispatch_unit(const uint4 (&raw)[2], bool 
 // B = 2: two units per pass, one unit per warp while the grid is not capped.
 // B = 4: four units per pass at 64 registers (four blocks per SM), for a grid
 // that then fits in one wave.
-template <bool MX, int B>
+template <int FMT, int B>
 __global__ void __launch_bounds__(256, B == 4 ? 4 : 1) quant_dispatch_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ inv_pad, int64_t T, int H, int K,
-    uint8_t* __restrict__ a, uint8_t* __restrict__ a_sf) {
+    const float* __restrict__ pt_rx, uint8_t* __restrict__ a, uint8_t* __restrict__ a_sf) {
   const int lane = threadIdx.x & 31, grp = lane >> 3, l8 = lane & 7;
   const int KB = H >> 7;
   const int units = (KB + 3) >> 2;
@@ -142,24 +158,29 @@ __global__ void __launch_bounds__(256, B == 4 ? 4 : 1) quant_dispatch_kernel(
       pdl_wait();
       waited = true;
     }
+    // per-tensor: the static scale's reciprocal (written by
+    // moe_set_activation_scales before any forward)
+    const float rx = FMT == 2 ? *pt_rx : 1.0f;
     int p[B];
 #pragma unroll
     for (int i = 0; i < B; ++i)
       p[i] = (lane < K && u0 + i * nwarps < total) ? inv_pad[(int64_t)t[i] * K + lane] : -1;
 #pragma unroll
     for (int i = 0; i < B; ++i)
-      quant_dispatch_unit<MX>(r[i], v[i], p[i], b[i], H, K, l8, a, a_sf);
+      quant_dispatch_unit<FMT>(r[i], v[i], p[i], b[i], H, K, l8, rx, a, a_sf);
   }
   pdl_trigger();
 }
 
 // Unfused SwiGLU + re-quantisation over the padded GEMM rows of this forward
 // (MX: one scale per 32 columns, four lanes, instead of per 128).
-template <bool MX>
+template <int FMT>
 __global__ void __launch_bounds__(256) swiglu_quant_kernel(
     const uint16_t* __restrict__ gu, const int32_t* __restrict__ total_mtiles, int I,
-    uint8_t* __restrict__ hq, uint8_t* __restrict__ h_sf) {
+    const float* __restrict__ pt_rh, uint8_t* __restrict__ hq, uint8_t* __restrict__ h_sf) {
+  constexpr bool MX = FMT == 1;
   pdl_wait();
+  const float rh = FMT == 2 ? *pt_rh : 1.0f;
   const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
   const int IB = I >> 7;
   const int units = (IB + 1) >> 1;
@@ -191,9 +212,10 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(
     } else {
       amax = half_warp_max(amax);
     }
-    const int e = pow2_scale_exp(amax);
+    const int e = FMT == 2 ? 0 : pow2_scale_exp(amax);
     if (valid) {
-      *reinterpret_cast<uint2*>(hq + blocked_offset(row, b * 128 + l16 * 8, I)) = quant8(h, e);
+      *reinterpret_cast<uint2*>(hq + blocked_offset(row, b * 128 + l16 * 8, I)) =
+          FMT == 2 ? quant8_rcp(h, rh) : quant8(h, e);
       if (MX) {
         if ((l16 & 3) == 0) h_sf[sf_atom_offset(row, 4 * b + (l16 >> 2), 4 * IB)] = (uint8_t)(e + 127);
       } else if (l16 == 0) {
@@ -351,43 +373,51 @@ static int stream_grid(int64_t work, int per_block, int64_t cap = 152 * 16) {
   return (int)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 
-int quant_dispatch_resident(bool mx, int batch) {
+int quant_dispatch_resident(int fmt, int batch) {
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return 0;
-  const void* k = batch == 4 ? (mx ? (const void*)quant_dispatch_kernel<true, 4>
-                                   : (const void*)quant_dispatch_kernel<false, 4>)
-                             : (mx ? (const void*)quant_dispatch_kernel<true, 2>
-                                   : (const void*)quant_dispatch_kernel<false, 2>);
+  const void* k4 = fmt == 2 ? (const void*)quant_dispatch_kernel<2, 4>
+                            : (fmt == 1 ? (const void*)quant_dispatch_kernel<1, 4>
+                                        : (const void*)quant_dispatch_kernel<0, 4>);
+  const void* k2 = fmt == 2 ? (const void*)quant_dispatch_kernel<2, 2>
+                            : (fmt == 1 ? (const void*)quant_dispatch_kernel<1, 2>
+                                        : (const void*)quant_dispatch_kernel<0, 2>);
+  const void* k = batch == 4 ? k4 : k2;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 256, 0) != cudaSuccess) return 0;
   return per_sm * sms;
 }
 
 cudaError_t launch_quant_dispatch(const Workspace& ws, const Layout& L, const uint16_t* x,
                                   int64_t T, cudaStream_t s, bool pdl, int max_ctas,
-                                  int resident2, int resident4) {
+                                  int resident2, int resident4, const float* pt_rx) {
   // one unit = four 128-column blocks of a token, eight warps per block
   const int64_t units = T * ((L.H / 128 + 3) / 4);
   const int g2 = stream_grid(units, 8, max_ctas), g4 = stream_grid(units, 32, max_ctas);
   // four units per warp only where one unit per warp would take more than
   // one wave and four per warp fit in one
   const bool b4 = g2 > resident2 && g4 <= resident4 && g4 < max_ctas;
-  if (b4)
-    return launch_k(L.mx ? quant_dispatch_kernel<true, 4> : quant_dispatch_kernel<false, 4>,
-                    dim3(g4), dim3(256), 0, s, pdl, nullptr, x, (const int32_t*)ws.inv_pad, T, L.H,
-                    L.K, ws.a, ws.a_sf);
-  return launch_k(L.mx ? quant_dispatch_kernel<true, 2> : quant_dispatch_kernel<false, 2>,
-                  dim3(g2), dim3(256), 0, s, pdl, nullptr, x, (const int32_t*)ws.inv_pad, T, L.H,
-                  L.K, ws.a, ws.a_sf);
+  const int fmt = L.pt ? 2 : (L.mx ? 1 : 0);
+  if (b4) {
+    auto k = fmt == 2 ? quant_dispatch_kernel<2, 4>
+                      : (fmt == 1 ? quant_dispatch_kernel<1, 4> : quant_dispatch_kernel<0, 4>);
+    return launch_k(k, dim3(g4), dim3(256), 0, s, pdl, nullptr, x, (const int32_t*)ws.inv_pad, T,
+                    L.H, L.K, pt_rx, ws.a, ws.a_sf);
+  }
+  auto k = fmt == 2 ? quant_dispatch_kernel<2, 2>
+                    : (fmt == 1 ? quant_dispatch_kernel<1, 2> : quant_dispatch_kernel<0, 2>);
+  return launch_k(k, dim3(g2), dim3(256), 0, s, pdl, nullptr, x, (const int32_t*)ws.inv_pad, T,
+                  L.H, L.K, pt_rx, ws.a, ws.a_sf);
 }
 
 cudaError_t launch_swiglu_quant(const Workspace& ws, const Layout& L, int max_ctas,
-                                cudaStream_t s, bool pdl) {
+                                cudaStream_t s, bool pdl, const float* pt_rh) {
   const int64_t warps = (L.rows_alloc) * ((L.I / 128 + 1) / 2);
-  return launch_k(L.mx ? swiglu_quant_kernel<true> : swiglu_quant_kernel<false>,
-                  dim3(stream_grid(warps, 8, max_ctas)), dim3(256), 0, s, pdl, nullptr,
-                  (const uint16_t*)ws.gu, (const int32_t*)ws.total_mtiles, L.I, ws.hq, ws.h_sf);
+  auto k = L.pt ? swiglu_quant_kernel<2> : (L.mx ? swiglu_quant_kernel<1> : swiglu_quant_kernel<0>);
+  return launch_k(k, dim3(stream_grid(warps, 8, max_ctas)), dim3(256), 0, s, pdl, nullptr,
+                  (const uint16_t*)ws.gu, (const int32_t*)ws.total_mtiles, L.I, pt_rh, ws.hq,
+                  ws.h_sf);
 }
 
 cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
@@ -462,6 +492,99 @@ __global__ void sfb_atoms_kernel(const uint8_t* __restrict__ sf, int64_t nblocks
   }
 }
 
+// Per-tensor weight quantisation (the per_tensor scale mode of flashinfer PR
+// #4688): one scale per matrix, s = float(amax / 448) (1 for an all-zero
+// matrix), codes = E4M3_RNE_sat(w * float(1 / s)).  Three passes over the
+// caller's buffers, no scratch: the matrix amax is gathered as float bits in
+// the scale array itself (non-negative floats order like their bits), then
+// turned into the scale in place, then every value is encoded.
+__global__ void pt_amax_kernel(const float* __restrict__ w, int64_t per_mat, int chunks_per_mat,
+                               uint32_t* __restrict__ amax_bits) {
+  const int64_t m = blockIdx.y;
+  const float* src = w + m * per_mat;
+  float amax = 0.f;
+  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < per_mat;
+       i += (int64_t)chunks_per_mat * blockDim.x * 4) {
+    const float4 f = *reinterpret_cast<const float4*>(src + i);
+    amax = fmaxf(fmaxf(amax, fabsf(f.x)), fmaxf(fmaxf(fabsf(f.y), fabsf(f.z)), fabsf(f.w)));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(amax_bits + m, __float_as_uint(amax));
+}
+
+__global__ void pt_scale_kernel(float* __restrict__ scale, int64_t nmat) {
+  for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < nmat;
+       m += (int64_t)gridDim.x * blockDim.x) {
+    const float amax = scale[m];  // written as bits by pt_amax_kernel
+    scale[m] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  }
+}
+
+__global__ void pt_quant_kernel(const float* __restrict__ w, int64_t per_mat,
+                                const float* __restrict__ scale, uint8_t* __restrict__ q) {
+  const int64_t m = blockIdx.y;
+  const float r = __fdiv_rn(1.0f, scale[m]);
+  const float* src = w + m * per_mat;
+  uint8_t* dst = q + m * per_mat;
+  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < per_mat;
+       i += (int64_t)gridDim.x * blockDim.x * 8) {
+    const float4 a = *reinterpret_cast<const float4*>(src + i);
+    const float4 b = *reinterpret_cast<const float4*>(src + i + 4);
+    uint2 o;
+    o.x = e4m3x4(__fmul_rn(a.x, r), __fmul_rn(a.y, r), __fmul_rn(a.z, r), __fmul_rn(a.w, r));
+    o.y = e4m3x4(__fmul_rn(b.x, r), __fmul_rn(b.y, r), __fmul_rn(b.z, r), __fmul_rn(b.w, r));
+    *reinterpret_cast<uint2*>(dst + i) = o;
+  }
+}
+
+cudaError_t launch_quantize_weights_pt(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
+                                       float* scale, cudaStream_t s) {
+  if (nmat == 0) return cudaSuccess;
+  if (nmat > 65535) return cudaErrorInvalidValue;
+  const int64_t per_mat = (int64_t)rows * cols;
+  if (cudaMemsetAsync(scale, 0, sizeof(float) * nmat, s) != cudaSuccess) return cudaGetLastError();
+  const int chunks = (int)((per_mat / 4 + 255) / 256 < 64 ? (per_mat / 4 + 255) / 256 : 64);
+  pt_amax_kernel<<<dim3(chunks, (unsigned)nmat), 256, 0, s>>>(w, per_mat, chunks,
+                                                              reinterpret_cast<uint32_t*>(scale));
+  pt_scale_kernel<<<(unsigned)((nmat + 255) / 256), 256, 0, s>>>(scale, nmat);
+  const int qchunks = (int)((per_mat / 8 + 255) / 256 < 512 ? (per_mat / 8 + 255) / 256 : 512);
+  pt_quant_kernel<<<dim3(qchunks, (unsigned)nmat), 256, 0, s>>>(w, per_mat, scale, q);
+  return cudaGetLastError();
+}
+
+// Per-tensor scales of a bound layer: the weight scales are copied at bind
+// (each must be a positive finite float); the static activation scales come
+// from moe_set_activation_scales, which also precomputes, per expert, the
+// factors the GEMM epilogues apply to their FP32 accumulators (x_scale *
+// s_w1[e] for FC1, h_scale * s_w2[e] for FC2) and the activation scales'
+// float reciprocals the quantisers multiply by.
+__global__ void pt_check_scales_kernel(const float* __restrict__ s, int n, float* __restrict__ dst,
+                                       uint32_t* status) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const float v = s[i];
+    if (!(v > 0.f) || !isfinite(v)) record_status(status, MOE_DEV_BAD_SCALE);
+    dst[i] = v;
+  }
+}
+
+__global__ void pt_set_scales_kernel(float* __restrict__ pt, int E, float x_scale, float h_scale) {
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+    pt[2 * E + e] = __fmul_rn(x_scale, pt[e]);      // FC1 factor
+    pt[3 * E + e] = __fmul_rn(h_scale, pt[E + e]);  // FC2 factor
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    pt[4 * E] = __fdiv_rn(1.0f, x_scale);
+    pt[4 * E + 1] = __fdiv_rn(1.0f, h_scale);
+  }
+}
+
+cudaError_t launch_pt_set_scales(const WeightStore& wst, const Layout& L, float x_scale,
+                                 float h_scale, cudaStream_t s) {
+  pt_set_scales_kernel<<<(L.E + 255) / 256, 256, 0, s>>>(wst.pt, L.E, x_scale, h_scale);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const uint8_t* w1,
                                   const float* w1s, const uint8_t* w2, const float* w2s,
                                   uint32_t* status, cudaStream_t s) {
@@ -469,6 +592,21 @@ cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const
   const int64_t w1_chunks = (int64_t)E * 2 * I * (H / 16), w2_chunks = (int64_t)E * H * (I / 16);
   bind_blocked_kernel<<<stream_grid(w1_chunks, 256), 256, 0, s>>>(w1, wst.w1, E, 2 * I, H, 1);
   bind_blocked_kernel<<<stream_grid(w2_chunks, 256), 256, 0, s>>>(w2, wst.w2, E, H, I, 0);
+  if (L.pt) {
+    // per-tensor: every block scale the tensor core applies is 1 (E8M0 127);
+    // the expert scales go to the epilogue factors
+    const size_t sf1 = (size_t)E * (2 * I / 128) * (H / 128), sf2 = (size_t)E * (H / 128) * (I / 128);
+    const size_t at1 = (size_t)E * (2 * I / 128) * ((H / 128 + 3) / 4) * kSfAtomBytes;
+    const size_t at2 = (size_t)E * (H / 128) * ((I / 128 + 3) / 4) * kSfAtomBytes;
+    if (cudaMemsetAsync(wst.w1_sf, 127, sf1, s) != cudaSuccess ||
+        cudaMemsetAsync(wst.w2_sf, 127, sf2, s) != cudaSuccess ||
+        cudaMemsetAsync(wst.w1_sfatoms, 127, at1, s) != cudaSuccess ||
+        cudaMemsetAsync(wst.w2_sfatoms, 127, at2, s) != cudaSuccess)
+      return cudaGetLastError();
+    pt_check_scales_kernel<<<(E + 255) / 256, 256, 0, s>>>(w1s, E, wst.pt, status);
+    pt_check_scales_kernel<<<(E + 255) / 256, 256, 0, s>>>(w2s, E, wst.pt + E, status);
+    return cudaGetLastError();
+  }
   if (L.mx) {
     const int64_t words1 = (int64_t)E * (2 * I / 128) * (H / 128) * 128;
     const int64_t words2 = (int64_t)E * (H / 128) * (I / 128) * 128;

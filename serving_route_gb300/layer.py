@@ -23,15 +23,17 @@ class MegaMoELayer:
         "pair" (CTA pairs, tcgen05 cta_group::2).  gemms (fused epilogue only):
         "auto" (FC1 -> FC2 in one persistent launch for short forwards, two
         launches for long ones), "one_launch" or "split"; same results.
-        fmt: "deepseek" (1x128 activation / 128x128 weight scales) or
+        fmt: "deepseek" (1x128 activation / 128x128 weight scales),
         "mxfp8" (one scale per 32 elements along K for both; weights from
-        quantize_weights(..., fmt="mxfp8")).
+        quantize_weights(..., fmt="mxfp8")) or "per_tensor" (one scale per
+        expert weight matrix from quantize_weights(..., fmt="per_tensor"),
+        and static activation scales given with set_activation_scales).
         workspace: a uint8 device
         tensor shared with other layers whose forwards never overlap with this
         one's (at least workspace_bytes() of every layer that shares it); by
         default the layer allocates its own."""
         self.H, self.I, self.E, self.K = hidden, inter, num_experts, top_k
-        assert fmt in ("deepseek", "mxfp8")
+        assert fmt in ("deepseek", "mxfp8", "per_tensor")
         self.fmt = fmt
         self.max_rows = max_rows
         self.flags = ((B.MOE_FLAG_FUSE_FC1_EPILOGUE if fuse_fc1 else 0)
@@ -43,7 +45,8 @@ class MegaMoELayer:
                       | (B.MOE_FLAG_WATCHDOG_ROUTE_TEST if watchdog_route_test else 0)
                       | {"auto": 0, "one_launch": B.MOE_FLAG_GEMMS_ONE_LAUNCH,
                          "split": B.MOE_FLAG_SPLIT_GEMMS}[gemms]
-                      | (B.MOE_FLAG_MXFP8 if fmt == "mxfp8" else 0))
+                      | (B.MOE_FLAG_MXFP8 if fmt == "mxfp8" else 0)
+                      | (B.MOE_FLAG_PER_TENSOR if fmt == "per_tensor" else 0))
         em = expected_m if expected_m is not None else max_rows
         ws, wb = B.moe_workspace_query(hidden, inter, num_experts, top_k, self.flags, em, max_rows,
                                        capacity_factor)
@@ -68,6 +71,7 @@ class MegaMoELayer:
         flags = ((B.MOE_FLAG_FUSE_FC1_EPILOGUE if fuse_fc1 else 0)
                  | (B.MOE_FLAG_EMIT_FC1 if emit_fc1 else 0)
                  | (B.MOE_FLAG_MXFP8 if fmt == "mxfp8" else 0)
+                 | (B.MOE_FLAG_PER_TENSOR if fmt == "per_tensor" else 0)
                  | {"auto": 0, "single": B.MOE_FLAG_GEMM_SINGLE_CTA,
                     "pair": B.MOE_FLAG_GEMM_CTA_PAIR}[gemm])
         em = expected_m if expected_m is not None else max_rows
@@ -78,13 +82,18 @@ class MegaMoELayer:
     @staticmethod
     def quantize_weights(w: torch.Tensor, stream=None, fmt: str = "deepseek"):
         """float32 [n, rows, cols] on the GPU -> (E4M3 uint8, float scales
-        [n, rows/128, cols/128]; for fmt="mxfp8" [n, rows, cols/32])."""
+        [n, rows/128, cols/128]; for fmt="mxfp8" [n, rows, cols/32]; for
+        fmt="per_tensor" [n])."""
         assert w.dtype == torch.float32 and w.is_cuda and w.is_contiguous() and w.dim() == 3
         n, r, c = w.shape
         q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
         if fmt == "mxfp8":
             s = torch.empty((n, r, c // 32), dtype=torch.float32, device=w.device)
             B.moe_quantize_weights_mx(w.data_ptr(), n, r, c, q.data_ptr(), s.data_ptr(),
+                                      _stream_ptr(stream))
+        elif fmt == "per_tensor":
+            s = torch.empty((n,), dtype=torch.float32, device=w.device)
+            B.moe_quantize_weights_pt(w.data_ptr(), n, r, c, q.data_ptr(), s.data_ptr(),
                                       _stream_ptr(stream))
         else:
             assert fmt == "deepseek"
@@ -101,11 +110,17 @@ class MegaMoELayer:
         if self.fmt == "mxfp8":
             assert tuple(w1_s.shape) == (self.E, 2 * self.I, self.H // 32)
             assert tuple(w2_s.shape) == (self.E, self.H, self.I // 32)
+        elif self.fmt == "per_tensor":
+            assert tuple(w1_s.shape) == (self.E,) and tuple(w2_s.shape) == (self.E,)
         else:
             assert tuple(w1_s.shape) == (self.E, 2 * self.I // 128, self.H // 128)
             assert tuple(w2_s.shape) == (self.E, self.H // 128, self.I // 128)
         B.moe_bind_weights(self.handle, w1_q.data_ptr(), w1_s.data_ptr(), w2_q.data_ptr(),
                            w2_s.data_ptr(), _stream_ptr(stream))
+
+    def set_activation_scales(self, x_scale: float, h_scale: float, stream=None) -> None:
+        """The static, calibrated activation scales of a per-tensor layer."""
+        B.moe_set_activation_scales(self.handle, x_scale, h_scale, _stream_ptr(stream))
 
     # -- forward ------------------------------------------------------------------
     def stage_output(self, out: torch.Tensor) -> None:

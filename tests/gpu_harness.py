@@ -41,11 +41,12 @@ def device_weights(wl: Workload, layer_cls, chunk_experts: int = 16, stream=None
     E, H, I = wl.E, wl.H, wl.I
     dev = torch.device("cuda")
     mx = fmt == "mxfp8"
+    pt = fmt == "per_tensor"
     w1q = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=dev)
-    w1s = torch.empty((E, 2 * I, H // 32) if mx else (E, 2 * I // 128, H // 128),
+    w1s = torch.empty((E,) if pt else ((E, 2 * I, H // 32) if mx else (E, 2 * I // 128, H // 128)),
                       dtype=torch.float32, device=dev)
     w2q = torch.empty((E, H, I), dtype=torch.uint8, device=dev)
-    w2s = torch.empty((E, H, I // 32) if mx else (E, H // 128, I // 128),
+    w2s = torch.empty((E,) if pt else ((E, H, I // 32) if mx else (E, H // 128, I // 128)),
                       dtype=torch.float32, device=dev)
     sp = (stream or torch.cuda.current_stream()).cuda_stream
     n1, n2 = 2 * I * H, H * I
@@ -70,7 +71,8 @@ def oracle_weights(orc, wl: Workload, experts=None, fmt="deepseek"):
     """Oracle-side weights: host generator + the oracle's quantiser.
     experts=None -> all experts; otherwise arrays hold only the listed experts
     in the order given.  fmt="mxfp8": the oracle's MXFP8 quantiser."""
-    quant = orc.quant_weights_mx if fmt == "mxfp8" else orc.quant_weights
+    quant = {"mxfp8": orc.quant_weights_mx, "per_tensor": orc.quant_weights_pt}.get(
+        fmt, orc.quant_weights)
     w1q, w1s = quant(problem.w1_f32(wl, experts))
     w2q, w2s = quant(problem.w2_f32(wl, experts))
     return w1q, w1s, w2q, w2s

@@ -37,7 +37,7 @@ def test_reference_arm_line():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("fmt", ["deepseek", "mxfp8"])
+@pytest.mark.parametrize("fmt", ["deepseek", "mxfp8", "per_tensor"])
 def test_main_line(fmt):
     d = run_bench("--config", "tiny", "--steps", "5", "--warmup", "3", "--no-cpu-baseline",
                   "--format", fmt, "--records", "v2lite")
@@ -53,6 +53,7 @@ def test_main_line(fmt):
     assert {"median", "p10", "p90"} <= set(d["step_ms"])
     assert d["l2_warm"]["ms_per_step"] > 0 and d["l2_warm"]["steps"] >= 1
     assert d["config"]["format"].startswith("MXFP8" if fmt == "mxfp8" else "E4M3")
+    assert ("per-tensor" in d["config"]["format"]) == (fmt == "per_tensor")
     lr = d["layer_roofline"]
     assert lr["fp8_peak"] == "2 x measured bf16 burst" and 0 < lr["fp8_peak_frac"] < 2
     # the per-workload record: the same timing method on another workload

@@ -8,7 +8,9 @@ Bars (written here, derived from the layer definition):
   * output (BF16): rel-L2 <= 1e-2 and max-abs <= 5e-2 * rms(reference);
   * fused FC1 epilogue vs the unfused path: bit-equal (hq, scales, out).
 Where FP32 accumulation flips a BF16 rounding of gate||up, the re-quantised
-hq may differ by one E4M3 code: the flip count is reported, not gated.
+hq may differ by one E4M3 code: the flip count is reported, not gated; the
+per-route FC2 output y is gated at rel-L2 <= 1e-2 and its max-abs reported
+(a flipped hq code moves one route's y by an hq ulp times a W2 column).
 """
 import numpy as np
 import pytest
@@ -103,9 +105,17 @@ def compare_outputs(dbg, out, ref, rows, check_gu=True):
     if R:
         hq = dbg["hq"][torch.from_numpy(rows).cuda()].cpu().numpy()
         stats["hq_code_flips"] = int(np.sum(hq != ref["hq"]))
-        # y (FC2 output per route, BF16): the output bar, before the weighting
+        # y (FC2 output per route, BF16): the output's rel-L2 bar.  Its
+        # max-abs is reported, not gated: one E4M3 code flip of hq (where the
+        # FP32 accumulation flips a BF16 rounding of gate||up) moves a single
+        # route's y by up to one hq ulp times its W2 column, which the
+        # top-k combine then averages; the max-abs bar is the combined
+        # output's, gated below
         y = gh.bf16_np(dbg["y"][torch.from_numpy(rows).cuda()])
-        stats.update(gate_out(y, gh.bits_to_f64(ref["y"]), "y"))
+        yr = gh.bits_to_f64(ref["y"])
+        stats["y_rel_l2"] = gh.rel_l2(y, yr)
+        stats["y_maxabs"] = float(np.max(np.abs(y - yr)))
+        assert stats["y_rel_l2"] <= OUT_TOL, stats
     o = gh.bf16_np(out)
     r = gh.bits_to_f64(ref["out"])
     stats["out_rel_l2"] = gh.rel_l2(o, r)
