@@ -78,6 +78,8 @@ def parse():
                         "another stream, per SM budget (prints that sweep instead of the bench line)")
     p.add_argument("--sm-budget", type=int, default=0,
                    help="cap the SMs the layer occupies (moe_set_sm_budget; 0: every SM)")
+    p.add_argument("--no-swap", action="store_true",
+                   help="keep the M128 x N256 GEMMs for small forwards (no token-as-N kernels)")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-records", action="store_true",
@@ -647,7 +649,9 @@ def rooflines(wl, counts, kern_ms, ms_step):
 
 def tactic_str(layer, plan):
     t = layer.tactic()
-    return {"gemm": ("cta pairs" if t["gemm_pair"] else "single cta") + f" x{t['gemm_ctas']}",
+    sw = plan.get("swap_ab_tokens", 0)
+    return {"gemm": ("cta pairs" if t["gemm_pair"] else "single cta") + f" x{t['gemm_ctas']}"
+                    + (f", token-as-N (tile {sw})" if sw else ""),
             "routing": "one cooperative kernel" if plan["route_kernels"] == 1 else "three kernels",
             "gemms": ("FC1 + FC2 in one persistent launch" if plan["gemm_launches"] == 1
                       else "two launches")}
@@ -672,7 +676,7 @@ def measure_record(torch, S, g, name, args, dev, stream, flush, weights_cache):
         weights_cache[key] = gpu_weights(torch, g, S.MegaMoELayer, wl, args.format, dev, stream)
     layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, expected_m=wl.T,
                            fuse_fc1=not args.unfused, check_routes=True, gemm=args.gemm,
-                           gemms=args.gemms, fmt=args.format)
+                           gemms=args.gemms, fmt=args.format, swap_ab=not args.no_swap)
     bind(layer, weights_cache[key], args.format, stream)
     x, idx, wts, _, _, counts = device_inputs(torch, g, wl, dev, stream)
     torch.cuda.synchronize()
@@ -733,7 +737,7 @@ def main():
 
     layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, expected_m=wl.T,
                            fuse_fc1=fused, check_routes=True, gemm=args.gemm,
-                           gemms=args.gemms, fmt=args.format)
+                           gemms=args.gemms, fmt=args.format, swap_ab=not args.no_swap)
     # weights: generated and quantised on the GPU, bound once; kept for the
     # per-workload record when workloads there share them (dsv3 prefill/decode)
     weights = gpu_weights(torch, g, S.MegaMoELayer, wl, args.format, dev, stream)

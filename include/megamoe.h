@@ -124,6 +124,16 @@ typedef enum moe_status {
  * x_scale * s_w1[e] (FC1) and h_scale * s_w2[e] (FC2) before the BF16
  * rounding.  Not combinable with MOE_FLAG_MXFP8 (MOE_ERR_INVALID_ARG). */
 #define MOE_FLAG_PER_TENSOR 0x400u
+/* Small forwards on the single-CTA tactic run their GEMMs token-as-N
+ * ("swap-AB"; flashinfer PR #4069, Limitations: no small-M swap-AB variant
+ * of the fused FC1 epilogue yet; PR #4688: swap-AB token tiles chosen per
+ * token bucket): when num_tokens <= 64 (so no expert has more than 64 routed
+ * rows) the weights are the M = 128 operand and the first 16, 32 or 64 rows
+ * of each expert segment the N operand, which leaves room for more weight
+ * stages in flight and double-buffered accumulators.  Same units, same
+ * arithmetic; checked against the oracle.  MOE_FLAG_NO_SWAP_AB keeps the
+ * M128 x N256 kernel for every forward. */
+#define MOE_FLAG_NO_SWAP_AB 0x800u
 
 typedef struct moe_dims {
   int32_t hidden;      /* H: multiple of 128, 128..16384 */
@@ -386,6 +396,7 @@ typedef struct moe_plan {
   int32_t gemm_launches;  /* 1 (FC1 -> FC2 in one persistent launch) or 2 */
   int32_t swiglu_kernels; /* 1 on the unfused path, else 0 */
   int32_t kernels;        /* all of them: + quant_dispatch + combine */
+  int32_t swap_ab_tokens; /* token tile of the token-as-N GEMMs (16, 32, 64), or 0 */
 } moe_plan;
 
 MOE_API moe_status moe_forward_plan(moe_handle* h, int64_t num_tokens, moe_plan* out);

@@ -24,6 +24,7 @@ struct moe_handle {
   Workspace ws;
   WeightStore wst;
   CUtensorMap tm_a, tm_hq;                  // blocked activations: one 128x128 box per load
+  CUtensorMap tm_a_sw[3], tm_hq_sw[3];      // the same with 16 / 32 / 64-row boxes (token-as-N GEMMs)
   CUtensorMap tm_w1, tm_w2;                 // blocked weights: one 128x128 box per load
   CUtensorMap tm_asf, tm_hsf;               // scale atoms as 2-D uint32 tensors (CTA pairs)
   CUtensorMap tm_w1sf, tm_w2sf;             // weight scale atoms, same form (CTA pairs)
@@ -87,12 +88,15 @@ bool encode_bf16_store_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t r
 // Blocked weight store [row blocks][kblocks][128 rows][128 B] as a 3-D byte
 // tensor {128, kblocks * 128, row blocks}; box {128, 128, 1} = one contiguous
 // 16 KB block, 128-byte swizzle.
-bool encode_blocked_map(CUtensorMap* m, const void* base, uint64_t kblocks, uint64_t row_blocks) {
+// box_rows < 128: the first box_rows rows of a block (the token tiles of the
+// token-as-N GEMMs).
+bool encode_blocked_map(CUtensorMap* m, const void* base, uint64_t kblocks, uint64_t row_blocks,
+                        uint32_t box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {128, kblocks * 128, row_blocks};
   cuuint64_t strides[2] = {128, kblocks * 128 * 128};
-  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t box[3] = {128, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -145,8 +149,16 @@ int gemm_grid(const moe_handle* h) {
 // cooperative routing kernel when its blocks can all be resident and no SM
 // budget is set; FC1 -> FC2 as one launch when the fused epilogue is on and
 // the forward is short (or forced).
+// Token tile of the token-as-N GEMMs for a forward of T tokens (0: the
+// M128 x N256 kernel): single-CTA tactic, not switched off, and T <= 64, so
+// that no expert has more routed rows than the tile.
+int swap_tokens(const moe_handle* h, int64_t T) {
+  if (h->L.pair || (h->dims.flags & MOE_FLAG_NO_SWAP_AB) || T <= 0) return 0;
+  return T <= 16 ? 16 : (T <= 32 ? 32 : (T <= 64 ? 64 : 0));
+}
+
 moe_plan forward_plan(const moe_handle* h, int64_t T) {
-  moe_plan p = {0, 0, 0, 0};
+  moe_plan p = {0, 0, 0, 0, 0};
   if (T <= 0) return p;
   const uint32_t f = h->dims.flags;
   const bool fused = (f & MOE_FLAG_FUSE_FC1_EPILOGUE) != 0;
@@ -158,6 +170,7 @@ moe_plan forward_plan(const moe_handle* h, int64_t T) {
   p.gemm_launches = one ? 1 : 2;
   p.swiglu_kernels = fused ? 0 : 1;
   p.kernels = p.route_kernels + 1 + p.gemm_launches + p.swiglu_kernels + 1;
+  p.swap_ab_tokens = swap_tokens(h, T);
   return p;
 }
 
@@ -291,7 +304,8 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
-  if (gemm_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
+  if (gemm_set_attributes() != cudaSuccess || gemm_swap_set_attributes() != cudaSuccess)
+    return MOE_ERR_CUDA;
   moe_handle* h = new (std::nothrow) moe_handle;
   if (!h) return MOE_ERR_INVALID_ARG;
   memset(h, 0, sizeof(*h));
@@ -344,7 +358,13 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
                        (uint64_t)L.E * (2 * L.I / 128) * atoms_along_k(L.H / 128, L.mx)) ||
       !encode_atom_map(&h->tm_w2sf, h->wst.w2_sfatoms,
                        (uint64_t)L.E * (L.H / 128) * atoms_along_k(L.I / 128, L.mx)) ||
-      !encode_bf16_store_map(&h->tm_y, w.y, L.H, L.rows_alloc)) {
+      !encode_bf16_store_map(&h->tm_y, w.y, L.H, L.rows_alloc) ||
+      !encode_blocked_map(&h->tm_a_sw[0], w.a, L.H / 128, (uint64_t)(L.rows_alloc / 128), 16) ||
+      !encode_blocked_map(&h->tm_a_sw[1], w.a, L.H / 128, (uint64_t)(L.rows_alloc / 128), 32) ||
+      !encode_blocked_map(&h->tm_a_sw[2], w.a, L.H / 128, (uint64_t)(L.rows_alloc / 128), 64) ||
+      !encode_blocked_map(&h->tm_hq_sw[0], w.hq, L.I / 128, (uint64_t)(L.rows_alloc / 128), 16) ||
+      !encode_blocked_map(&h->tm_hq_sw[1], w.hq, L.I / 128, (uint64_t)(L.rows_alloc / 128), 32) ||
+      !encode_blocked_map(&h->tm_hq_sw[2], w.hq, L.I / 128, (uint64_t)(L.rows_alloc / 128), 64)) {
     delete h;
     return MOE_ERR_CUDA;
   }
@@ -532,8 +552,16 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   if (ev) record_event(ev[5], s);
   const bool pair = L.pair;
   const int ctas = gemm_grid(h);
-  if (!mega && launch_gemm(m1, pair, &h->tm_a, &h->tm_w1, &h->tm_asf, &h->tm_w1sf, &h->tm_y, g1,
-                           ctas, s, pdl) != cudaSuccess)
+  // token-as-N GEMMs for small forwards: the maps whose box is the token tile
+  const int swap = plan.swap_ab_tokens;
+  const int si = swap == 16 ? 0 : (swap == 32 ? 1 : 2);
+  if (!mega && swap &&
+      launch_gemm_swap(m1, swap, &h->tm_a_sw[si], &h->tm_w1, &h->tm_a_sw[si], &h->tm_w1, g1, g1, ctas,
+                       s, pdl) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!mega && !swap &&
+      launch_gemm(m1, pair, &h->tm_a, &h->tm_w1, &h->tm_asf, &h->tm_w1sf, &h->tm_y, g1, ctas, s,
+                  pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[6], s);
   if (!fused && launch_swiglu_quant(ws, L, stream_ctas, s, pdl, pt_rh) != cudaSuccess)
@@ -567,12 +595,19 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
     g2.fc1_ntiles = g1.NT;
     g1.fc1_done = ws.fc1_done;
     g1.fc1_ntiles = g1.NT;
-    if (launch_gemm_mega(pair, &h->tm_a, &h->tm_w1, &h->tm_asf, &h->tm_w1sf, &h->tm_hq, &h->tm_w2,
-                         &h->tm_hsf, &h->tm_w2sf, &h->tm_y, g1, g2, ctas, s, pdl) != cudaSuccess)
-      return MOE_ERR_CUDA;
-  } else if (launch_gemm(kModeY, pair, &h->tm_hq, &h->tm_w2, &h->tm_hsf, &h->tm_w2sf, &h->tm_y, g2,
-                         ctas, s, pdl) != cudaSuccess) {
-    return MOE_ERR_CUDA;
+    const cudaError_t e =
+        swap ? launch_gemm_swap(kModeMega, swap, &h->tm_a_sw[si], &h->tm_w1, &h->tm_hq_sw[si],
+                                &h->tm_w2, g1, g2, ctas, s, pdl)
+             : launch_gemm_mega(pair, &h->tm_a, &h->tm_w1, &h->tm_asf, &h->tm_w1sf, &h->tm_hq,
+                                &h->tm_w2, &h->tm_hsf, &h->tm_w2sf, &h->tm_y, g1, g2, ctas, s, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    const cudaError_t e =
+        swap ? launch_gemm_swap(kModeY, swap, &h->tm_hq_sw[si], &h->tm_w2, &h->tm_hq_sw[si],
+                                &h->tm_w2, g2, g2, ctas, s, pdl)
+             : launch_gemm(kModeY, pair, &h->tm_hq, &h->tm_w2, &h->tm_hsf, &h->tm_w2sf, &h->tm_y, g2,
+                           ctas, s, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (ev) record_event(ev[8], s);
   if (launch_combine(ws, L, d_topk_w, h->out, num_tokens, s, pdl, stream_ctas) != cudaSuccess)

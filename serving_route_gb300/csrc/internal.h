@@ -182,6 +182,16 @@ cudaError_t launch_gemm_mega(bool pair, const CUtensorMap* tmA, const CUtensorMa
                              const CUtensorMap* tmY, const GemmArgs& g, const GemmArgs& g2, int ctas,
                              cudaStream_t s, bool pdl);
 
+// gemm_swap.cu: the token-as-N form of the same units for forwards that
+// route at most ntok (16, 32 or 64) rows to any expert.  tmX / tmX2: the
+// activation buffers (A, hq) as blocked maps whose box is ntok rows high;
+// tmW / tmW2: the weight maps of launch_gemm.  Scale atoms by bulk copy from
+// g.sfa / g.sfb.  kModeMega takes both phases (g2.fc1_done set).
+cudaError_t gemm_swap_set_attributes();
+cudaError_t launch_gemm_swap(GemmMode mode, int ntok, const CUtensorMap* tmX, const CUtensorMap* tmW,
+                             const CUtensorMap* tmX2, const CUtensorMap* tmW2, const GemmArgs& g,
+                             const GemmArgs& g2, int ctas, cudaStream_t s, bool pdl);
+
 // combine.cu
 cudaError_t launch_combine(const Workspace& ws, const Layout& L, const float* topk_w,
                            uint16_t* out, int64_t T, cudaStream_t s, bool pdl, int max_ctas);

@@ -20,7 +20,7 @@ from tests.test_gpu_parity import compare_outputs, small_problem
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("gemm", ["single", "pair"])
+@pytest.mark.parametrize("gemm", ["single", "pair", "swap"])
 @pytest.mark.parametrize("split", [False, True])
 def test_watchdog_expires_with_status_and_context_survives(orc, split, gemm):
     """split=False: the one-launch FC1 -> FC2 kernel, where the FC2 tiles of
@@ -28,13 +28,16 @@ def test_watchdog_expires_with_status_and_context_survives(orc, split, gemm):
     pair 0) never publishes, and expire on their own bound.  gemm="pair": the
     leader's MMA wait expires; the peer's waits on the leader's commits expire
     too, and both CTAs meet at the cluster barrier before freeing the pair's
-    tensor memory."""
+    tensor memory.  gemm="swap": a 40-token forward on single CTAs, which runs
+    the token-as-N kernels (double-buffered accumulators, counter schedule)."""
     import __graft_entry__ as ge
     ge.build()
     import serving_route_gb300 as S
     import serving_route_gb300.binding as B
 
-    T, H, I, E, K = 300, 512, 256, 8, 2
+    T, H, I, E, K = (40 if gemm == "swap" else 300), 512, 256, 8, 2
+    swap = gemm == "swap"
+    gemm = "single" if swap else gemm
     x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=31)
     q1, s1 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w1).cuda())
     q2, s2 = S.MegaMoELayer.quantize_weights(torch.from_numpy(w2).cuda())
@@ -42,6 +45,7 @@ def test_watchdog_expires_with_status_and_context_survives(orc, split, gemm):
 
     bad = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm=gemm, watchdog_test=True,
                          gemms="split" if split else "one_launch")
+    assert (bad.plan(T)["swap_ab_tokens"] > 0) == swap
     bad.bind_weights(q1, s1, q2, s2)
     bad.forward(xt, it, wt)
     st, bits = bad.read_status()
