@@ -134,6 +134,18 @@ typedef enum moe_status {
  * arithmetic; checked against the oracle.  MOE_FLAG_NO_SWAP_AB keeps the
  * M128 x N256 kernel for every forward. */
 #define MOE_FLAG_NO_SWAP_AB 0x800u
+/* Opt-in: the token-as-N FC2 folds the combine in (flashinfer PR #4069,
+ * Description: the grouped combine after FC2).  Every warp counts, per token
+ * and 256-column n-tile, the y chunks it has stored, and the warp whose count
+ * completes a token's routes combines that token's columns right away -- the
+ * combine kernel's arithmetic (a float fma chain over the active routes in
+ * ascending k from +0, one BF16 rounding), so the output is bit-identical --
+ * and no combine kernel runs.  Off by default: it was measured 0.5-0.9%
+ * slower at decode T = 8 and 64 (the tokens completed by the last units are
+ * combined by the few warps that finish last, where the combine kernel
+ * spreads them over every SM).  Has no effect on forwards that do not run
+ * the token-as-N GEMMs. */
+#define MOE_FLAG_COMBINE_IN_FC2 0x1000u
 
 typedef struct moe_dims {
   int32_t hidden;      /* H: multiple of 128, 128..16384 */
@@ -395,8 +407,9 @@ typedef struct moe_plan {
   int32_t route_kernels;  /* 1 (one cooperative kernel) or 3 */
   int32_t gemm_launches;  /* 1 (FC1 -> FC2 in one persistent launch) or 2 */
   int32_t swiglu_kernels; /* 1 on the unfused path, else 0 */
-  int32_t kernels;        /* all of them: + quant_dispatch + combine */
+  int32_t kernels;        /* all of them: + quant_dispatch (+ combine unless folded) */
   int32_t swap_ab_tokens; /* token tile of the token-as-N GEMMs (16, 32, 64), or 0 */
+  int32_t combine_in_fc2; /* 1: the combine is folded into FC2 (MOE_FLAG_COMBINE_IN_FC2; no combine kernel) */
 } moe_plan;
 
 MOE_API moe_status moe_forward_plan(moe_handle* h, int64_t num_tokens, moe_plan* out);

@@ -44,6 +44,7 @@ MOE_FLAG_MXFP8 = 0x100
 MOE_FLAG_WATCHDOG_ROUTE_TEST = 0x200
 MOE_FLAG_PER_TENSOR = 0x400
 MOE_FLAG_NO_SWAP_AB = 0x800
+MOE_FLAG_COMBINE_IN_FC2 = 0x1000
 
 # every function the header declares (checked against include/megamoe.h by a test)
 API_NAMES = ("moe_workspace_query", "moe_create", "moe_quantize_weights", "moe_quantize_weights_mx",
@@ -73,7 +74,7 @@ class moe_debug_view(ctypes.Structure):
 class moe_plan(ctypes.Structure):
     _fields_ = [("route_kernels", ctypes.c_int32), ("gemm_launches", ctypes.c_int32),
                 ("swiglu_kernels", ctypes.c_int32), ("kernels", ctypes.c_int32),
-                ("swap_ab_tokens", ctypes.c_int32)]
+                ("swap_ab_tokens", ctypes.c_int32), ("combine_in_fc2", ctypes.c_int32)]
 
 
 class MoEError(RuntimeError):

@@ -158,7 +158,7 @@ int swap_tokens(const moe_handle* h, int64_t T) {
 }
 
 moe_plan forward_plan(const moe_handle* h, int64_t T) {
-  moe_plan p = {0, 0, 0, 0, 0};
+  moe_plan p = {0, 0, 0, 0, 0, 0};
   if (T <= 0) return p;
   const uint32_t f = h->dims.flags;
   const bool fused = (f & MOE_FLAG_FUSE_FC1_EPILOGUE) != 0;
@@ -169,8 +169,10 @@ moe_plan forward_plan(const moe_handle* h, int64_t T) {
                    ((f & MOE_FLAG_GEMMS_ONE_LAUNCH) || gemm_rounds_estimate(h, gemm_grid(h), T) <= 48.0);
   p.gemm_launches = one ? 1 : 2;
   p.swiglu_kernels = fused ? 0 : 1;
-  p.kernels = p.route_kernels + 1 + p.gemm_launches + p.swiglu_kernels + 1;
   p.swap_ab_tokens = swap_tokens(h, T);
+  // the token-as-N FC2 folds the combine in when asked to
+  p.combine_in_fc2 = (p.swap_ab_tokens && (f & MOE_FLAG_COMBINE_IN_FC2)) ? 1 : 0;
+  p.kernels = p.route_kernels + 1 + p.gemm_launches + p.swiglu_kernels + (p.combine_in_fc2 ? 0 : 1);
   return p;
 }
 
@@ -239,8 +241,12 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
   // status word at +0, total_mtiles at +4, routing arrival counter at +8;
   // the megakernel's per-m-tile counters follow at +1024, so one memset
   // clears both
-  L->o_status = take(1024 + 4 * MB);
+  // the token-as-N FC2's combine counters ([64 tokens][ceil(H/256)]) follow
+  // the per-m-tile counters, under the same memset
+  const size_t cmb_bytes = 4 * 64 * (size_t)((H + 255) / 256);
+  L->o_status = take(1024 + 4 * MB + cmb_bytes);
   L->o_fc1_done = L->o_status + 1024;
+  L->o_cmb = L->o_fc1_done + 4 * MB;
   L->o_counts = take(4 * E);
   L->o_offsets = take(4 * (E + 1));
   L->o_pad_offsets = take(4 * (E + 1));
@@ -325,6 +331,7 @@ moe_status moe_create(const moe_dims* dims, int64_t expected_m, int64_t max_rows
   w.grid_sync = reinterpret_cast<uint32_t*>(b + L.o_status + 8);
   w.gemm_sched = reinterpret_cast<int32_t*>(b + L.o_status + 12);
   w.fc1_done = reinterpret_cast<int32_t*>(b + L.o_fc1_done);
+  w.cmb_cnt = reinterpret_cast<int32_t*>(b + L.o_cmb);
   w.counts = reinterpret_cast<int32_t*>(b + L.o_counts);
   w.offsets = reinterpret_cast<int32_t*>(b + L.o_offsets);
   w.pad_offsets = reinterpret_cast<int32_t*>(b + L.o_pad_offsets);
@@ -488,7 +495,11 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   // status word, total_mtiles, the routing kernel's arrival counter, the
   // GEMM launches' unit counters and (for the megakernel) the per-m-tile FC1
   // counters
-  cudaMemsetAsync(ws.status, 0, mega ? 1024 + 4 * (size_t)(L.rows_alloc / 128) : 20, s);
+  // (and the token-as-N FC2's combine counters of this forward's tokens)
+  const bool fold = plan.combine_in_fc2 != 0;
+  const size_t reset = fold ? L.o_cmb - L.o_status + 4 * (size_t)num_tokens * ((L.H + 255) / 256)
+                            : (mega ? 1024 + 4 * (size_t)(L.rows_alloc / 128) : 20);
+  cudaMemsetAsync(ws.status, 0, reset, s);
   // Under an SM budget the routing keeps to its three small kernels: a
   // cooperative grid would have to be resident beside the side-stream work.
   const int coop = plan.route_kernels == 1 ? h->route_coop_blocks : 0;
@@ -588,6 +599,16 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   g2.wait_limit_ns = g1.wait_limit_ns;
   g2.sched = dyn_sched ? ws.gemm_sched + 1 : nullptr;
   g2.pt_scale = L.pt ? h->wst.pt + 3 * L.E : nullptr;
+  if (fold) {
+    g2.cmb_cnt = ws.cmb_cnt;
+    g2.cmb_out = h->out;
+    g2.cmb_w = d_topk_w;
+    g2.cmb_inv = ws.inv_pad;
+    g2.cmb_perm = ws.perm;
+    g2.cmb_offsets = ws.offsets;
+    g2.cmb_T = (int)num_tokens;
+    g2.cmb_K = L.K;
+  }
   if (ev) record_event(ev[7], s);
   if (mega) {
     // the FC1 epilogue publishes, per m-tile, how many of its NT tiles are stored
@@ -610,7 +631,7 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (ev) record_event(ev[8], s);
-  if (launch_combine(ws, L, d_topk_w, h->out, num_tokens, s, pdl, stream_ctas) != cudaSuccess)
+  if (!fold && launch_combine(ws, L, d_topk_w, h->out, num_tokens, s, pdl, stream_ctas) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[9], s);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

@@ -94,6 +94,49 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __device__ __forceinline__ uint8_t e4m3x1(float v) { return (uint8_t)(e4m3x2(v, 0.f) & 0xFFu); }
 
+// The combine of one token's 256 output columns [c0, c0 + 256) by one warp
+// (8 columns per lane): out[t, c] = bf16_rn(fma chain over the active k =
+// 0..K-1, ascending, of w[t, k] * y[inv_pad[t*K + k], c]) from +0 -- the
+// combine kernel's arithmetic, so the output is bit-identical.  The K route
+// rows are loaded together, from L2 (other warps and CTAs stored them).
+__device__ __forceinline__ void combine_token(const GemmArgs& gy, const uint16_t* y, int64_t ld,
+                                              int64_t t, int c0, int N, int lane) {
+  const int c = c0 + lane * 8;
+  if (c >= N) return;
+  const int K = gy.cmb_K;
+  int p[8];
+  float wk[8];
+  uint4 v[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    p[k] = k < K ? __ldg(gy.cmb_inv + t * K + k) : -1;
+    wk[k] = k < K ? __ldg(gy.cmb_w + t * K + k) : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    v[k] = p[k] >= 0 ? __ldcg(reinterpret_cast<const uint4*>(y + (int64_t)p[k] * ld + c))
+                     : make_uint4(0u, 0u, 0u, 0u);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (p[k] < 0) continue;
+    const uint32_t vv[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(wk[k], bf16_bits_to_float(vv[i] & 0xFFFFu), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wk[k], bf16_bits_to_float(vv[i] >> 16), acc[2 * i + 1]);
+    }
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  *reinterpret_cast<uint4*>(gy.cmb_out + t * N + c) = o;
+}
+
 // Bounded wait until *count >= target (acquire), then a proxy fence for the
 // TMA loads that follow (as in the M128 x N256 kernel).
 __device__ __noinline__ bool swap_wait_count_geq(const int32_t* count, int target,
@@ -417,6 +460,29 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       }
       return __shfl_sync(0xFFFFFFFFu, v, 0);
     };
+    // With the combine folded into FC2, a token whose routes are all masked
+    // completes no count: one warp writes its output row, +0 (as the combine
+    // kernel does), before any unit (the routing is complete here).
+    const GemmArgs& gc = kMega ? g2 : g;
+    if (gc.cmb_cnt && blockIdx.x == 0 && warp == 2) {
+      const int N = gc.N;
+      for (int t0 = 0; t0 < gc.cmb_T; t0 += 32) {
+        const int t = t0 + lane;
+        bool dead = false;
+        if (t < gc.cmb_T) {
+          int nact = 0;
+          for (int k = 0; k < gc.cmb_K; ++k) nact += __ldg(gc.cmb_inv + (int64_t)t * gc.cmb_K + k) >= 0;
+          dead = nact == 0;
+        }
+        uint32_t m = __ballot_sync(0xFFFFFFFFu, dead);
+        while (m) {
+          const int src = __ffs(m) - 1;
+          m &= m - 1;
+          for (int c = lane * 8; c < N; c += 256)
+            *reinterpret_cast<uint4*>(gc.cmb_out + (int64_t)(t0 + src) * N + c) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
     int i = 0;
     for (int u = dyn ? take() : unit0; u < total; u = dyn ? take() : u + ustride, ++i) {
       const int b = i & 1;
@@ -461,6 +527,36 @@ __global__ void __launch_bounds__(kSwThreads, 1)
           uint16_t* dst = out + (row0 + c) * ld + (int64_t)nt * 256 + irow;
           dst[0] = (uint16_t)(pack_bf16x2(a0[c], 0.f) & 0xFFFFu);
           if (second) dst[128] = (uint16_t)(pack_bf16x2(a1[c], 0.f) & 0xFFFFu);
+        }
+        const GemmArgs& gy = (kMega && ph) ? g2 : g;
+        if (gy.cmb_cnt) {
+          // The combine, folded in.  Each token's 256 columns of this unit
+          // are stored by the four lane-quadrant warps of its token half;
+          // every warp counts each of its live tokens once its y stores are
+          // visible (each lane's fence, then the warp's sync), into the
+          // token's count for this n-tile.  The warp whose add completes a
+          // token's count (4 x its active routes) combines that token's
+          // columns of the n-tile.
+          __threadfence();
+          __syncwarp();
+          int64_t tok = -1;
+          bool complete = false;
+          if (lane < NT2 && col0 + lane < live) {
+            const int64_t pos = row0 + lane - g.pad_offsets[e_t] + gy.cmb_offsets[e_t];
+            tok = gy.cmb_perm[pos] / gy.cmb_K;
+            int nact = 0;
+            for (int k = 0; k < gy.cmb_K; ++k) nact += __ldg(gy.cmb_inv + tok * gy.cmb_K + k) >= 0;
+            const int old = atomicAdd(gy.cmb_cnt + tok * gy.NT + nt, 1);
+            complete = old == 4 * nact - 1;
+          }
+          uint32_t todo = __ballot_sync(0xFFFFFFFFu, complete);
+          if (todo) __threadfence();
+          while (todo) {
+            const int src = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int64_t t = __shfl_sync(0xFFFFFFFFu, tok, src);
+            combine_token(gy, out, ld, t, nt * 256, N, lane);
+          }
         }
       }
       if (em_gu) {

@@ -19,11 +19,12 @@ class MegaMoELayer:
                  gemm: str = "auto", watchdog_test: bool = False, device="cuda",
                  workspace: torch.Tensor | None = None, gemms: str = "auto",
                  fmt: str = "deepseek", watchdog_route_test: bool = False,
-                 swap_ab: bool = True):
+                 swap_ab: bool = True, combine_in_fc2: bool = False):
         """gemm: "auto" (tactic from expected_m), "single" (one CTA per SM) or
         "pair" (CTA pairs, tcgen05 cta_group::2).  swap_ab: forwards of at
         most 64 tokens on single CTAs run the token-as-N GEMMs (False keeps
-        the M128 x N256 kernel).  gemms (fused epilogue only):
+        the M128 x N256 kernel); combine_in_fc2: their FC2 folds the combine
+        in (no combine kernel; bit-identical output).  gemms (fused epilogue only):
         "auto" (FC1 -> FC2 in one persistent launch for short forwards, two
         launches for long ones), "one_launch" or "split"; same results.
         fmt: "deepseek" (1x128 activation / 128x128 weight scales),
@@ -50,7 +51,8 @@ class MegaMoELayer:
                          "split": B.MOE_FLAG_SPLIT_GEMMS}[gemms]
                       | (B.MOE_FLAG_MXFP8 if fmt == "mxfp8" else 0)
                       | (B.MOE_FLAG_PER_TENSOR if fmt == "per_tensor" else 0)
-                      | (0 if swap_ab else B.MOE_FLAG_NO_SWAP_AB))
+                      | (0 if swap_ab else B.MOE_FLAG_NO_SWAP_AB)
+                      | (B.MOE_FLAG_COMBINE_IN_FC2 if combine_in_fc2 else 0))
         em = expected_m if expected_m is not None else max_rows
         ws, wb = B.moe_workspace_query(hidden, inter, num_experts, top_k, self.flags, em, max_rows,
                                        capacity_factor)
@@ -174,7 +176,7 @@ class MegaMoELayer:
         p = B.moe_forward_plan(self.handle, num_tokens)
         return dict(route_kernels=p.route_kernels, gemm_launches=p.gemm_launches,
                     swiglu_kernels=p.swiglu_kernels, kernels=p.kernels,
-                    swap_ab_tokens=p.swap_ab_tokens)
+                    swap_ab_tokens=p.swap_ab_tokens, combine_in_fc2=p.combine_in_fc2)
 
     def route_kernels(self, num_tokens: int) -> int:
         """Kernels the routing step launches for a forward of num_tokens tokens (1 or 3)."""

@@ -600,7 +600,7 @@ def test_forward_plan(lib):
     dv2 = (2048, 1408, 64, 6)
     short = S.MegaMoELayer(*dv2, max_rows=4096, fuse_fc1=True)
     assert short.plan(4096) == dict(route_kernels=1, gemm_launches=1, swiglu_kernels=0, kernels=4,
-                                    swap_ab_tokens=0)
+                                    swap_ab_tokens=0, combine_in_fc2=0)
     assert short.plan(0)["kernels"] == 0
     dv3 = (7168, 2048, 256, 8)
     long_ = S.MegaMoELayer(*dv3, max_rows=1024, fuse_fc1=True, gemm="single")
@@ -612,7 +612,7 @@ def test_forward_plan(lib):
     assert split.plan(4096)["gemm_launches"] == 2
     unfused = S.MegaMoELayer(*dv2, max_rows=4096, fuse_fc1=False)
     assert unfused.plan(4096) == dict(route_kernels=1, gemm_launches=2, swiglu_kernels=1, kernels=6,
-                                      swap_ab_tokens=0)
+                                      swap_ab_tokens=0, combine_in_fc2=0)
     short.set_sm_budget(64)
     assert short.plan(4096)["route_kernels"] == 3
 

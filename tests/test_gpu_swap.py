@@ -7,8 +7,9 @@ expert segment as the N operand (the small-M swap-AB variant flashinfer PR
 bucket).  Bars as in test_gpu_parity: bit-exact routing and activation
 bytes; gate||up rel-L2 <= 1e-3 against the oracle; output rel-L2 <= 1e-2 and
 max-abs <= 5e-2 * rms; the fused epilogue bit-equal to the unfused path and
-one launch bit-equal to two, within the token-as-N kernels; the plan reports
-the tile; NaN-poisoned padding rows change nothing.
+one launch bit-equal to two, within the token-as-N kernels; the combine
+folded into the token-as-N FC2 (opt-in) bit-equal to the combine kernel; the
+plan reports the tile and the fold; NaN-poisoned padding rows change nothing.
 """
 import numpy as np
 import pytest
@@ -163,3 +164,38 @@ def test_swap_poisoned_padding_rows_change_nothing(lib, orc, fuse):
     second = layer.forward(xt, it, wt)
     assert layer.read_status() == (0, 0)
     assert torch.equal(first.view(torch.int16), second.view(torch.int16))
+
+
+@pytest.mark.parametrize("T,H,I,E,K,mask,fmt,gemms", [
+    (1, 256, 128, 4, 1, 0.0, "deepseek", "auto"),         # one token
+    (8, 512, 256, 64, 8, 0.0, "deepseek", "one_launch"),  # decode-like, FC1 -> FC2 in one launch
+    (20, 384, 256, 6, 2, 0.3, "deepseek", "split"),       # masked slots (some all-masked tokens); H % 256 == 128
+    (40, 768, 256, 16, 6, 0.1, "mxfp8", "auto"),
+    (64, 512, 384, 8, 8, 0.05, "per_tensor", "auto"),     # tile 64, every expert's rows up to the tile
+])
+def test_swap_folded_combine_bit_equal_combine_kernel(lib, orc, T, H, I, E, K, mask, fmt, gemms):
+    """The token-as-N FC2 with the combine folded in (per token and n-tile
+    completion counts; the completing warp combines) against the same
+    forward with the separate combine kernel: the output bit for bit, and
+    against the oracle."""
+    x, idx, w, w1, w2 = small_problem(orc, T, H, I, E, K, seed=130 + T, mask=mask)
+    if mask:
+        idx[T // 2] = -1                 # a token with no route: +0 either way
+    xt, it, wt = gh.to_device(x, idx, w)
+    outs = []
+    for fold in (True, False):
+        layer, wo = make(lib, orc, T, H, I, E, K, w1, w2, fmt=fmt, fuse_fc1=True, gemms=gemms,
+                         combine_in_fc2=fold)
+        p = layer.plan(T)
+        assert p["swap_ab_tokens"] > 0 and p["combine_in_fc2"] == (1 if fold else 0)
+        assert p["kernels"] == p["route_kernels"] + 1 + p["gemm_launches"] + (0 if fold else 1)
+        for _ in range(2):               # twice: the counters restart from zero
+            out = layer.forward(xt, it, wt).clone()
+            assert layer.read_status() == (0, 0)
+        outs.append(out.view(torch.int16))
+        del layer
+    assert torch.equal(outs[0], outs[1])
+    ref = oracle(orc, fmt, x, idx, w, wo)
+    gate_out(gh.bf16_np(outs[0].view(torch.bfloat16)), gh.bits_to_f64(ref["out"]))
+    if mask:
+        assert not torch.any(outs[0][T // 2])
