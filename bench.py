@@ -78,6 +78,8 @@ def parse():
                         "another stream, per SM budget (prints that sweep instead of the bench line)")
     p.add_argument("--sm-budget", type=int, default=0,
                    help="cap the SMs the layer occupies (moe_set_sm_budget; 0: every SM)")
+    p.add_argument("--combine-in-fc2", action="store_true",
+                   help="fold the combine into FC2 (single-CTA forwards; no combine kernel)")
     p.add_argument("--no-swap", action="store_true",
                    help="keep the M128 x N256 GEMMs for small forwards (no token-as-N kernels)")
     p.add_argument("--no-graph", action="store_true")
@@ -654,7 +656,8 @@ def tactic_str(layer, plan):
                     + (f", token-as-N (tile {sw})" if sw else ""),
             "routing": "one cooperative kernel" if plan["route_kernels"] == 1 else "three kernels",
             "gemms": ("FC1 + FC2 in one persistent launch" if plan["gemm_launches"] == 1
-                      else "two launches")}
+                      else "two launches")
+                     + (", combine folded into FC2" if plan.get("combine_in_fc2") else "")}
 
 
 def l2_note(wl, b_alg):
@@ -676,7 +679,8 @@ def measure_record(torch, S, g, name, args, dev, stream, flush, weights_cache):
         weights_cache[key] = gpu_weights(torch, g, S.MegaMoELayer, wl, args.format, dev, stream)
     layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, expected_m=wl.T,
                            fuse_fc1=not args.unfused, check_routes=True, gemm=args.gemm,
-                           gemms=args.gemms, fmt=args.format, swap_ab=not args.no_swap)
+                           gemms=args.gemms, fmt=args.format, swap_ab=not args.no_swap,
+                           combine_in_fc2=args.combine_in_fc2)
     bind(layer, weights_cache[key], args.format, stream)
     x, idx, wts, _, _, counts = device_inputs(torch, g, wl, dev, stream)
     torch.cuda.synchronize()
@@ -737,7 +741,8 @@ def main():
 
     layer = S.MegaMoELayer(wl.H, wl.I, wl.E, wl.K, max_rows=wl.T, expected_m=wl.T,
                            fuse_fc1=fused, check_routes=True, gemm=args.gemm,
-                           gemms=args.gemms, fmt=args.format, swap_ab=not args.no_swap)
+                           gemms=args.gemms, fmt=args.format, swap_ab=not args.no_swap,
+                           combine_in_fc2=args.combine_in_fc2)
     # weights: generated and quantised on the GPU, bound once; kept for the
     # per-workload record when workloads there share them (dsv3 prefill/decode)
     weights = gpu_weights(torch, g, S.MegaMoELayer, wl, args.format, dev, stream)

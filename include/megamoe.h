@@ -134,17 +134,21 @@ typedef enum moe_status {
  * arithmetic; checked against the oracle.  MOE_FLAG_NO_SWAP_AB keeps the
  * M128 x N256 kernel for every forward. */
 #define MOE_FLAG_NO_SWAP_AB 0x800u
-/* Opt-in: the token-as-N FC2 folds the combine in (flashinfer PR #4069,
- * Description: the grouped combine after FC2).  Every warp counts, per token
- * and 256-column n-tile, the y chunks it has stored, and the warp whose count
- * completes a token's routes combines that token's columns right away -- the
- * combine kernel's arithmetic (a float fma chain over the active routes in
- * ascending k from +0, one BF16 rounding), so the output is bit-identical --
- * and no combine kernel runs.  Off by default: it was measured 0.5-0.9%
- * slower at decode T = 8 and 64 (the tokens completed by the last units are
- * combined by the few warps that finish last, where the combine kernel
- * spreads them over every SM).  Has no effect on forwards that do not run
- * the token-as-N GEMMs. */
+/* Opt-in: FC2 folds the combine in (flashinfer PR #4069, Description: the
+ * grouped combine after FC2).  Per token and 256-column n-tile, the y chunks
+ * stored so far are counted, and the warp whose count completes a token's
+ * routes combines that token's columns right away -- the combine kernel's
+ * arithmetic (a float fma chain over the active routes in ascending k from
+ * +0, one BF16 rounding), so the output is bit-identical -- and no combine
+ * kernel runs.  In the token-as-N FC2 the epilogue warps count and combine;
+ * in the M128 x N256 FC2 (and the one-launch FC1 -> FC2) the epilogue warps
+ * count and queue the completed (token, n-tile) pairs in shared memory for
+ * two warps of their own, which combine them.  Single-CTA forwards only: ignored under CTA pairs.  Off by
+ * default: it was measured slower everywhere -- 0.5-0.9% at decode T = 8 and
+ * 64, 0.2% at T = 256 and 1024, 10% at the dsv2lite shape -- because each
+ * completed token needs dependent L2 round trips that the combine kernel
+ * overlaps across every SM, and many tokens complete only in FC2's last
+ * wave. */
 #define MOE_FLAG_COMBINE_IN_FC2 0x1000u
 
 typedef struct moe_dims {

@@ -170,8 +170,9 @@ moe_plan forward_plan(const moe_handle* h, int64_t T) {
   p.gemm_launches = one ? 1 : 2;
   p.swiglu_kernels = fused ? 0 : 1;
   p.swap_ab_tokens = swap_tokens(h, T);
-  // the token-as-N FC2 folds the combine in when asked to
-  p.combine_in_fc2 = (p.swap_ab_tokens && (f & MOE_FLAG_COMBINE_IN_FC2)) ? 1 : 0;
+  // single-CTA FC2 launches (token-as-N or M128 x N256) fold the combine in
+  // when asked to; CTA pairs keep the combine kernel
+  p.combine_in_fc2 = (!h->L.pair && (f & MOE_FLAG_COMBINE_IN_FC2)) ? 1 : 0;
   p.kernels = p.route_kernels + 1 + p.gemm_launches + p.swiglu_kernels + (p.combine_in_fc2 ? 0 : 1);
   return p;
 }
@@ -241,9 +242,9 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
   // status word at +0, total_mtiles at +4, routing arrival counter at +8;
   // the megakernel's per-m-tile counters follow at +1024, so one memset
   // clears both
-  // the token-as-N FC2's combine counters ([64 tokens][ceil(H/256)]) follow
+  // the folded combine's counters ([max_rows tokens][ceil(H/256)]) follow
   // the per-m-tile counters, under the same memset
-  const size_t cmb_bytes = 4 * 64 * (size_t)((H + 255) / 256);
+  const size_t cmb_bytes = 4 * (size_t)max_rows * ((H + 255) / 256);
   L->o_status = take(1024 + 4 * MB + cmb_bytes);
   L->o_fc1_done = L->o_status + 1024;
   L->o_cmb = L->o_fc1_done + 4 * MB;
@@ -495,7 +496,7 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   // status word, total_mtiles, the routing kernel's arrival counter, the
   // GEMM launches' unit counters and (for the megakernel) the per-m-tile FC1
   // counters
-  // (and the token-as-N FC2's combine counters of this forward's tokens)
+  // (and, with the combine folded into FC2, the counters of this forward's tokens)
   const bool fold = plan.combine_in_fc2 != 0;
   const size_t reset = fold ? L.o_cmb - L.o_status + 4 * (size_t)num_tokens * ((L.H + 255) / 256)
                             : (mega ? 1024 + 4 * (size_t)(L.rows_alloc / 128) : 20);

@@ -48,6 +48,10 @@
 //    stores); an FC2 tile's producer waits for its m-tile's count before its
 //    first TMA load of hq.  Every CTA takes its FC1 units before its FC2
 //    units, so the waits always end (see the kernel's comment).
+//  * Combine folded into FC2 (opt-in, single CTA): the FC2 epilogue counts
+//    each stored row into its token's per-n-tile count and queues the pairs
+//    it completes for two extra warps, which combine them (bit-identical to
+//    the combine kernel; slower than it on the measured shapes).
 //  * Launched as a programmatic dependent: the barrier / TMEM prologue
 //    overlaps the previous kernel, the wait comes before the first global
 //    read.
@@ -60,6 +64,15 @@ namespace mm {
 
 constexpr int kEpiWarps = 8;                   // two per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
+// Single-CTA launches that store y (FC2, or the megakernel) carry two more
+// warps: the combine role, used when the combine is folded into FC2.
+constexpr int kCombineWarps = 2;
+template <int MODE, bool PAIR>
+struct Roles {
+  static constexpr bool kFold = !PAIR && (MODE == kModeY || MODE == kModeMega);
+  static constexpr int kThreads = mm::kThreads + (kFold ? 32 * kCombineWarps : 0);
+};
+constexpr int kCq = 256;  // the combine queue's slots (one per completed token n-tile)
 constexpr uint32_t kTmemCols = 512;
 // Scale factors live in TMEM after the accumulator (columns 0-255): four
 // 16-column slots used in turn by successive groups of four K blocks (A atom
@@ -104,6 +117,62 @@ __device__ __noinline__ bool wait_count_geq(const int32_t* count, int target, vo
   return true;
 }
 
+// The folded combine's arithmetic for up to NTOK (token, n-tile) pairs at
+// once (one warp, eight columns per lane of the n-tile's 256; t < 0: none):
+// out[t, c] = bf16_rn(fma chain over the active k = 0..K-1, ascending, of
+// w[t, k] * y[inv_pad[t*K + k], c]) from +0 -- the combine kernel's
+// arithmetic, so the output is bit-identical.  Every route row is loaded
+// before any arithmetic, so the warp waits for one L2 round trip per call.
+template <int NTOK>
+__device__ __forceinline__ void fold_combine(const GemmArgs& gy, const int64_t (&t)[NTOK],
+                                             const int (&nt)[NTOK], int lane) {
+  const int K = gy.cmb_K;
+  int c[NTOK];
+  int p[NTOK][8];
+  float wk[NTOK][8];
+  uint4 v[NTOK][8];
+#pragma unroll
+  for (int j = 0; j < NTOK; ++j) {
+    c[j] = nt[j] * 256 + lane * 8;
+    const bool on = t[j] >= 0 && c[j] < gy.N;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      p[j][k] = (on && k < K) ? __ldg(gy.cmb_inv + t[j] * K + k) : -1;
+      wk[j][k] = (on && k < K) ? __ldg(gy.cmb_w + t[j] * K + k) : 0.f;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NTOK; ++j)
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      v[j][k] = p[j][k] >= 0
+                    ? __ldcg(reinterpret_cast<const uint4*>(gy.out + (int64_t)p[j][k] * gy.ld_out + c[j]))
+                    : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int j = 0; j < NTOK; ++j) {
+    if (t[j] < 0 || c[j] >= gy.N) continue;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (p[j][k] < 0) continue;
+      const uint32_t vv[4] = {v[j][k].x, v[j][k].y, v[j][k].z, v[j][k].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(wk[j][k], bf16_bits_to_float(vv[i] & 0xFFFFu), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wk[j][k], bf16_bits_to_float(vv[i] >> 16), acc[2 * i + 1]);
+      }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(gy.cmb_out + t[j] * gy.N + c[j]) = o;
+  }
+}
+
 // One launch runs the tiles of one GEMM (phase 0), or with MODE == kModeMega
 // the FC1 tiles (phase 0: tmA/tmB/tmSfa/tmSfb, g) and then the FC2 tiles
 // (phase 1: tmA2/tmB2/tmSfa2/tmSfb2, g2, tmY).  Units are numbered phase 0
@@ -117,7 +186,7 @@ __device__ __noinline__ bool wait_count_geq(const int32_t* count, int target, vo
 // for their m-tile's fc1_done count -- never hold up an FC1 tile: with every
 // CTA resident the waits always end.
 template <int MODE, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<MODE, PAIR>::kThreads, 1)
     fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmSfa,
@@ -143,6 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ float amax_sh[2][2][128];  // [tile parity][column half][row] (fused epilogue)
+  // the folded combine's queue: epilogue warps -> combine role, one entry per
+  // completed (token, n-tile); an entry is published by writing its slot's
+  // mark (index + 1)
+  using R = Roles<MODE, PAIR>;
+  __shared__ int2 cq_item[R::kFold ? kCq : 1];
+  __shared__ int cq_mark[R::kFold ? kCq : 1];
+  __shared__ int cq_tail, cq_head, cq_freed, epi_done;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -169,6 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&unit_empty[i]), 1 + kEpiWarps);  // the MMA thread + every epilogue warp
     }
     abort_sh = 0;
+    if constexpr (R::kFold) {
+      for (int i = 0; i < kCq; ++i) cq_mark[i] = 0;
+      cq_tail = cq_head = cq_freed = epi_done = 0;
+    }
     fence_mbar_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
@@ -214,6 +294,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto m_of = [&](int u, int ph) { return ph ? (u - total0) / g2.NT : u / g.NT; };
   auto nt_of = [&](int u, int ph, int m) { return ph ? (u - total0) - m * g2.NT : u - m * g.NT; };
   auto own_mtile = [&](int m) { return PAIR ? 2 * m + (int)rank : m; };
+  // The folded combine's consumer (the combine role, and every epilogue warp
+  // once its own tiles are done): lane 0 claims two queue entries and waits
+  // (bounded) for each, or for the end -- every epilogue warp done and the
+  // index past the tail; the warp combines the entries it found together.
+  auto fold_consume = [&]() {
+    const GemmArgs& gy = kMega ? g2 : g;
+    while (true) {
+      int r = 0;  // bit j: entry j found; -1: given up
+      int2 it[2] = {make_int2(-1, 0), make_int2(-1, 0)};
+      if (lane == 0) {
+        const int base = atomicAdd(&cq_head, 2);
+        for (int j = 0; j < 2 && r >= 0; ++j) {
+          const int idx = base + j;
+          const uint64_t t0 = globaltimer_ns();
+          while (true) {
+            if (*(volatile int*)&cq_mark[idx % kCq] == idx + 1) {
+              __threadfence_block();
+              it[j] = cq_item[idx % kCq];
+              __threadfence_block();
+              atomicAdd(&cq_freed, 1);
+              r |= 1 << j;
+              break;
+            }
+            if (*(volatile int*)&epi_done == kEpiWarps) {
+              __threadfence_block();
+              if (idx >= *(volatile int*)&cq_tail) break;
+            }
+            if (*abort) {
+              r = -1;
+              break;
+            }
+            if (globaltimer_ns() - t0 > g.wait_limit_ns) {
+              *abort = 1;
+              record_status(g.status, MOE_DEV_TIMEOUT);
+              r = -1;
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
+      }
+      r = __shfl_sync(0xFFFFFFFFu, r, 0);
+      if (r <= 0) break;
+      const int64_t tt[2] = {(r & 1) ? (int64_t)__shfl_sync(0xFFFFFFFFu, it[0].x, 0) : -1,
+                             (r & 2) ? (int64_t)__shfl_sync(0xFFFFFFFFu, it[1].x, 0) : -1};
+      const int nn[2] = {__shfl_sync(0xFFFFFFFFu, it[0].y, 0), __shfl_sync(0xFFFFFFFFu, it[1].y, 0)};
+      fold_combine<2>(gy, tt, nn, lane);
+      if (!(r & 2)) break;  // the second index was past the end
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -494,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     // Eight warps, two per TMEM lane quadrant; thread = accumulator row, and
     // the two warps of a quadrant split the columns: FC2 -> columns
@@ -516,6 +646,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the dynamic schedule's next unit: lane 0 takes it from the ring for the warp
     int slot = 0;
     uint32_t slot_ph = 0;
+    // the folded combine: a lane queues a completed (token, n-tile) for the
+    // combine role (bounded wait for a free slot)
+    auto cq_push = [&](int tok, int ntile) -> bool {
+      const int idx = atomicAdd(&cq_tail, 1);
+      const uint64_t t0 = globaltimer_ns();
+      while (idx - *(volatile int*)&cq_freed >= kCq) {
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > g.wait_limit_ns) {
+          *abort = 1;
+          record_status(g.status, MOE_DEV_TIMEOUT);
+          return false;
+        }
+      }
+      cq_item[idx % kCq] = make_int2(tok, ntile);
+      __threadfence_block();
+      *(volatile int*)&cq_mark[idx % kCq] = idx + 1;
+      return true;
+    };
     auto take = [&]() -> int {
       int v = total;
       if (lane == 0 &&
@@ -550,6 +698,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool em_y = em == kModeY;
       const bool em_gu = em == kModeGU || em == kModeFusedGU;
       const bool em_fused = em == kModeFused || em == kModeFusedGU;
+      // the folded combine: this row's token and its count target (two
+      // column halves per active route), read before the accumulator wait
+      int f_tok = -1, f_target = 0;
+      if constexpr (R::kFold) {
+        const GemmArgs& gy = (kMega && ph) ? g2 : g;
+        if (em_y && gy.cmb_cnt && live) {
+          const int64_t local = (int64_t)mt * 128 + row_in_tile - g.pad_offsets[e_t];
+          if (local < g.counts[e_t]) {
+            f_tok = gy.cmb_perm[gy.cmb_offsets[e_t] + local] / gy.cmb_K;
+            int nact = 0;
+            for (int k = 0; k < gy.cmb_K; ++k)
+              nact += __ldg(gy.cmb_inv + (int64_t)f_tok * gy.cmb_K + k) >= 0;
+            f_target = 2 * nact;
+          }
+        }
+      }
       if (!mbar_wait(smem_u32(&accf_bar), acc_phase, abort, g.status, g.wait_limit_ns)) break;
       tc_fence_after();
       const int64_t row = (int64_t)mt * 128 + row_in_tile;
@@ -635,6 +799,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int v = 0; v < 8; ++v)
             st_global_v8(dst + 16 * v, pk[8 * v], pk[8 * v + 1], pk[8 * v + 2], pk[8 * v + 3],
                          pk[8 * v + 4], pk[8 * v + 5], pk[8 * v + 6], pk[8 * v + 7]);
+        }
+      }
+      if constexpr (R::kFold) {
+        // The combine folded in: once this warp's y boxes are written (not
+        // only read out of shared memory) and made visible at GPU scope,
+        // each routed row adds one to its token's count for the n-tile (a
+        // tile half past H stores nothing and counts all the same).  The
+        // lane whose add completes a count queues the (token, n-tile) for
+        // the combine role.
+        const GemmArgs& gy = (kMega && ph) ? g2 : g;
+        if (em_y && gy.cmb_cnt && live) {
+          if (lane == 0 && active) {
+            bulk_wait_group0();
+            fence_proxy_async_global();
+          }
+          __syncwarp();
+          __threadfence();
+          const bool done =
+              f_tok >= 0 && atomicAdd(gy.cmb_cnt + (int64_t)f_tok * gy.NT + nt, 1) == f_target - 1;
+          if (__any_sync(0xFFFFFFFFu, done)) __threadfence();
+          const int ok = done ? (cq_push(f_tok, nt) ? 1 : 0) : 1;
+          if (!__all_sync(0xFFFFFFFFu, ok)) break;
         }
       }
       if (em_gu && active) {
@@ -764,10 +950,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++fc1_tiles;
       }
     }
+    if constexpr (R::kFold) {
+      // nothing more to queue from this warp; it helps combine what is left
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        atomicAdd(&epi_done, 1);
+      }
+      if ((kMega ? g2 : g).cmb_cnt) fold_consume();
+    }
+  } else if constexpr (R::kFold) {
+    // ------------------------------------------------------------ combine role
+    // With the combine folded in (the FC2 args carry cmb_cnt), two warps
+    // combine the (token, n-tile) pairs whose counts the epilogue completed:
+    // a count is complete at 2 x the token's active routes (both column
+    // halves of every route row stored), and the lane whose add completes it
+    // queues the pair.  Tokens with no active route get +0 rows here, as the
+    // combine kernel gives them.
+    const GemmArgs& gy = kMega ? g2 : g;
+    if (gy.cmb_cnt) {
+      const int cw = warp - 2 - kEpiWarps;
+      const int K = gy.cmb_K;
+      const int64_t zstride = (int64_t)gridDim.x * kCombineWarps * 32;
+      for (int64_t t = ((int64_t)blockIdx.x * kCombineWarps + cw) * 32 + lane; t < gy.cmb_T;
+           t += zstride) {
+        int nact = 0;
+        for (int k = 0; k < K; ++k) nact += __ldg(gy.cmb_inv + t * K + k) >= 0;
+        if (nact == 0)
+          for (int c = 0; c < gy.N; c += 8)
+            *reinterpret_cast<uint4*>(gy.cmb_out + t * gy.N + c) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      fold_consume();
+    }
   }
 
   if constexpr ((MODE == kModeY || MODE == kModeMega) && StageCfg<PAIR>::kTmaStoreY) {
-    if (warp >= 2 && lane == 0) bulk_wait_group0();  // this warp's output boxes are written
+    // this warp's output boxes are written
+    if (warp >= 2 && warp < 2 + kEpiWarps && lane == 0) bulk_wait_group0();
   }
   tc_fence_before();
   __syncthreads();
@@ -839,11 +1058,11 @@ static cudaError_t launch_mode(bool pair, const CUtensorMap* tmA, const CUtensor
                                const CUtensorMap* tmY, const GemmArgs& g, const GemmArgs& g2,
                                int ctas, cudaStream_t s, bool pdl) {
   if (!pair)
-    return launch_k(fp8_grouped_gemm_kernel<MODE, false>, dim3(ctas), dim3(kThreads),
+    return launch_k(fp8_grouped_gemm_kernel<MODE, false>, dim3(ctas), dim3(Roles<MODE, false>::kThreads),
                     StageCfg<false>::kDynSmem, s, pdl, nullptr, *tmA, *tmB, *tmA, *tmA, *tmY, g,
                     *tmA2, *tmB2, *tmA2, *tmA2, g2);
   const cudaLaunchAttribute cluster = pair_cluster_attr();
-  return launch_k(fp8_grouped_gemm_kernel<MODE, true>, dim3(ctas), dim3(kThreads),
+  return launch_k(fp8_grouped_gemm_kernel<MODE, true>, dim3(ctas), dim3(Roles<MODE, true>::kThreads),
                   StageCfg<true>::kDynSmem, s, pdl, &cluster, *tmA, *tmB, *tmSfa, *tmSfb, *tmY, g,
                   *tmA2, *tmB2, *tmSfa2, *tmSfb2, g2);
 }

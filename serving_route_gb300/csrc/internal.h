@@ -16,8 +16,8 @@ struct Workspace {
   int32_t* total_mtiles;   // number of 128-row GEMM tiles of this forward
   uint32_t* grid_sync;     // arrival counter of the one-kernel routing (zeroed before each forward)
   int32_t* gemm_sched;     // [2] unit counters of the FC1 and FC2 launches (zeroed before each forward)
-  int32_t* cmb_cnt;        // [64][ceil(H/256)] stored y chunks per token and n-tile (zeroed before each
-                           // forward that folds the combine into the token-as-N FC2)
+  int32_t* cmb_cnt;        // [max_rows][ceil(H/256)] stored y chunks per token and n-tile (zeroed
+                           // before each forward that folds the combine into FC2)
   int32_t* fc1_done;       // [max_mtiles] FC1 tiles published per m-tile (zeroed before each forward)
   int32_t* counts;         // [E]
   int32_t* offsets;        // [E+1]
@@ -65,7 +65,7 @@ struct Layout {
   size_t ws_bytes, w_bytes;
   // byte offsets inside the workspace / weight store
   size_t o_fc1_done;   // [max_mtiles] int32 counters of the megakernel, right after the status
-  size_t o_cmb;        // [64][ceil(H/256)] int32 combine counters of the token-as-N FC2, after those
+  size_t o_cmb;        // [max_rows][ceil(H/256)] int32 counters of the folded combine, after those
   size_t o_status, o_counts, o_offsets, o_pad_offsets, o_mtile_expert, o_block_counts, o_base_u,
       o_base_p, o_perm, o_inv, o_inv_pad, o_a, o_a_sf, o_gu, o_hq, o_h_sf, o_y;
   size_t o_w1, o_w2, o_w1_sf, o_w2_sf, o_w1_sfatoms, o_w2_sfatoms, o_pt;
@@ -162,11 +162,12 @@ struct GemmArgs {
   // nullptr in the block-scaled formats
   const float* pt_scale;
   const float* pt_rh;
-  // token-as-N FC2 with the combine folded in (nullptr cmb_cnt: the combine
-  // kernel runs after): per token and 256-column n-tile, the stored y chunks
-  // (one count per route and lane-quadrant warp; zeroed before each
-  // forward); the warp that completes a token's count combines that column
-  // range of the token into the BF16 output, as the combine kernel does
+  // FC2 with the combine folded in (nullptr cmb_cnt: the combine kernel runs
+  // after): per token and 256-column n-tile, the stored y chunks (token-as-N:
+  // one count per route and lane-quadrant warp; M128 x N256: one per route
+  // and column half; zeroed before each forward); the warp that completes a
+  // token's count combines that column range of the token into the BF16
+  // output, as the combine kernel does
   int32_t* cmb_cnt;         // [T][NT]
   uint16_t* cmb_out;        // BF16 [T, H]
   const float* cmb_w;       // top-k weights [T, K]

@@ -23,8 +23,9 @@ class MegaMoELayer:
         """gemm: "auto" (tactic from expected_m), "single" (one CTA per SM) or
         "pair" (CTA pairs, tcgen05 cta_group::2).  swap_ab: forwards of at
         most 64 tokens on single CTAs run the token-as-N GEMMs (False keeps
-        the M128 x N256 kernel); combine_in_fc2: their FC2 folds the combine
-        in (no combine kernel; bit-identical output).  gemms (fused epilogue only):
+        the M128 x N256 kernel); combine_in_fc2: on single CTAs (either
+        kernel) FC2 folds the combine in (no combine kernel; bit-identical
+        output); ignored under CTA pairs.  gemms (fused epilogue only):
         "auto" (FC1 -> FC2 in one persistent launch for short forwards, two
         launches for long ones), "one_launch" or "split"; same results.
         fmt: "deepseek" (1x128 activation / 128x128 weight scales),
