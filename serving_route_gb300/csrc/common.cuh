@@ -133,7 +133,11 @@ __device__ __forceinline__ void record_status(uint32_t* status, uint32_t bits) {
 // memory that any earlier kernel of the forward writes or reads (the wait
 // returns once the predecessor grid has completed and its writes are
 // visible; completion is transitive along the chain).  pdl_trigger() lets the
-// successor launch once every CTA of this grid has issued it or exited.
+// successor launch once every CTA of this grid has issued it or exited.  A
+// kernel that is itself a dependent issues pdl_trigger() only after its
+// pdl_wait(): quant_dispatch triggering at its very start (so that the GEMM
+// after it could launch while the routing still ran) read routing tables the
+// routing had not yet written (a one-token forward's A row came out wrong).
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -328,11 +332,6 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
 // CTA made visible to it before is visible to a thread that acquires the sum.
 __device__ __forceinline__ void red_release_gpu_add(int32_t* p, int32_t v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const void* map) {
