@@ -230,6 +230,30 @@ MOE_API moe_status moe_quantize_weights_mx(const float* d_w, int64_t num_mats, i
                                            struct CUstream_st* stream);
 
 /*
+ * moe_requantize_weights_nvfp4 -- NVFP4 checkpoint weights to the format
+ * moe_bind_weights takes by default (128x128 blocks, as moe_quantize_weights
+ * gives): the one-time requantization through which NVFP4 checkpoints run
+ * on the FP8 layer (flashinfer PR #4069, Reviewer notes).  Every value is
+ *   v = e2m1(code) * e4m3(block scale) * global, rounded to float once,
+ * and the 128x128 blocks of v are quantised as moe_quantize_weights does.
+ *   d_codes         uint8 [num_mats, rows, cols/2]: two E2M1 codes per byte
+ *                   along the columns, column 2b in the low nibble of byte b
+ *                   (16-byte aligned).
+ *   d_block_scales  uint8 [num_mats, rows, cols/16]: one E4M3 scale per 16
+ *                   consecutive columns of a row (4-byte aligned).
+ *   d_global_scales float [num_mats]: one scale per matrix.
+ *   d_q, d_scale    outputs as moe_quantize_weights (d_q 16-byte aligned).
+ * Block and global scales must be finite (NaN scale codes give undefined
+ * output).  Asynchronous on `stream`.  MOE_ERR_INVALID_ARG for a NULL or
+ * misaligned pointer or a non-positive size, MOE_ERR_UNSUPPORTED unless rows
+ * and cols are multiples of 128.
+ */
+MOE_API moe_status moe_requantize_weights_nvfp4(const uint8_t* d_codes, const uint8_t* d_block_scales,
+                                                const float* d_global_scales, int64_t num_mats,
+                                                int32_t rows, int32_t cols, uint8_t* d_q,
+                                                float* d_scale, struct CUstream_st* stream);
+
+/*
  * moe_quantize_weights_pt -- FP32 expert weights to the per-tensor form that
  * moe_bind_weights takes under MOE_FLAG_PER_TENSOR: one scale per matrix,
  * s = float(amax / 448) (1 for an all-zero matrix), codes =

@@ -68,6 +68,9 @@ def lib():
         L.or_quant_rows_bf16_bw.argtypes = [vp, i64, i64, i32, vp, vp]
         L.or_quant_weights.argtypes = [vp, i64, i64, i64, vp, vp]
         L.or_quant_weights_mx.argtypes = [vp, i64, i64, i64, vp, vp]
+        L.or_e2m1_decode.argtypes = [ctypes.c_uint8]
+        L.or_e2m1_decode.restype = ctypes.c_double
+        L.or_dequant_nvfp4.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         L.or_route.argtypes = [i64, i32, i32, vp, vp, i32, vp, vp, vp, vp]
         L.or_route.restype = ctypes.c_uint32
         L.or_expert_ffn.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -162,6 +165,31 @@ def quant_weights_mx(w: np.ndarray):
     s = np.empty((nmat, rows, cols // 32), np.float32)
     lib().or_quant_weights_mx(_p(w), nmat, rows, cols, _p(q), _p(s))
     return q, s
+
+
+def e2m1_decode(nibble: int) -> float:
+    return lib().or_e2m1_decode(nibble)
+
+
+def dequant_nvfp4(codes: np.ndarray, sblk: np.ndarray, g: np.ndarray) -> np.ndarray:
+    """NVFP4 matrices -> float32 values: codes uint8 [nmat, rows, cols/2] (two
+    E2M1 codes per byte, the even column in the low nibble), sblk uint8
+    [nmat, rows, cols/16] (E4M3 scale per 16 columns), g float32 [nmat]."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sblk = np.ascontiguousarray(sblk, dtype=np.uint8)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    nmat, rows, half = codes.shape
+    cols = 2 * half
+    assert sblk.shape == (nmat, rows, cols // 16) and g.shape == (nmat,)
+    out = np.empty((nmat, rows, cols), np.float32)
+    lib().or_dequant_nvfp4(_p(codes), _p(sblk), _p(g), nmat, rows, cols, _p(out))
+    return out
+
+
+def requant_nvfp4(codes: np.ndarray, sblk: np.ndarray, g: np.ndarray):
+    """NVFP4 matrices -> the 128x128 FP8 weight format (q, s): the weight
+    quantiser applied to the dequantised float values."""
+    return quant_weights(dequant_nvfp4(codes, sblk, g))
 
 
 # --------------------------------------------------------------------------

@@ -232,6 +232,42 @@ void or_quant_weights_mx(const float* w, int64_t nmat, int64_t rows, int64_t col
 }
 
 /* ---------------------------------------------------------------------------
+ * NVFP4 checkpoint weights (flashinfer PR #4069, Reviewer notes: NVFP4
+ * checkpoints ride the FP8 backend unchanged through a one-time
+ * requantization).  An NVFP4 matrix [rows, cols] holds E2M1 codes packed two
+ * per byte along the columns (column 2b in the low nibble of byte b, column
+ * 2b+1 in the high nibble), one E4M3 scale per 16 consecutive columns of a
+ * row and one float scale per matrix:
+ *   value = e2m1(code) * e4m3(block scale) * global,
+ * rounded to float once (the first product is exact).  The requantization
+ * is the 128x128 weight quantiser above applied to these float values.
+ * ------------------------------------------------------------------------- */
+
+/* E2M1: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0; exponent
+ * field 0 is the subnormal m * 0.5.  Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double or_e2m1_decode(uint8_t nibble) {
+  const int sgn = (nibble >> 3) & 1, e = (nibble >> 1) & 3, m = nibble & 1;
+  const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return sgn ? -mag : mag;
+}
+
+/* codes [nmat, rows, cols/2], sblk [nmat, rows, cols/16] E4M3, g [nmat]
+ * -> out float [nmat, rows, cols].  The double product is exact (at most 30
+ * significant bits), so the one conversion to float is the only rounding. */
+void or_dequant_nvfp4(const uint8_t* codes, const uint8_t* sblk, const float* g, int64_t nmat,
+                      int64_t rows, int64_t cols, float* out) {
+  for (int64_t m = 0; m < nmat; ++m)
+    for (int64_t r = 0; r < rows; ++r)
+      for (int64_t c = 0; c < cols; ++c) {
+        const int64_t row = m * rows + r;
+        const uint8_t nib = (uint8_t)((codes[row * (cols / 2) + c / 2] >> (4 * (c & 1))) & 0xF);
+        const double v = or_e2m1_decode(nib) * or_e4m3_decode(sblk[row * (cols / 16) + c / 16]) *
+                         (double)g[m];
+        out[row * cols + c] = (float)v;
+      }
+}
+
+/* ---------------------------------------------------------------------------
  * Routing: validation, histogram, exclusive scan, stable scatter.
  * ------------------------------------------------------------------------- */
 

@@ -48,7 +48,8 @@ MOE_FLAG_COMBINE_IN_FC2 = 0x1000
 
 # every function the header declares (checked against include/megamoe.h by a test)
 API_NAMES = ("moe_workspace_query", "moe_create", "moe_quantize_weights", "moe_quantize_weights_mx",
-             "moe_quantize_weights_pt", "moe_bind_weights", "moe_set_activation_scales",
+             "moe_quantize_weights_pt", "moe_requantize_weights_nvfp4", "moe_bind_weights",
+             "moe_set_activation_scales",
              "moe_stage_inputs", "moe_forward", "moe_read_status", "moe_debug_views",
              "moe_set_profile_events", "moe_set_sm_budget", "moe_forward_plan", "moe_route_noalloc",
              "moe_destroy", "moe_status_str")
@@ -102,6 +103,7 @@ def lib() -> ctypes.CDLL:
         L.moe_quantize_weights.argtypes = [vp, i64, i32, i32, vp, vp, vp]
         L.moe_quantize_weights_mx.argtypes = [vp, i64, i32, i32, vp, vp, vp]
         L.moe_quantize_weights_pt.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+        L.moe_requantize_weights_nvfp4.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp, vp]
         L.moe_set_activation_scales.argtypes = [vp, ctypes.c_float, ctypes.c_float, vp]
         L.moe_bind_weights.argtypes = [vp, vp, vp, vp, vp, vp]
         L.moe_stage_inputs.argtypes = [vp, vp]
@@ -166,6 +168,13 @@ def moe_quantize_weights_mx(d_w, num_mats, rows, cols, d_q, d_scale, stream) -> 
 def moe_quantize_weights_pt(d_w, num_mats, rows, cols, d_q, d_scale, stream) -> None:
     _check(lib().moe_quantize_weights_pt(d_w, num_mats, rows, cols, d_q, d_scale, stream),
            "moe_quantize_weights_pt")
+
+
+def moe_requantize_weights_nvfp4(d_codes, d_block_scales, d_global_scales, num_mats, rows, cols, d_q,
+                                 d_scale, stream) -> None:
+    _check(lib().moe_requantize_weights_nvfp4(d_codes, d_block_scales, d_global_scales, num_mats, rows,
+                                              cols, d_q, d_scale, stream),
+           "moe_requantize_weights_nvfp4")
 
 
 def moe_set_activation_scales(h, x_scale, h_scale, stream) -> None:

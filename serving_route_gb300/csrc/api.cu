@@ -398,6 +398,23 @@ moe_status moe_quantize_weights(const float* d_w, int64_t num_mats, int32_t rows
   return MOE_OK;
 }
 
+moe_status moe_requantize_weights_nvfp4(const uint8_t* d_codes, const uint8_t* d_block_scales,
+                                        const float* d_global_scales, int64_t num_mats, int32_t rows,
+                                        int32_t cols, uint8_t* d_q, float* d_scale,
+                                        struct CUstream_st* stream) {
+  if (!d_codes || !d_block_scales || !d_global_scales || !d_q || !d_scale || num_mats < 0 ||
+      rows <= 0 || cols <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (rows % 128 || cols % 128) return MOE_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(d_codes) % 16 || reinterpret_cast<uintptr_t>(d_block_scales) % 4 ||
+      reinterpret_cast<uintptr_t>(d_q) % 16)
+    return MOE_ERR_INVALID_ARG;
+  if (launch_requant_nvfp4(d_codes, d_block_scales, d_global_scales, num_mats, rows, cols, d_q,
+                           d_scale, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status moe_quantize_weights_mx(const float* d_w, int64_t num_mats, int32_t rows, int32_t cols,
                                    uint8_t* d_q, float* d_scale, struct CUstream_st* stream) {
   if (!d_w || !d_q || !d_scale || num_mats < 0 || rows <= 0 || cols <= 0) return MOE_ERR_INVALID_ARG;

@@ -113,6 +113,11 @@ cudaError_t launch_pt_set_scales(const WeightStore& wst, const Layout& L, float 
                                  float h_scale, cudaStream_t s);
 cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
                                     float* scale, cudaStream_t s);
+// NVFP4 checkpoint weights (codes [nmat, rows, cols/2], E4M3 scales
+// [nmat, rows, cols/16], float global [nmat]) -> the 128x128 FP8 format.
+cudaError_t launch_requant_nvfp4(const uint8_t* codes, const uint8_t* sblk, const float* gs,
+                                 int64_t nmat, int rows, int cols, uint8_t* q, float* scale,
+                                 cudaStream_t s);
 cudaError_t launch_quantize_weights_mx(const float* w, int64_t nmat, int rows, int cols, uint8_t* q,
                                        float* scale, cudaStream_t s);
 cudaError_t launch_bind_transform(const WeightStore& wst, const Layout& L, const uint8_t* w1,

@@ -272,6 +272,89 @@ __global__ void __launch_bounds__(256) quantize_weights_kernel(const float* __re
   if (threadIdx.x == 0) scale[(m * rb + bi) * cb + bj] = pow2_neg(-e);
 }
 
+// NVFP4 checkpoint weights -> the 128x128 FP8 weight format (flashinfer PR
+// #4069, Reviewer notes: NVFP4 checkpoints ride the FP8 backend unchanged
+// through a one-time requantization).  An NVFP4 matrix holds E2M1 codes two
+// per byte along the columns (the even column in the low nibble), an E4M3
+// scale per 16 columns of a row and a float scale per matrix; each value is
+// e2m1 * e4m3 * global with one float rounding (the first product is
+// exact), then quantised as quantize_weights_kernel does.  The two decoders
+// follow the formats' definitions.
+__device__ __forceinline__ float e2m1_value(uint32_t nib) {
+  // sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0; exponent 0 is
+  // the subnormal mantissa * 0.5
+  const uint32_t e = (nib >> 1) & 3u, m = nib & 1u;
+  const float mag =
+      e == 0u ? 0.5f * (float)m : __int_as_float((int)((e + 126u) << 23)) * (1.0f + 0.5f * (float)m);
+  return (nib & 8u) ? -mag : mag;
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  // OCP E4M3FN: exponent bits 6..3 (bias 7), mantissa bits 2..0; exponent 0
+  // is the subnormal mantissa * 2^-9; S.1111.111 is NaN
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  float mag;
+  if (e == 15u && m == 7u)
+    mag = __int_as_float(0x7FC00000);
+  else if (e == 0u)
+    mag = (float)m * 0.001953125f;
+  else
+    mag = __int_as_float((int)((e + 120u) << 23)) * (1.0f + 0.125f * (float)m);
+  return (c & 0x80u) ? -mag : mag;
+}
+
+// One CTA per 128x128 block, a thread per half row (64 values: 32 code bytes,
+// four block scales).
+__global__ void __launch_bounds__(256) requant_nvfp4_kernel(const uint8_t* __restrict__ codes,
+                                                            const uint8_t* __restrict__ sblk,
+                                                            const float* __restrict__ gs, int rows,
+                                                            int cols, uint8_t* __restrict__ q,
+                                                            float* __restrict__ scale) {
+  __shared__ float red[8];
+  const int rb = rows >> 7, cb = cols >> 7;
+  const int64_t blk = blockIdx.x;
+  const int64_t m = blk / ((int64_t)rb * cb);
+  const int bi = (int)((blk / cb) % rb), bj = (int)(blk % cb);
+  const int r = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 64;
+  const int64_t row = m * rows + (int64_t)bi * 128 + r;
+  const int64_t col = (int64_t)bj * 128 + c0;
+  const float g = gs[m];
+  const uint4 b0 = *reinterpret_cast<const uint4*>(codes + row * (cols / 2) + col / 2);
+  const uint4 b1 = *reinterpret_cast<const uint4*>(codes + row * (cols / 2) + col / 2 + 16);
+  const uint32_t sw = *reinterpret_cast<const uint32_t*>(sblk + row * (cols / 16) + col / 16);
+  const uint32_t wd[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+  float v[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const uint32_t nib = (wd[i >> 3] >> (4 * (i & 7))) & 0xFu;
+    const float sc = e4m3_value((sw >> (8 * (i >> 4))) & 0xFFu);
+    v[i] = __fmul_rn(e2m1_value(nib) * sc, g);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  const int e = pow2_scale_exp(amax);
+  const float inv = pow2_neg(e);
+  const int64_t base = row * cols + col;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 o;
+    o.x = e4m3x4(v[16 * i + 0] * inv, v[16 * i + 1] * inv, v[16 * i + 2] * inv, v[16 * i + 3] * inv);
+    o.y = e4m3x4(v[16 * i + 4] * inv, v[16 * i + 5] * inv, v[16 * i + 6] * inv, v[16 * i + 7] * inv);
+    o.z = e4m3x4(v[16 * i + 8] * inv, v[16 * i + 9] * inv, v[16 * i + 10] * inv, v[16 * i + 11] * inv);
+    o.w = e4m3x4(v[16 * i + 12] * inv, v[16 * i + 13] * inv, v[16 * i + 14] * inv, v[16 * i + 15] * inv);
+    *reinterpret_cast<uint4*>(q + base + 16 * i) = o;
+  }
+  if (threadIdx.x == 0) scale[(m * rb + bi) * cb + bj] = pow2_neg(-e);
+}
+
 // MXFP8 weights: every row quantised in 1x32 blocks along its columns; one
 // thread per 32-float chunk (chunks are contiguous, so the scale index is the
 // chunk index: [nmat, rows, cols/32]).
@@ -426,6 +509,16 @@ cudaError_t launch_quantize_weights(const float* w, int64_t nmat, int rows, int 
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   quantize_weights_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, rows, cols, q, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_requant_nvfp4(const uint8_t* codes, const uint8_t* sblk, const float* gs,
+                                 int64_t nmat, int rows, int cols, uint8_t* q, float* scale,
+                                 cudaStream_t s) {
+  const int64_t blocks = nmat * (rows / 128) * (cols / 128);
+  if (blocks == 0) return cudaSuccess;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  requant_nvfp4_kernel<<<(unsigned)blocks, 256, 0, s>>>(codes, sblk, gs, rows, cols, q, scale);
   return cudaGetLastError();
 }
 

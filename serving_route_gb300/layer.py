@@ -109,6 +109,28 @@ class MegaMoELayer:
                                    _stream_ptr(stream))
         return q, s
 
+    @staticmethod
+    def requantize_weights_nvfp4(codes: torch.Tensor, block_scales: torch.Tensor,
+                                 global_scales: torch.Tensor, stream=None):
+        """NVFP4 checkpoint matrices on the GPU -> the default 128x128 FP8
+        format (E4M3 uint8 [n, rows, cols], float scales [n, rows/128,
+        cols/128]): codes uint8 [n, rows, cols/2] (two E2M1 codes per byte,
+        the even column in the low nibble), block_scales uint8 [n, rows,
+        cols/16] (E4M3, one per 16 columns), global_scales float32 [n]."""
+        for t in (codes, block_scales, global_scales):
+            assert t.is_cuda and t.is_contiguous()
+        assert codes.dtype == torch.uint8 and block_scales.dtype == torch.uint8
+        assert global_scales.dtype == torch.float32 and codes.dim() == 3
+        n, r, half = codes.shape
+        c = 2 * half
+        assert tuple(block_scales.shape) == (n, r, c // 16) and tuple(global_scales.shape) == (n,)
+        q = torch.empty((n, r, c), dtype=torch.uint8, device=codes.device)
+        s = torch.empty((n, r // 128, c // 128), dtype=torch.float32, device=codes.device)
+        B.moe_requantize_weights_nvfp4(codes.data_ptr(), block_scales.data_ptr(),
+                                       global_scales.data_ptr(), n, r, c, q.data_ptr(), s.data_ptr(),
+                                       _stream_ptr(stream))
+        return q, s
+
     def bind_weights(self, w1_q, w1_s, w2_q, w2_s, stream=None) -> None:
         for t in (w1_q, w1_s, w2_q, w2_s):
             assert t.is_cuda and t.is_contiguous()
