@@ -269,16 +269,27 @@ __global__ void __launch_bounds__(kFusedTokens) route_fused_kernel(
   }
   if (err) record_status(status, err);
   __syncthreads();
+  // One block (at most 512 tokens): its histogram is the whole one, so the
+  // expert totals go straight to shared memory (no earlier block: prefix 0)
+  // and the grid barrier and the histogram's round trip through global
+  // memory are skipped.
+  const bool one = nb == 1;
   for (int e = tid; e < E; e += blockDim.x) {
     int c = 0;
 #pragma unroll
     for (int v = 0; v < kRouteWarps; ++v) c += wh[v * E + e];
     block_counts[(int64_t)b * E + e] = c;
+    if (one) {
+      bu[e] = c;
+      bp[e] = 0;
+    }
   }
 
   // ---- grid barrier
   __syncthreads();
-  if (tid == 0) {
+  if (one) {
+    if (tid == 0) passed = 1;
+  } else if (tid == 0) {
     __threadfence();  // this block's histogram row before its arrival
     if (b != withhold) atomicAdd(grid_sync, 1u);  // withhold: the barrier test's missing block
     bool ok = true;
@@ -312,12 +323,14 @@ __global__ void __launch_bounds__(kFusedTokens) route_fused_kernel(
   // expert totals and this block's prefix over the earlier blocks: the
   // (block, expert) entries spread over the threads, eight loads in flight
   // per thread, summed with shared-memory atomics
-  for (int e = tid; e < E; e += blockDim.x) {
-    bu[e] = 0;
-    bp[e] = 0;
+  if (!one) {
+    for (int e = tid; e < E; e += blockDim.x) {
+      bu[e] = 0;
+      bp[e] = 0;
+    }
   }
   __syncthreads();
-  const int n_ent = nb * E;
+  const int n_ent = one ? 0 : nb * E;
   for (int p0 = tid; p0 < n_ent; p0 += 8 * kFusedTokens) {
     int c[8];
 #pragma unroll
