@@ -20,16 +20,20 @@ from tests.test_gpu_parity import compare_outputs, small_problem
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("gemm", ["single", "pair", "swap"])
+@pytest.mark.parametrize("gemm,fold", [("single", False), ("pair", False), ("swap", False),
+                                       ("single", True), ("swap", True)])
 @pytest.mark.parametrize("split", [False, True])
-def test_watchdog_expires_with_status_and_context_survives(orc, split, gemm):
+def test_watchdog_expires_with_status_and_context_survives(orc, split, gemm, fold):
     """split=False: the one-launch FC1 -> FC2 kernel, where the FC2 tiles of
     the other CTAs also wait in vain for the m-tile counts that CTA 0 (or
     pair 0) never publishes, and expire on their own bound.  gemm="pair": the
     leader's MMA wait expires; the peer's waits on the leader's commits expire
     too, and both CTAs meet at the cluster barrier before freeing the pair's
     tensor memory.  gemm="swap": a 40-token forward on single CTAs, which runs
-    the token-as-N kernels (double-buffered accumulators, counter schedule)."""
+    the token-as-N kernels (double-buffered accumulators, counter schedule).
+    fold: the combine folded into FC2 as well, whose queue and counters wait
+    on the tiles the expired CTA never stores (their waits end on the abort
+    flag or their own bound)."""
     import __graft_entry__ as ge
     ge.build()
     import serving_route_gb300 as S
@@ -44,8 +48,9 @@ def test_watchdog_expires_with_status_and_context_survives(orc, split, gemm):
     xt, it, wt = gh.to_device(x, idx, w)
 
     bad = S.MegaMoELayer(H, I, E, K, max_rows=T, fuse_fc1=True, gemm=gemm, watchdog_test=True,
-                         gemms="split" if split else "one_launch")
+                         gemms="split" if split else "one_launch", combine_in_fc2=fold)
     assert (bad.plan(T)["swap_ab_tokens"] > 0) == swap
+    assert bad.plan(T)["combine_in_fc2"] == (1 if fold else 0)
     bad.bind_weights(q1, s1, q2, s2)
     bad.forward(xt, it, wt)
     st, bits = bad.read_status()
