@@ -517,12 +517,16 @@ moe_status moe_forward(moe_handle* h, const uint16_t* d_x, const int32_t* d_topk
   const bool fold = plan.combine_in_fc2 != 0;
   const size_t reset = fold ? L.o_cmb - L.o_status + 4 * (size_t)num_tokens * ((L.H + 255) / 256)
                             : (mega ? 1024 + 4 * (size_t)(L.rows_alloc / 128) : 20);
-  cudaMemsetAsync(ws.status, 0, reset, s);
+  // A one-block routing kernel (the one-kernel form, at most 512 tokens)
+  // clears them itself, which saves the forward a memset node.
+  const bool route_clears = plan.route_kernels == 1 && num_tokens <= 512;
+  if (!route_clears && cudaMemsetAsync(ws.status, 0, reset, s) != cudaSuccess) return MOE_ERR_CUDA;
   // Under an SM budget the routing keeps to its three small kernels: a
   // cooperative grid would have to be resident beside the side-stream work.
   const int coop = plan.route_kernels == 1 ? h->route_coop_blocks : 0;
   if (launch_route(ws, L, d_topk_idx, d_topk_w, num_tokens, check, s, ev ? ev + 1 : nullptr,
-                   coop, (h->dims.flags & MOE_FLAG_WATCHDOG_ROUTE_TEST) != 0) != cudaSuccess)
+                   coop, (h->dims.flags & MOE_FLAG_WATCHDOG_ROUTE_TEST) != 0,
+                   route_clears ? (int64_t)(reset / 4) : 0) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev) record_event(ev[4], s);
   // Kernels after the first are programmatic dependents of their predecessor

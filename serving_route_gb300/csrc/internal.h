@@ -86,9 +86,13 @@ moe_status compute_layout(const moe_dims* d, int64_t expected_m, int64_t max_row
 // three kernels route_count / route_scan / route_scatter.  Same outputs.
 // watchdog_test: the one-kernel form's last block withholds its arrival at
 // the grid barrier, whose bound drops to 20 ms (test only).
+// zero_words: when the one-kernel form runs as a single block (T <= 512),
+// it clears that many 32-bit words from ws.status on (the forward's status
+// word and counters) before anything else; the caller then skips its memset.
 cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* topk_idx,
                          const float* topk_w, int64_t T, bool check, cudaStream_t s,
-                         cudaEvent_t const* ev, int coop_max_blocks, bool watchdog_test = false);
+                         cudaEvent_t const* ev, int coop_max_blocks, bool watchdog_test = false,
+                         int64_t zero_words = 0);
 // Largest grid of the one-kernel routing that is co-resident on the current
 // device for E experts (0 if cooperative launch is unavailable).
 int route_fused_max_blocks(int E);

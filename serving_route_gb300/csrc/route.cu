@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kFusedTokens) route_fused_kernel(
     int32_t* __restrict__ pad_offsets, int32_t* __restrict__ mtile_expert,
     int32_t* __restrict__ total_mtiles, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
     int32_t* __restrict__ inv_pad, uint32_t* __restrict__ status, uint64_t wait_limit_ns,
-    int withhold) {
+    int withhold, uint32_t* __restrict__ zero_base, int zero_words) {
   extern __shared__ int32_t sm[];
   int32_t* wh = sm;                   // [warps][E]: per-warp counts, then running bases
   int32_t* bu = sm + kRouteWarps * E;  // [E]: expert totals, then this block's unpadded bases
@@ -238,6 +238,11 @@ __global__ void __launch_bounds__(kFusedTokens) route_fused_kernel(
   __shared__ int tot_u, tot_p, passed;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = (int)gridDim.x, b = (int)blockIdx.x;
+  // a one-block routing is the forward's first kernel and its only block:
+  // it clears the forward's status word and counters itself (the barrier
+  // below orders the clearing before this block's first status update)
+  if (nb == 1)
+    for (int i = tid; i < zero_words; i += blockDim.x) zero_base[i] = 0u;
   for (int i = tid; i < kRouteWarps * E; i += blockDim.x) wh[i] = 0;
   __syncthreads();
 
@@ -448,13 +453,19 @@ int route_fused_max_blocks(int E) {
 
 cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* topk_idx,
                          const float* topk_w, int64_t T, bool check, cudaStream_t s,
-                         cudaEvent_t const* ev, int coop_max_blocks, bool watchdog_test) {
+                         cudaEvent_t const* ev, int coop_max_blocks, bool watchdog_test,
+                         int64_t zero_words) {
   const int nb = (int)((T + kRouteTokens - 1) / kRouteTokens);
   const int E = L.E;
   const int max_mtiles = (int)(L.rows_alloc / 128);
   const int pad_rows = L.pad_rows > 0 ? L.pad_rows : 128;
   const int nb_fused = (int)((T + kFusedTokens - 1) / kFusedTokens);
-  if (ws.grid_sync && coop_max_blocks > 0 && nb_fused <= coop_max_blocks) {
+  const bool fused = ws.grid_sync && coop_max_blocks > 0 && nb_fused <= coop_max_blocks;
+  // only a one-block fused kernel clears the words itself; otherwise a memset
+  if (zero_words > 0 && !(fused && nb_fused == 1) &&
+      cudaMemsetAsync(ws.status, 0, (size_t)zero_words * 4, s) != cudaSuccess)
+    return cudaErrorUnknown;
+  if (fused) {
     if (ev) record_event(ev[0], s);
     cudaLaunchAttribute coop;
     coop.id = cudaLaunchAttributeCooperative;
@@ -465,7 +476,8 @@ cudaError_t launch_route(const Workspace& ws, const Layout& L, const int32_t* to
         ws.block_counts, ws.grid_sync, ws.counts, ws.offsets, ws.pad_offsets, ws.mtile_expert,
         ws.total_mtiles, ws.perm, ws.inv, ws.inv_pad, ws.status,
         watchdog_test ? (uint64_t)20000000ull : (uint64_t)kWaitLimitNs,
-        watchdog_test && nb_fused > 1 ? nb_fused - 1 : -1);
+        watchdog_test && nb_fused > 1 ? nb_fused - 1 : -1, ws.status,
+        nb_fused == 1 ? (int)zero_words : 0);
     if (ev) {  // the scan and scatter are inside the one kernel: zero-length spans
       record_event(ev[1], s);
       record_event(ev[2], s);
