@@ -48,10 +48,11 @@
 //    stores); an FC2 tile's producer waits for its m-tile's count before its
 //    first TMA load of hq.  Every CTA takes its FC1 units before its FC2
 //    units, so the waits always end (see the kernel's comment).
-//  * Combine folded into FC2 (opt-in, single CTA): the FC2 epilogue counts
-//    each stored row into its token's per-n-tile count and queues the pairs
-//    it completes for two extra warps, which combine them (bit-identical to
-//    the combine kernel; slower than it on the measured shapes).
+//  * Combine folded into FC2 (opt-in, single CTA; FOLD instantiations): the
+//    FC2 epilogue counts each stored row into its token's per-n-tile count
+//    and queues the pairs it completes for two extra warps, which combine
+//    them (bit-identical to the combine kernel; slower than it on the
+//    measured shapes).
 //  * Launched as a programmatic dependent: the barrier / TMEM prologue
 //    overlaps the previous kernel, the wait comes before the first global
 //    read.
@@ -64,12 +65,13 @@ namespace mm {
 
 constexpr int kEpiWarps = 8;                   // two per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
-// Single-CTA launches that store y (FC2, or the megakernel) carry two more
-// warps: the combine role, used when the combine is folded into FC2.
+// Single-CTA launches that store y (FC2, or the megakernel) with the combine
+// folded in are separate instantiations (FOLD) that carry two more warps:
+// the combine role.  Every other launch compiles none of it.
 constexpr int kCombineWarps = 2;
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool FOLD>
 struct Roles {
-  static constexpr bool kFold = !PAIR && (MODE == kModeY || MODE == kModeMega);
+  static constexpr bool kFold = FOLD && !PAIR && (MODE == kModeY || MODE == kModeMega);
   static constexpr int kThreads = mm::kThreads + (kFold ? 32 * kCombineWarps : 0);
 };
 constexpr int kCq = 256;  // the combine queue's slots (one per completed token n-tile)
@@ -185,8 +187,8 @@ __device__ __forceinline__ void fold_combine(const GemmArgs& gy, const int64_t (
 // taken by a running CTA before any FC2 unit, and FC2 tiles -- which wait
 // for their m-tile's fc1_done count -- never hold up an FC1 tile: with every
 // CTA resident the waits always end.
-template <int MODE, bool PAIR>
-__global__ void __launch_bounds__(Roles<MODE, PAIR>::kThreads, 1)
+template <int MODE, bool PAIR, bool FOLD>
+__global__ void __launch_bounds__(Roles<MODE, PAIR, FOLD>::kThreads, 1)
     fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmSfa,
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(Roles<MODE, PAIR>::kThreads, 1)
   // the folded combine's queue: epilogue warps -> combine role, one entry per
   // completed (token, n-tile); an entry is published by writing its slot's
   // mark (index + 1)
-  using R = Roles<MODE, PAIR>;
+  using R = Roles<MODE, PAIR, FOLD>;
   __shared__ int2 cq_item[R::kFold ? kCq : 1];
   __shared__ int cq_mark[R::kFold ? kCq : 1];
   __shared__ int cq_tail, cq_head, cq_freed, epi_done;
@@ -1001,9 +1003,9 @@ __global__ void __launch_bounds__(Roles<MODE, PAIR>::kThreads, 1)
   }
 }
 
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool FOLD = false>
 static cudaError_t set_attr() {
-  return cudaFuncSetAttribute(fp8_grouped_gemm_kernel<MODE, PAIR>,
+  return cudaFuncSetAttribute(fp8_grouped_gemm_kernel<MODE, PAIR, FOLD>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)StageCfg<PAIR>::kDynSmem);
 }
@@ -1019,6 +1021,8 @@ cudaError_t gemm_set_attributes() {
   if ((e = set_attr<kModeFused, true>()) != cudaSuccess) return e;
   if ((e = set_attr<kModeFusedGU, true>()) != cudaSuccess) return e;
   if ((e = set_attr<kModeMega, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<kModeY, false, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<kModeMega, false, true>()) != cudaSuccess) return e;
   return set_attr<kModeMega, true>();
 }
 
@@ -1041,7 +1045,7 @@ int gemm_max_pairs() {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fp8_grouped_gemm_kernel<kModeY, true>, &cfg) !=
+  if (cudaOccupancyMaxActiveClusters(&n, fp8_grouped_gemm_kernel<kModeY, true, false>, &cfg) !=
       cudaSuccess)
     return 0;
   return n;
@@ -1057,12 +1061,21 @@ static cudaError_t launch_mode(bool pair, const CUtensorMap* tmA, const CUtensor
                                const CUtensorMap* tmSfa2, const CUtensorMap* tmSfb2,
                                const CUtensorMap* tmY, const GemmArgs& g, const GemmArgs& g2,
                                int ctas, cudaStream_t s, bool pdl) {
+  // the combine folded into FC2 (single CTAs): the FC2 args carry its counters
+  const bool fold = !pair && (MODE == kModeY || MODE == kModeMega) &&
+                    (MODE == kModeMega ? g2.cmb_cnt : g.cmb_cnt) != nullptr;
+  if (fold) {
+    constexpr int M = (MODE == kModeY || MODE == kModeMega) ? MODE : kModeY;  // (others never fold)
+    return launch_k(fp8_grouped_gemm_kernel<M, false, true>, dim3(ctas),
+                    dim3(Roles<M, false, true>::kThreads), StageCfg<false>::kDynSmem, s, pdl, nullptr,
+                    *tmA, *tmB, *tmA, *tmA, *tmY, g, *tmA2, *tmB2, *tmA2, *tmA2, g2);
+  }
   if (!pair)
-    return launch_k(fp8_grouped_gemm_kernel<MODE, false>, dim3(ctas), dim3(Roles<MODE, false>::kThreads),
-                    StageCfg<false>::kDynSmem, s, pdl, nullptr, *tmA, *tmB, *tmA, *tmA, *tmY, g,
-                    *tmA2, *tmB2, *tmA2, *tmA2, g2);
+    return launch_k(fp8_grouped_gemm_kernel<MODE, false, false>, dim3(ctas),
+                    dim3(Roles<MODE, false, false>::kThreads), StageCfg<false>::kDynSmem, s, pdl,
+                    nullptr, *tmA, *tmB, *tmA, *tmA, *tmY, g, *tmA2, *tmB2, *tmA2, *tmA2, g2);
   const cudaLaunchAttribute cluster = pair_cluster_attr();
-  return launch_k(fp8_grouped_gemm_kernel<MODE, true>, dim3(ctas), dim3(Roles<MODE, true>::kThreads),
+  return launch_k(fp8_grouped_gemm_kernel<MODE, true, false>, dim3(ctas), dim3(Roles<MODE, true, false>::kThreads),
                   StageCfg<true>::kDynSmem, s, pdl, &cluster, *tmA, *tmB, *tmSfa, *tmSfb, *tmY, g,
                   *tmA2, *tmB2, *tmSfa2, *tmSfb2, g2);
 }
