@@ -38,7 +38,8 @@
 //    every fourth K block the A scale atom and the two B scale atoms built at
 //    bind time), one thread of warp 1 issues the scale copies (tcgen05.cp)
 //    and MMAs and probes the next stage while the current one computes,
-//    warps 2-9 the epilogue (two per TMEM lane quadrant).
+//    warps 2-9 the epilogue (two per TMEM lane quadrant); the FOLD
+//    instantiations add warps 10-11, the combine role (384 threads).
 //  * Epilogues: FC2 -> BF16 y (TMA stores); FC1 unfused -> BF16 gate||up;
 //    FC1 fused -> BF16-rounded gate/up, SwiGLU, 1x128 (or MXFP8 1x32)
 //    re-quantisation to E4M3 + E8M0 atoms (bit-equal to the unfused path,
