@@ -326,14 +326,16 @@ MOE_API moe_status moe_stage_inputs(moe_handle* h, uint16_t* d_out);
  *   d_topk_w    float [num_tokens, K]; ignored (may be NaN) on masked slots.
  *   num_tokens  0..max_rows.  0 returns MOE_OK and writes nothing.
  * Writes d_out[0:num_tokens, :] of the staged output.  Route errors set the
- * device status word; the output is then undefined.  Enqueues a status reset
- * and four to eight kernels (moe_forward_plan says which): the routing as one
- * cooperative kernel (histogram, one grid-wide barrier, scan, stable scatter)
- * when its ceil(num_tokens/512) blocks can all be resident and no SM budget
- * is set, else as three kernels (histogram, scan, scatter) with the same
- * results; quant_dispatch; FC1 and FC2 as one persistent launch or two (see
+ * device status word; the output is then undefined.  Enqueues three to
+ * seven kernels (moe_forward_plan says which): the routing as one cooperative
+ * kernel (histogram, one grid-wide barrier, scan, stable scatter) when its
+ * ceil(num_tokens/512) blocks can all be resident and no SM budget is set,
+ * else as three kernels (histogram, scan, scatter) with the same results;
+ * quant_dispatch; FC1 and FC2 as one persistent launch or two (see
  * MOE_FLAG_GEMMS_ONE_LAUNCH), with swiglu_quant between them on the unfused
- * path; combine.  Every kernel after the first is launched as a programmatic
+ * path; combine, unless MOE_FLAG_COMBINE_IN_FC2 folds it into FC2.  The
+ * status word and the forward's counters are reset first: by a memset, or by
+ * the routing kernel itself when it is one block (at most 512 tokens).  Every kernel after the first is launched as a programmatic
  * dependent of the one before (it may start while its predecessor drains and
  * waits for it before touching the forward's data).
  */
