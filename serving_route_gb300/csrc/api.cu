@@ -91,7 +91,8 @@ bool encode_bf16_store_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t r
 // box_rows < 128: the first box_rows rows of a block (the token tiles of the
 // token-as-N GEMMs).
 bool encode_blocked_map(CUtensorMap* m, const void* base, uint64_t kblocks, uint64_t row_blocks,
-                        uint32_t box_rows = 128) {
+                        uint32_t box_rows = 128,
+                        CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {128, kblocks * 128, row_blocks};
@@ -100,7 +101,7 @@ bool encode_blocked_map(CUtensorMap* m, const void* base, uint64_t kblocks, uint
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Scale atoms [n_atoms][512 B] as a 2-D uint32 tensor [n_atoms, 128]; one
@@ -474,8 +475,12 @@ moe_status moe_bind_weights(moe_handle* h, const uint8_t* d_w1, const float* d_w
       cudaStreamSynchronize(stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (st & MOE_DEV_BAD_SCALE) return MOE_ERR_BAD_SCALE;
-  if (!encode_blocked_map(&h->tm_w1, h->wst.w1, L.H / 128, (uint64_t)L.E * (2 * L.I / 128)) ||
-      !encode_blocked_map(&h->tm_w2, h->wst.w2, L.I / 128, (uint64_t)L.E * (L.H / 128)))
+  // weight boxes are contiguous 16 KB runs read once per tile: no L2
+  // promotion (decode T = 256: 1.6563 -> 1.6544 ms against 256-byte promotion)
+  if (!encode_blocked_map(&h->tm_w1, h->wst.w1, L.H / 128, (uint64_t)L.E * (2 * L.I / 128), 128,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
+      !encode_blocked_map(&h->tm_w2, h->wst.w2, L.I / 128, (uint64_t)L.E * (L.H / 128), 128,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return MOE_ERR_CUDA;
   h->bound = true;
   return MOE_OK;
