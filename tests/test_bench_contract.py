@@ -52,6 +52,7 @@ def test_main_line(fmt):
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     assert {"median", "p10", "p90"} <= set(d["step_ms"])
     assert d["l2_warm"]["ms_per_step"] > 0 and d["l2_warm"]["steps"] >= 1
+    assert "idle" in d["config"]["timing"]          # the settled power state is stated
     assert d["config"]["format"].startswith("MXFP8" if fmt == "mxfp8" else "E4M3")
     assert ("per-tensor" in d["config"]["format"]) == (fmt == "per_tensor")
     lr = d["layer_roofline"]
