@@ -327,7 +327,7 @@ MOE_API moe_status moe_stage_inputs(moe_handle* h, uint16_t* d_out);
  *   num_tokens  0..max_rows.  0 returns MOE_OK and writes nothing.
  * Writes d_out[0:num_tokens, :] of the staged output.  Route errors set the
  * device status word; the output is then undefined.  Enqueues three to
- * seven kernels (moe_forward_plan says which): the routing as one cooperative
+ * eight kernels (moe_forward_plan says which): the routing as one cooperative
  * kernel (histogram, one grid-wide barrier, scan, stable scatter) when its
  * ceil(num_tokens/512) blocks can all be resident and no SM budget is set,
  * else as three kernels (histogram, scan, scatter) with the same results;
