@@ -168,10 +168,20 @@ __global__ void __launch_bounds__(kRouteTokens) route_scatter_kernel(
   int32_t* my = wh + warp * E;
   const int32_t* bu = base_u + (int64_t)blockIdx.x * E;
   const int32_t* bp = base_p + (int64_t)blockIdx.x * E;
-  for (int64_t rb = r0; rb < r1; rb += 32) {
+  // the warp's route ids, loaded together (at most K <= 8 rounds of 32)
+  int idv[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t r = r0 + j * 32 + lane;
+    idv[j] = r < r1 ? idx[r] : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t rb = r0 + j * 32;
+    if (rb >= r1) break;  // the same for the whole warp
     const int64_t r = rb + lane;
     const bool in = r < r1;
-    const int id = in ? idx[r] : -1;
+    const int id = idv[j];
     const bool act = in && id >= 0 && id < E;
     const unsigned amask = __ballot_sync(0xFFFFFFFFu, act);
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, act ? id : -1) & amask;
@@ -290,6 +300,19 @@ __global__ void __launch_bounds__(kFusedTokens) route_fused_kernel(
     }
   }
 
+  // The flat route ids of this warp's phase-3 routes (tokens [t0, t0 + 32),
+  // at most K <= 8 rounds of 32), loaded now so that their latency overlaps
+  // the barrier; idx is an input of the forward, no kernel writes it.
+  const int64_t t0 = (int64_t)b * kFusedTokens + warp * 32;
+  const int64_t r0 = t0 * K;
+  const int64_t r1 = min((int64_t)T, t0 + 32) * K;
+  int idv[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t r = r0 + j * 32 + lane;
+    idv[j] = r < r1 ? idx[r] : -1;
+  }
+
   // ---- grid barrier
   __syncthreads();
   if (one) {
@@ -315,9 +338,9 @@ __global__ void __launch_bounds__(kFusedTokens) route_fused_kernel(
     // No routing this forward (the status says why): this block's routes are
     // marked unrouted, so every later kernel skips them; total_mtiles keeps
     // the 0 written before the forward unless block 0 got through.
-    const int64_t r0 = (int64_t)b * kFusedTokens * K;
-    const int64_t r1 = min((int64_t)T, (int64_t)(b + 1) * kFusedTokens) * K;
-    for (int64_t r = r0 + tid; r < r1; r += blockDim.x) {
+    const int64_t q0 = (int64_t)b * kFusedTokens * K;
+    const int64_t q1 = min((int64_t)T, (int64_t)(b + 1) * kFusedTokens) * K;
+    for (int64_t r = q0 + tid; r < q1; r += blockDim.x) {
       inv[r] = -1;
       inv_pad[r] = -1;
     }
@@ -401,15 +424,15 @@ __global__ void __launch_bounds__(kFusedTokens) route_fused_kernel(
   }
   __syncthreads();
 
-  // ---- phase 3 (as route_scatter)
+  // ---- phase 3 (as route_scatter; the ids were loaded before the barrier)
   int32_t* my = wh + warp * E;
-  const int64_t t0 = (int64_t)b * kFusedTokens + warp * 32;
-  const int64_t r0 = t0 * K;
-  const int64_t r1 = min((int64_t)T, t0 + 32) * K;
-  for (int64_t rb = r0; rb < r1; rb += 32) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t rb = r0 + j * 32;
+    if (rb >= r1) break;  // the same for the whole warp
     const int64_t r = rb + lane;
     const bool in = r < r1;
-    const int id = in ? idx[r] : -1;
+    const int id = idv[j];
     const bool act = in && id >= 0 && id < E;
     const unsigned amask = __ballot_sync(0xFFFFFFFFu, act);
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, act ? id : -1) & amask;
